@@ -1,0 +1,210 @@
+// Oracle for the small-M affine-quantized matrix multiply
+//     Y[M,N] = X[M,K] · dequant(Wq, scales, biases)[N,K]^T
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+// definition that the CUDA library is checked against.  Only the tests, the
+// smoke check and the benchmark's CPU-baseline leg may build, load or call it.
+// It shares no code, header, table or helper with the CUDA library, and the
+// library never calls it: there is no CPU fallback anywhere in the product.
+//
+// Arithmetic: IEEE binary64, single thread, every sum over k in ascending
+// order, compiled with -O2 -ffp-contract=off (no fused multiply-add, no
+// fast-math).
+//
+// What is computed, and where the pages say so:
+//  * Affine group quantization, w = scale * q + bias, one fp16 scale and one
+//    fp16 bias per group of `group_size` weights along K.
+//      - "MLX quantized_matmul small-M verify kernels", fact "Fix family 1"
+//        (the affine mode of qmv_wide) and fact "Group-size mechanism" (4 B of
+//        scale+bias per group: 2 B fp16 scale + 2 B fp16 bias).
+//  * W is stored [N,K] and the product is X · W^T:
+//      - same page, fact "Microbench": (M,5120)@(17408,5120)^T.
+//  * bf16 activations:
+//      - same page, facts "qmv_wide speedup" ("bf16 act") and "Fix family 2"
+//        ("load A straight from device bf16").
+//  * Packing of q into 32-bit words.  The pages print no bit layout.  The
+//    reading adopted is the plainest one: little-endian uint32 words, rows of
+//    W contiguous along K, codes low-bits-first inside each word, i.e. for
+//    b-bit codes word j of row n holds k = j*(32/b) ... j*(32/b) + 32/b - 1 and
+//    code k sits at bit offset b * (k mod (32/b)).
+//  * Unsigned codes 0 .. 2^b - 1; "affine" adds the bias, there is no other
+//    zero point.
+//
+// Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
+// shapes, closed forms (all-zero codes, one-hot X, X = 1, saturated codes),
+// the scale=1/bias=0 special case against numpy's integer matmul, linearity,
+// row-permutation and batch invariance, and the two documented pack words.
+
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+namespace {
+
+// binary16 -> binary64, written out from the IEEE 754 binary16 format:
+// 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+double half_bits_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int expo = (h >> 10) & 0x1F;
+  const int frac = h & 0x3FF;
+  double mag;
+  if (expo == 0) {
+    mag = std::ldexp(static_cast<double>(frac), -24);              // subnormal: frac * 2^-24
+  } else if (expo == 31) {
+    mag = frac == 0 ? INFINITY : NAN;
+  } else {
+    mag = std::ldexp(static_cast<double>(1024 + frac), expo - 25); // (1 + frac/1024) * 2^(expo-15)
+  }
+  return sign ? -mag : mag;
+}
+
+// bfloat16 -> binary64: bfloat16 is the upper half of a binary32 pattern
+// (1 sign bit, 8 exponent bits with bias 127, 7 fraction bits).
+double bf16_bits_to_double(uint16_t b) {
+  const int sign = (b >> 15) & 1;
+  const int expo = (b >> 7) & 0xFF;
+  const int frac = b & 0x7F;
+  double mag;
+  if (expo == 0) {
+    mag = std::ldexp(static_cast<double>(frac), -133);              // frac * 2^-7 * 2^-126
+  } else if (expo == 255) {
+    mag = frac == 0 ? INFINITY : NAN;
+  } else {
+    mag = std::ldexp(static_cast<double>(128 + frac), expo - 134);  // (1 + frac/128) * 2^(expo-127)
+  }
+  return sign ? -mag : mag;
+}
+
+bool bits_ok(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+
+// Code k of row n, read straight from the packed words.
+inline unsigned code_at(const uint32_t* Wq, int64_t words_per_row, int64_t n, int64_t k, int bits) {
+  const int64_t per_word = 32 / bits;
+  const uint32_t word = Wq[n * words_per_row + k / per_word];
+  const unsigned shift = static_cast<unsigned>(bits * (k % per_word));
+  const uint32_t mask = (1u << bits) - 1u;
+  return (word >> shift) & mask;
+}
+
+// Dequantized weight w[n,k] = scale[n, k/g] * q[n,k] + bias[n, k/g].
+inline double weight_at(const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
+                        int64_t K, int bits, int64_t g, int64_t n, int64_t k) {
+  const int64_t words_per_row = K * bits / 32;
+  const int64_t groups = K / g;
+  const double s = half_bits_to_double(S[n * groups + k / g]);
+  const double b = half_bits_to_double(B[n * groups + k / g]);
+  const double q = static_cast<double>(code_at(Wq, words_per_row, n, k, bits));
+  return s * q + b;
+}
+
+int check_shape(int64_t M, int64_t N, int64_t K, int bits, int64_t g) {
+  if (M < 0 || N < 0 || K < 0) return 2;
+  if (!bits_ok(bits)) return 3;
+  if (g <= 0) return 3;
+  if (K % g != 0) return 2;
+  if ((K * bits) % 32 != 0) return 2;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+double oracle_half_to_double(uint16_t h) { return half_bits_to_double(h); }
+double oracle_bf16_to_double(uint16_t b) { return bf16_bits_to_double(b); }
+
+// Pack codes q[N,K] (one code per byte, each < 2^bits) into words Wq[N, K*bits/32].
+// Returns 0, or non-zero for an unsupported bit width / shape / out-of-range code.
+int oracle_pack(const uint8_t* q, int64_t N, int64_t K, int bits, uint32_t* Wq) {
+  if (!bits_ok(bits) || N < 0 || K < 0 || (K * bits) % 32 != 0) return 2;
+  const int64_t per_word = 32 / bits;
+  const int64_t words_per_row = K / per_word;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t j = 0; j < words_per_row; ++j) {
+      uint32_t word = 0;
+      for (int64_t i = 0; i < per_word; ++i) {
+        const uint32_t code = q[n * K + j * per_word + i];
+        if (code >> bits) return 3;
+        word |= code << (bits * i);
+      }
+      Wq[n * words_per_row + j] = word;
+    }
+  }
+  return 0;
+}
+
+// Inverse of oracle_pack.
+int oracle_unpack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint8_t* q) {
+  if (!bits_ok(bits) || N < 0 || K < 0 || (K * bits) % 32 != 0) return 2;
+  const int64_t words_per_row = K * bits / 32;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k)
+      q[n * K + k] = static_cast<uint8_t>(code_at(Wq, words_per_row, n, k, bits));
+  return 0;
+}
+
+// Full product.  X: bf16 bit patterns [M,K]; Wq: packed [N, K*bits/32];
+// S, B: fp16 bit patterns [N, K/g].  Writes Y[M,N] = sum_k x*w and
+// A[M,N] = sum_k |x*w| (the scale the tolerance is stated against), both fp64.
+// A may be null.  Each row of W is dequantized once into fp64 and reused for
+// all M rows of X; every sum still runs over k in ascending order.
+int oracle_qmm(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
+               int64_t M, int64_t N, int64_t K, int bits, int64_t g, double* Y, double* A) {
+  const int rc = check_shape(M, N, K, bits, g);
+  if (rc) return rc;
+  std::vector<double> x(static_cast<size_t>(M * K));
+  for (int64_t i = 0; i < M * K; ++i) x[i] = bf16_bits_to_double(X[i]);
+  std::vector<double> w(static_cast<size_t>(K));
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t k = 0; k < K; ++k) w[k] = weight_at(Wq, S, B, K, bits, g, n, k);
+    for (int64_t m = 0; m < M; ++m) {
+      const double* xm = x.data() + m * K;
+      double y = 0.0, a = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = xm[k] * w[k];
+        y += p;
+        a += std::fabs(p);
+      }
+      Y[m * N + n] = y;
+      if (A) A[m * N + n] = a;
+    }
+  }
+  return 0;
+}
+
+// The same definition evaluated only at the listed (m, n) output positions,
+// for spot checks of full-size problems.
+int oracle_qmm_sampled(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
+                       int64_t M, int64_t N, int64_t K, int bits, int64_t g,
+                       const int64_t* ms, const int64_t* ns, int64_t count, double* y_out, double* a_out) {
+  const int rc = check_shape(M, N, K, bits, g);
+  if (rc) return rc;
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t m = ms[i], n = ns[i];
+    if (m < 0 || m >= M || n < 0 || n >= N) return 2;
+    double y = 0.0, a = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double x = bf16_bits_to_double(X[m * K + k]);
+      const double w = weight_at(Wq, S, B, K, bits, g, n, k);
+      const double p = x * w;
+      y += p;
+      a += std::fabs(p);
+    }
+    y_out[i] = y;
+    if (a_out) a_out[i] = a;
+  }
+  return 0;
+}
+
+// Dequantized weight matrix W[N,K] in fp64 (used by closed-form pins).
+int oracle_dequant(const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
+                   int64_t N, int64_t K, int bits, int64_t g, double* W) {
+  const int rc = check_shape(0, N, K, bits, g);
+  if (rc) return rc;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k)
+      W[n * K + k] = weight_at(Wq, S, B, K, bits, g, n, k);
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+"""Seeded synthetic inputs for the small-M affine-quantized matmul.
+
+This module only draws random numbers and rounds them to their storage
+formats (fp16 for scales and biases, bf16 for activations).  It holds none of
+the method's arithmetic: it does not pack, dequantize or multiply.  Both the
+CUDA path and the CPU oracle take their inputs from here and nowhere else.
+
+Recipe (one numpy PCG64 stream per tensor, keyed by ``(seed, stream)``):
+
+* codes ``q ~ Uniform{0 .. 2^bits - 1}``, uint8 ``[N, K]``;
+* ``scale = fp16(0.002 * |N(0,1)| + 1e-4)`` per (row, group);
+* ``bias  = fp16(-(2^bits - 1)/2 * scale)``, i.e. ``-7.5 * scale`` at 4 bits
+  and ``-1.5 * scale`` at 2 bits (the scale is taken after its fp16 rounding);
+* ``X = bf16(N(0,1))`` drawn for 16 rows; an M-row problem uses the first M
+  rows, so every M of a sweep sees the same leading rows.
+
+Rounding to fp16 is numpy's (round to nearest even); rounding binary32 to
+bf16 is round to nearest even on the bit pattern.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+MAX_ROWS = 16
+
+STREAM_CODES = 0
+STREAM_SCALES = 1
+STREAM_X = 2
+
+
+def rng_for(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), int(stream)])))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round binary32 values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to binary32 (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f64_to_fp16_bits(a: np.ndarray) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+@dataclass
+class Problem:
+    """One weight matrix with its metadata and 16 rows of activations.
+
+    ``q``: uint8 codes [N, K]; ``scales``/``biases``: fp16 bit patterns
+    [N, K/group_size]; ``x``: bf16 bit patterns [16, K].
+    """
+
+    N: int
+    K: int
+    bits: int
+    group_size: int
+    q: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    x: np.ndarray
+    seed: int
+
+    def x_rows(self, M: int) -> np.ndarray:
+        return np.ascontiguousarray(self.x[:M])
+
+
+def make_codes(seed: int, N: int, K: int, bits: int) -> np.ndarray:
+    return rng_for(seed, STREAM_CODES).integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+
+
+def make_scales_biases(seed: int, N: int, groups: int, bits: int):
+    z = rng_for(seed, STREAM_SCALES).standard_normal(size=(N, groups))
+    scale_bits = f64_to_fp16_bits(0.002 * np.abs(z) + 1e-4)
+    scale = scale_bits.view(np.float16).astype(np.float64)
+    bias_bits = f64_to_fp16_bits(-((1 << bits) - 1) / 2.0 * scale)
+    return scale_bits, bias_bits
+
+
+def make_x(seed: int, K: int, rows: int = MAX_ROWS) -> np.ndarray:
+    z = rng_for(seed, STREAM_X).standard_normal(size=(rows, K), dtype=np.float32)
+    return f32_to_bf16_bits(z)
+
+
+def make_problem(seed: int, N: int, K: int, bits: int, group_size: int, rows: int = MAX_ROWS) -> Problem:
+    if K % group_size:
+        raise ValueError("K must be a multiple of group_size")
+    groups = K // group_size
+    q = make_codes(seed, N, K, bits)
+    scales, biases = make_scales_biases(seed, N, groups, bits)
+    x = make_x(seed, K, rows)
+    return Problem(N=N, K=K, bits=bits, group_size=group_size, q=q, scales=scales, biases=biases, x=x, seed=seed)

@@ -1,0 +1,105 @@
+"""Named synthetic workloads and their algorithmic byte counts.
+
+Every workload is a set of (N, K) weight shapes, a bit width, a group size and
+the activation row counts M it is run at.  Shapes stand in for the model
+layers the pages benchmark on; no model weights are involved.
+
+Algorithmic bytes of one call (moved once, whatever M is):
+
+    weight bytes   W_B    = N * K * bits / 8
+    metadata bytes Meta_B = N * (K / g) * 4      (fp16 scale + fp16 bias)
+
+The "total" count adds the activations (2*M*K) and the output (2 or 4 * M*N).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+@dataclass(frozen=True)
+class Shape:
+    name: str
+    N: int
+    K: int
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    shapes: tuple
+    bits: int
+    group_size: int
+    ms: tuple
+    seed_base: int
+    layers: int = 1
+    note: str = ""
+    variants: tuple = field(default_factory=tuple)  # extra (bits, group_size) pairs run on the same shapes
+
+
+def weight_bytes(N: int, K: int, bits: int) -> int:
+    return N * K * bits // 8
+
+
+def meta_bytes(N: int, K: int, group_size: int) -> int:
+    return N * (K // group_size) * 4
+
+
+def call_bytes(N: int, K: int, bits: int, group_size: int) -> int:
+    """Weight + metadata bytes one call has to stream (the roofline numerator)."""
+    return weight_bytes(N, K, bits) + meta_bytes(N, K, group_size)
+
+
+def total_bytes(M: int, N: int, K: int, bits: int, group_size: int, out_bytes: int = 2) -> int:
+    return call_bytes(N, K, bits, group_size) + 2 * M * K + out_bytes * M * N
+
+
+SINGLE_LAYER = Workload(
+    name="single_layer_1024x1024_4b_g64",
+    shapes=(Shape("layer", 1024, 1024),),
+    bits=4, group_size=64, ms=(4,), seed_base=1000,
+    note="one 1024x1024 layer at M=4; small enough for the full oracle in seconds",
+)
+
+M_SWEEP = Workload(
+    name="m_sweep_5120x5120_4b_g64",
+    shapes=(Shape("square", 5120, 5120),),
+    bits=4, group_size=64, ms=tuple(range(1, 17)), seed_base=2000,
+    note="M = 1..16 on one 5120x5120 layer",
+)
+
+DENSE_27B_LAYER = Workload(
+    name="dense27b_layer_4b_g64",
+    shapes=(Shape("qkv", 7168, 5120), Shape("o", 5120, 5120),
+            Shape("gate_up", 34816, 5120), Shape("down", 5120, 17408)),
+    bits=4, group_size=64, ms=(1, 2, 3, 4, 5, 8), seed_base=3000,
+    note="projections of a 27B-class dense decoder layer",
+)
+
+GROUP_BIT_SWEEP = Workload(
+    name="group_bit_sweep_8192x8192",
+    shapes=(Shape("square", 8192, 8192),),
+    bits=4, group_size=64, ms=tuple(range(1, 17)), seed_base=4000,
+    variants=((4, 32), (4, 64), (4, 128), (2, 64)),
+    note="4-bit at g32/g64/g128 and 2-bit at g64 on one 8192x8192 layer",
+)
+
+VERIFY_STEP = Workload(
+    name="verify_step_36x4096_4b_g64",
+    shapes=(Shape("qkv", 6144, 4096), Shape("o", 4096, 4096),
+            Shape("gate_up", 24576, 4096), Shape("down", 4096, 12288)),
+    bits=4, group_size=64, ms=tuple(range(1, 9)), seed_base=5000, layers=36,
+    note="36 layers x 4 projections of a 4096-hidden dense stack, back to back on one stream",
+)
+
+ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP)
+BY_NAME = {w.name: w for w in ALL}
+
+
+def shape_seed(workload: Workload, shape_index: int, layer: int = 0, bits: int | None = None,
+               group_size: int | None = None) -> int:
+    """Seed of one weight matrix: base + shape index + 4*layer, plus 100 per
+    (bits, group) variant index."""
+    seed = workload.seed_base + shape_index + 4 * layer
+    if bits is not None and group_size is not None and workload.variants:
+        seed += 100 * workload.variants.index((bits, group_size))
+    return seed

@@ -1,0 +1,235 @@
+"""Pins that tie the fp64 oracle to things other than itself.
+
+Each ``pin_*`` takes an ``OracleLib`` and raises ``AssertionError`` when the
+oracle disagrees with what the mathematics or the stated layout fixes:
+
+* exhaustive decoders: every fp16 / bf16 bit pattern against numpy's own
+  float16 / float32 conversion;
+* the documented pack words (4-bit 0..7 -> 0x76543210, 2-bit 0,1,2,3 repeated
+  -> 0xE4E4E4E4) and pack/unpack round trips;
+* exact rational brute force (``fractions.Fraction``) on tiny shapes, written
+  here from the definition w = s*q + b, y = sum_k x*w, with the codes taken
+  from the generator rather than from the packed words;
+* closed forms: all-zero codes, one-hot X, X = 1, saturated codes;
+* the scale = 1 / bias = 0 special case against numpy's float64 matmul;
+* invariants: batch invariance, exact scaling by 2, additivity over disjoint
+  supports, permutation of the rows of W;
+* the sampled entry point against the full one.
+
+The same functions run against deliberately broken builds of the oracle in
+``test_oracle_mutants.py``, which checks that each planted mistake trips at
+least one pin.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+
+from quantized_matmul_speculative_gb300 import synth
+
+BF16_ONE = 0x3F80
+FP16_ONE = 0x3C00
+
+
+# ---------------------------------------------------------------- helpers
+def frac_half(bits: int) -> Fraction:
+    return Fraction(float(np.array([bits], dtype=np.uint16).view(np.float16)[0]))
+
+
+def frac_bf16(bits: int) -> Fraction:
+    return Fraction(float(synth.bf16_bits_to_f32(np.array([bits], dtype=np.uint16))[0]))
+
+
+def f64_half(a):
+    return np.asarray(a, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def f64_bf16(a):
+    return synth.bf16_bits_to_f32(np.asarray(a, dtype=np.uint16)).astype(np.float64)
+
+
+def close(y, ref, a, rel=1e-12, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    a = np.asarray(a, dtype=np.float64)
+    bad = np.abs(y - ref) > rel * np.abs(a) + 1e-300
+    assert not bad.any(), f"{what}: {int(bad.sum())} mismatches, first at {np.argwhere(bad)[0]}: {y[bad][0]} vs {ref[bad][0]}"
+
+
+TINY_CASES = [
+    # (M, N, K, bits, g)
+    (3, 5, 64, 4, 32),
+    (2, 4, 128, 4, 64),
+    (1, 3, 256, 4, 128),
+    (3, 4, 64, 2, 32),
+    (2, 3, 128, 2, 64),
+    (2, 2, 256, 2, 128),
+]
+
+
+# ---------------------------------------------------------------- pins
+def pin_decoders(lib):
+    # every fp16 pattern against numpy's float16
+    for h in range(0, 1 << 16, 1):
+        ref = float(np.array([h], dtype=np.uint16).view(np.float16)[0])
+        got = lib.half_to_double(h)
+        if np.isnan(ref):
+            assert np.isnan(got), f"fp16 {h:#06x}"
+        else:
+            assert got == ref, f"fp16 {h:#06x}: {got} vs {ref}"
+    # every bf16 pattern against float32 widening
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    refs = synth.bf16_bits_to_f32(pats).astype(np.float64)
+    for h in range(0, 1 << 16, 1):
+        got = lib.bf16_to_double(h)
+        ref = refs[h]
+        if np.isnan(ref):
+            assert np.isnan(got), f"bf16 {h:#06x}"
+        else:
+            assert got == ref, f"bf16 {h:#06x}: {got} vs {ref}"
+
+
+def pin_pack_words(lib):
+    q4 = np.arange(8, dtype=np.uint8).reshape(1, 8)
+    assert int(lib.pack(q4, 4)[0, 0]) == 0x76543210
+    q2 = np.tile(np.arange(4, dtype=np.uint8), 4).reshape(1, 16)
+    assert int(lib.pack(q2, 2)[0, 0]) == 0xE4E4E4E4
+    q8 = np.array([[1, 2, 3, 4]], dtype=np.uint8)
+    assert int(lib.pack(q8, 8)[0, 0]) == 0x04030201
+    rng = np.random.default_rng(7)
+    for bits in (2, 4, 8):
+        q = rng.integers(0, 1 << bits, size=(5, 96), dtype=np.uint8)
+        wq = lib.pack(q, bits)
+        assert wq.shape == (5, 96 * bits // 32)
+        assert np.array_equal(lib.unpack(wq, 96, bits), q)
+        # the row-major word order: row 1 starts right after row 0
+        flat = lib.pack(q.reshape(1, -1)[:, : 96], bits)
+        assert np.array_equal(flat[0], wq[0])
+
+
+def exact_product(p: synth.Problem, M: int):
+    """y[m][n] and a[m][n] as Fractions, from the codes, fp16 and bf16 values."""
+    g = p.group_size
+    s = [[frac_half(v) for v in row] for row in p.scales]
+    b = [[frac_half(v) for v in row] for row in p.biases]
+    x = [[frac_bf16(v) for v in row] for row in p.x[:M]]
+    ys, as_ = [], []
+    for m in range(M):
+        yrow, arow = [], []
+        for n in range(p.N):
+            acc = Fraction(0)
+            mag = Fraction(0)
+            for k in range(p.K):
+                w = s[n][k // g] * int(p.q[n, k]) + b[n][k // g]
+                t = x[m][k] * w
+                acc += t
+                mag += abs(t)
+            yrow.append(acc)
+            arow.append(mag)
+        ys.append(yrow)
+        as_.append(arow)
+    return ys, as_
+
+
+def pin_brute_force(lib):
+    for i, (M, N, K, bits, g) in enumerate(TINY_CASES):
+        p = synth.make_problem(900 + i, N, K, bits, g, rows=M)
+        wq = lib.pack(p.q, bits)
+        y, a = lib.qmm(p.x_rows(M), wq, p.scales, p.biases, bits, g)
+        ye, ae = exact_product(p, M)
+        for m in range(M):
+            for n in range(N):
+                err = abs(Fraction(float(y[m, n])) - ye[m][n])
+                assert err <= Fraction(1, 10**12) * ae[m][n], f"case {i} y[{m},{n}] off by {float(err)}"
+                assert abs(Fraction(float(a[m, n])) - ae[m][n]) <= Fraction(1, 10**12) * ae[m][n], f"case {i} a[{m},{n}]"
+
+
+def pin_closed_forms(lib):
+    for bits, g in ((4, 64), (4, 32), (2, 64), (4, 128)):
+        M, N, K = 3, 6, 4 * g
+        G = K // g
+        p = synth.make_problem(950 + bits * 10 + g, N, K, bits, g, rows=M)
+        x = f64_bf16(p.x_rows(M))
+        s = f64_half(p.scales)
+        b = f64_half(p.biases)
+        xs = x.reshape(M, G, g).sum(axis=2)  # per-group sums of x
+        # all codes zero: y = sum_g b[n,g] * sum_{k in g} x[m,k]
+        q0 = np.zeros_like(p.q)
+        y, a = lib.qmm(p.x_rows(M), lib.pack(q0, bits), p.scales, p.biases, bits, g)
+        close(y, xs @ b.T, a, 1e-12, "all-zero codes")
+        # saturated codes: w = (2^bits-1) s + b
+        qs = np.full_like(p.q, (1 << bits) - 1)
+        y, a = lib.qmm(p.x_rows(M), lib.pack(qs, bits), p.scales, p.biases, bits, g)
+        close(y, xs @ (((1 << bits) - 1) * s + b).T, a, 1e-12, "saturated codes")
+        # one-hot X picks column k0 of dequant(W)
+        for k0 in (0, 1, g - 1, g, K - 1):
+            xo = np.zeros((1, K), dtype=np.uint16)
+            xo[0, k0] = BF16_ONE
+            y, _ = lib.qmm(xo, lib.pack(p.q, bits), p.scales, p.biases, bits, g)
+            col = s[:, k0 // g] * p.q[:, k0].astype(np.float64) + b[:, k0 // g]
+            assert np.array_equal(y[0], col), f"one-hot k0={k0}"
+        # X = 1: y = sum_k w[n,k] = sum_g (s * sum q + g * b)
+        x1 = np.full((2, K), BF16_ONE, dtype=np.uint16)
+        y, a = lib.qmm(x1, lib.pack(p.q, bits), p.scales, p.biases, bits, g)
+        qsum = p.q.astype(np.float64).reshape(N, G, g).sum(axis=2)
+        ref = (s * qsum + g * b).sum(axis=1)
+        close(y[0], ref, a[0], 1e-12, "x = 1")
+        close(y[1], ref, a[1], 1e-12, "x = 1")
+
+
+def pin_integer_special_case(lib):
+    # scale 1, bias 0: y = X @ Q^T, an integer-matrix times bf16 product
+    for bits, g in ((4, 64), (2, 32)):
+        M, N, K = 4, 7, 256
+        p = synth.make_problem(970 + bits, N, K, bits, g, rows=M)
+        ones = np.full(p.scales.shape, FP16_ONE, dtype=np.uint16)
+        zeros = np.zeros(p.biases.shape, dtype=np.uint16)
+        y, a = lib.qmm(p.x_rows(M), lib.pack(p.q, bits), ones, zeros, bits, g)
+        ref = f64_bf16(p.x_rows(M)) @ p.q.astype(np.float64).T
+        close(y, ref, a, 1e-12, "integer special case")
+
+
+def pin_invariants(lib):
+    M, N, K, bits, g = 5, 9, 320, 4, 64
+    p = synth.make_problem(990, N, K, bits, g, rows=M)
+    wq = lib.pack(p.q, bits)
+    y, a = lib.qmm(p.x_rows(M), wq, p.scales, p.biases, bits, g)
+    # batch invariance: row m of an M-row call equals the 1-row call on that row
+    for m in range(M):
+        y1, _ = lib.qmm(p.x[m:m + 1], wq, p.scales, p.biases, bits, g)
+        assert np.array_equal(y1[0], y[m]), f"batch invariance row {m}"
+    # scaling X by 2 is exact in bf16 and in the product
+    x2 = (f64_bf16(p.x_rows(M)) * 2).astype(np.float32)
+    y2, _ = lib.qmm(synth.f32_to_bf16_bits(x2), wq, p.scales, p.biases, bits, g)
+    assert np.array_equal(y2, 2 * y), "scaling by 2"
+    # additivity over disjoint supports
+    xe = p.x_rows(M).copy()
+    xe[:, 1::2] = 0
+    xo = p.x_rows(M).copy()
+    xo[:, 0::2] = 0
+    ye, _ = lib.qmm(xe, wq, p.scales, p.biases, bits, g)
+    yo, _ = lib.qmm(xo, wq, p.scales, p.biases, bits, g)
+    close(ye + yo, y, a, 1e-13, "additivity")
+    # permuting the rows of W permutes the columns of Y
+    perm = np.random.default_rng(3).permutation(N)
+    yp, _ = lib.qmm(p.x_rows(M), lib.pack(p.q[perm], bits), p.scales[perm], p.biases[perm], bits, g)
+    assert np.array_equal(yp, y[:, perm]), "row permutation"
+
+
+def pin_sampled(lib):
+    M, N, K, bits, g = 4, 11, 192, 2, 64
+    p = synth.make_problem(995, N, K, bits, g, rows=M)
+    wq = lib.pack(p.q, bits)
+    y, a = lib.qmm(p.x_rows(M), wq, p.scales, p.biases, bits, g)
+    ms = np.array([0, 3, 1, 2, 3])
+    ns = np.array([0, 10, 5, 7, 0])
+    ys, as_ = lib.qmm_sampled(p.x_rows(M), wq, p.scales, p.biases, bits, g, ms, ns)
+    assert np.array_equal(ys, y[ms, ns]) and np.array_equal(as_, a[ms, ns])
+
+
+# Pins that run fast enough for the mutation test (the exhaustive decoder pin
+# is run once against the real oracle only).
+FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
+             pin_invariants, pin_sampled)
+ALL_PINS = (pin_decoders,) + FAST_PINS

@@ -1,0 +1,39 @@
+"""Plant plausible mistakes in copies of the oracle source and check that the
+pins catch every one of them (CPU only; the real oracle is never modified)."""
+import pytest
+
+import oracle_pins
+from oracle import oracle
+
+# (name, text in the oracle source, replacement): a wrong sign, a dropped
+# term, swapped operands, a reversed code order, a wrong group index, a
+# reversed k index, a dropped absolute value, an off-by-one in the decoders.
+MUTANTS = [
+    ("bias_sign", "return s * q + b;", "return s * q - b;"),
+    ("bias_dropped", "return s * q + b;", "return s * q;"),
+    ("scale_bias_swapped", "return s * q + b;", "return b * q + s;"),
+    ("code_order_reversed", "bits * (k % per_word)", "bits * (per_word - 1 - k % per_word)"),
+    ("group_index", "S[n * groups + k / g]", "S[n * groups + (k / g + 1) % groups]"),
+    ("k_reversed", "xm[k] * w[k]", "xm[k] * w[K - 1 - k]"),
+    ("abs_dropped", "a += std::fabs(p);\n      }\n      Y[m * N + n] = y;", "a += p;\n      }\n      Y[m * N + n] = y;"),
+    ("half_bias", "expo - 25", "expo - 24"),
+    ("bf16_frac", "128 + frac), expo - 134", "127 + frac), expo - 134"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = oracle.SOURCE.read_text()
+    assert old in src, f"mutation site for {name} not found"
+    mutant = tmp_path / f"mutant_{name}.cpp"
+    mutant.write_text(src.replace(old, new, 1))
+    lib = oracle.OracleLib(oracle.compile_source(mutant, tmp_path / f"lib_{name}.so"))
+    caught = []
+    for pin in oracle_pins.FAST_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+        except Exception as exc:  # an error return from the mutant also counts as caught
+            caught.append(f"{pin.__name__}:{type(exc).__name__}")
+    assert caught, f"mutant {name} passed every pin"
