@@ -1,0 +1,111 @@
+/*
+ * qmm.h -- C ABI of libqmm: the small-M affine-quantized matrix multiply
+ *
+ *     Y[M,N] = X[M,K] . dequant(Wq, scales, biases)[N,K]^T,   1 <= M <= 16
+ *
+ * that a speculative-decoding verify step issues with a handful of draft rows.
+ * The library streams the packed weights from HBM once per call whatever M is,
+ * dequantizes each weight group once and reuses it for all M rows.
+ *
+ * Sources of the definition (page title, section):
+ *   - "MLX quantized_matmul small-M verify kernels", fact "Stock qmv streams
+ *     the weight matrix once per input row": the problem (cost linear in M).
+ *   - same page, fact "Fix family 1": dequantize each group once into
+ *     registers and reuse it across the M rows; affine mode.
+ *   - same page, fact "Fix family 2": weights as the matrix operand, split K
+ *     across the warps of a block, read the bf16 activations directly.
+ *   - same page, fact "Group-size mechanism": fp16 scale + fp16 bias per group
+ *     (4 bytes per group).
+ *   - same page, fact "Microbench": W is stored [N,K] and Y = X . W^T.
+ *
+ * Data formats (all row-major, all buffers owned by the caller):
+ *   X       bf16 [M, K]                         device
+ *   Wq      uint32 [N, K*bits/32]               device
+ *           code k of row n sits in word k/(32/bits) of that row at bit
+ *           offset bits*(k mod (32/bits)); codes are unsigned 0..2^bits-1.
+ *           (The pages print no bit layout; this is the layout qmm_pack
+ *           writes.)
+ *   scales  fp16 [N, K/group_size]              device
+ *   biases  fp16 [N, K/group_size]              device
+ *           w[n,k] = scales[n, k/g] * q[n,k] + biases[n, k/g]
+ *   Y       bf16 (round to nearest even) or fp32 [M, N]    device
+ *
+ * Arithmetic: codes are exact in bf16 and their products with bf16 X are
+ * exact in fp32; sums are fp32; each group's scale and bias are applied once
+ * to the group's fp32 partial sums.  Results are deterministic for a given
+ * (variant, splits, shape): no atomics, fixed reduction order.
+ *
+ * Execution: every compute call is asynchronous on `stream` (a cudaStream_t
+ * passed as void*, 0 = legacy default stream).  Arguments are validated on the
+ * host before anything is launched; a validation failure returns an error and
+ * launches nothing.  There is no CPU fallback.  The library allocates no device
+ * memory and keeps no per-call state.  X, Wq, scales, biases must not overlap Y.
+ */
+#ifndef QMM_H_
+#define QMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QMM_OK = 0,
+  QMM_ERR_NULL = 1,        /* a required pointer is null                          */
+  QMM_ERR_SHAPE = 2,       /* M outside 0..16, N or K negative, K not a multiple   */
+                           /* of group_size, or a size that overflows              */
+  QMM_ERR_UNSUPPORTED = 3, /* bits not in {2,4}, group_size not in {32,64,128},    */
+                           /* unknown variant, bad split count or output dtype     */
+  QMM_ERR_ALIGN = 4,       /* X or Wq not 16-byte aligned, scales/biases/Y not     */
+                           /* aligned to their element size                        */
+  QMM_ERR_CUDA = 5,        /* the CUDA runtime reported an error; see               */
+                           /* qmm_last_cuda_error()                                 */
+  QMM_ERR_TABLE = 6        /* the dispatch table has no usable entry                */
+} qmm_status;
+
+typedef enum { QMM_OUT_BF16 = 0, QMM_OUT_F32 = 1 } qmm_out_dtype;
+
+/* Y = X . dequant(W)^T with the variant the dispatch table picks for
+ * (M, N, K, bits, group_size); bf16 output.
+ * M == 0 or N == 0: nothing to compute, returns QMM_OK without launching.
+ * K == 0: Y is the empty sum, filled with zeros on `stream`.                    */
+qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                       int M, int N, int K, int bits, int group_size, void* Y, void* stream);
+
+/* Same, with the output dtype and an optional forced kernel variant
+ * (variant = -1: dispatch table; 0 .. qmm_num_variants()-1: that variant) and
+ * split-K count across a thread-block cluster (splits = -1: the table's or the
+ * variant's default; 1..16 otherwise).                                          */
+qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                          int M, int N, int K, int bits, int group_size, void* Y,
+                          int out_dtype, int variant, int splits, void* stream);
+
+/* Number of uint32 words of a packed [N, K] matrix: N * K * bits / 32
+ * (0 if bits is unsupported or K*bits is not a multiple of 32).                 */
+size_t qmm_packed_words(int64_t N, int64_t K, int bits);
+
+/* Host-side packing of codes q[N,K] (one code per byte, each < 2^bits) into the
+ * word layout above.  Host pointers.  Returns QMM_ERR_SHAPE for a code out of
+ * range or a K that does not fill whole words.                                 */
+qmm_status qmm_pack(const uint8_t* q, int64_t N, int64_t K, int bits, uint32_t* Wq);
+
+/* Inverse of qmm_pack (host pointers).                                          */
+qmm_status qmm_unpack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint8_t* q);
+
+/* Introspection of the dispatcher: the variant and split count qmm_small_m
+ * would use, or -1 (and *splits untouched) if the shape is unsupported.         */
+int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* splits);
+
+int qmm_num_variants(void);
+const char* qmm_variant_name(int variant);     /* NULL for an unknown id          */
+const char* qmm_status_string(int status);
+int qmm_last_cuda_error(void);                 /* cudaError_t of the last failure */
+const char* qmm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H_ */

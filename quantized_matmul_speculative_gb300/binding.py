@@ -1,0 +1,158 @@
+"""ctypes binding of libqmm (C ABI in ``include/qmm.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libqmm.so``.  PyTorch supplies device memory and the current
+stream.  If the library has not been built, the first call raises
+``RuntimeError``; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import numpy as np
+
+LIBRARY = Path(__file__).resolve().parent / "libqmm.so"
+
+STATUS = {
+    0: "QMM_OK",
+    1: "QMM_ERR_NULL",
+    2: "QMM_ERR_SHAPE",
+    3: "QMM_ERR_UNSUPPORTED",
+    4: "QMM_ERR_ALIGN",
+    5: "QMM_ERR_CUDA",
+    6: "QMM_ERR_TABLE",
+}
+OUT_BF16 = 0
+OUT_F32 = 1
+
+# Every function the header declares, with its ctypes signature.
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+SIGNATURES = {
+    "qmm_small_m": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "qmm_small_m_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
+    "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
+    "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
+    "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
+    "qmm_select_variant": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
+    "qmm_num_variants": (_i32, []),
+    "qmm_variant_name": (ctypes.c_char_p, [_i32]),
+    "qmm_status_string": (ctypes.c_char_p, [_i32]),
+    "qmm_last_cuda_error": (_i32, []),
+    "qmm_version": (ctypes.c_char_p, []),
+}
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        super().__init__(f"{where}: {name}{(' (' + detail + ')') if detail else ''}")
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not LIBRARY.exists():
+            raise RuntimeError(f"{LIBRARY.name} is not built; run __graft_entry__.build() "
+                               "or quantized_matmul_speculative_gb300/build.py")
+        handle = ctypes.CDLL(str(LIBRARY))
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = handle
+    return _LIB
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        detail = ""
+        if rc == 5:
+            detail = f"cudaError {lib().qmm_last_cuda_error()}"
+        raise QmmError(rc, where, detail)
+
+
+# ---------------------------------------------------------------- host helpers
+def packed_words(N: int, K: int, bits: int) -> int:
+    return int(lib().qmm_packed_words(N, K, bits))
+
+
+def pack(q: np.ndarray, bits: int) -> np.ndarray:
+    """Pack uint8 codes [N, K] into uint32 words [N, K*bits/32] (host)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    N, K = q.shape
+    out = np.empty((N, K * bits // 32), dtype=np.uint32)
+    _check(lib().qmm_pack(q.ctypes.data, N, K, bits, out.ctypes.data), "qmm_pack")
+    return out
+
+
+def unpack(wq: np.ndarray, K: int, bits: int) -> np.ndarray:
+    wq = np.ascontiguousarray(wq, dtype=np.uint32)
+    N = wq.shape[0]
+    out = np.empty((N, K), dtype=np.uint8)
+    _check(lib().qmm_unpack(wq.ctypes.data, N, K, bits, out.ctypes.data), "qmm_unpack")
+    return out
+
+
+def select_variant(M: int, N: int, K: int, bits: int, group_size: int):
+    s = ctypes.c_int(0)
+    v = lib().qmm_select_variant(M, N, K, bits, group_size, ctypes.byref(s))
+    return (v, s.value) if v >= 0 else (None, None)
+
+
+def variant_names():
+    L = lib()
+    return [L.qmm_variant_name(i).decode() for i in range(L.qmm_num_variants())]
+
+
+# ---------------------------------------------------------------- device call
+def small_m_ptr(x_ptr: int, wq_ptr: int, s_ptr: int, b_ptr: int, M: int, N: int, K: int, bits: int,
+                group_size: int, y_ptr: int, out_dtype: int = OUT_BF16, variant: int = -1, splits: int = -1,
+                stream: int = 0) -> None:
+    """Raw-pointer call of qmm_small_m_ex (device pointers, cudaStream_t as int)."""
+    rc = lib().qmm_small_m_ex(x_ptr, wq_ptr, s_ptr, b_ptr, M, N, K, bits, group_size, y_ptr,
+                              out_dtype, variant, splits, stream)
+    _check(rc, "qmm_small_m_ex")
+
+
+def small_m(x, wq, scales, biases, bits: int, group_size: int, out=None, out_dtype=None,
+            variant: int = -1, splits: int = -1, stream=None):
+    """Y = X . dequant(Wq, scales, biases)^T on the GPU.
+
+    ``x``: bf16 [M, K]; ``wq``: int32/uint32 [N, K*bits/32]; ``scales``,
+    ``biases``: fp16 [N, K/group_size]; all CUDA tensors, contiguous.  Returns
+    ``out`` (bf16 or fp32 [M, N]), allocated by torch if not given.
+    """
+    import torch
+
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if x.dtype != torch.bfloat16 or scales.dtype != torch.float16 or biases.dtype != torch.float16:
+        raise TypeError("x must be bfloat16, scales and biases float16")
+    if wq.dtype not in (torch.int32, getattr(torch, "uint32", torch.int32)):
+        raise TypeError("wq must hold 32-bit words (int32 or uint32)")
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out dtype must be bfloat16 or float32")
+    for name, t in (("x", x), ("wq", wq), ("scales", scales), ("biases", biases)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    M, K = x.shape
+    N = wq.shape[0]
+    if wq.shape[1] * 32 != K * bits:
+        raise ValueError("wq shape does not match K and bits")
+    if tuple(scales.shape) != (N, K // group_size) or tuple(biases.shape) != (N, K // group_size):
+        raise ValueError("scales/biases must be [N, K/group_size]")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    elif tuple(out.shape) != (M, N) or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    small_m_ptr(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), M, N, K, bits, group_size,
+                out.data_ptr(), OUT_F32 if out_dtype == torch.float32 else OUT_BF16, variant, splits, handle)
+    return out

@@ -1,0 +1,303 @@
+// C ABI of libqmm (declared in include/qmm.h): argument validation, the
+// variant registry, the dispatcher and the host-side packing helpers.
+//
+// The dispatcher follows the pages' lesson that the kernel choice must come
+// from measurement ("MLX quantized_matmul small-M verify kernels", facts "The
+// qmv/qmm switch" and "Maintainers (zcbenz) ... Dispatch-constant tuning was
+// tested and refuted"; llama.cpp PR #29869: row thresholds measured per type):
+// it looks the shape up in a table generated from a committed benchmark sweep
+// (qmm_dispatch_table.inc) and falls back to a rule only for shapes the sweep
+// did not cover.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/qmm.h"
+#include "qmm_internal.h"
+
+namespace qmm {
+
+// Per-(bits, group) launchers, one translation unit each (qmm_mma_inst.cu).
+template <int BITS, int GS>
+cudaError_t launch_mma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<4, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<4, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+
+namespace {
+
+const VariantDesc kVariants[] = {
+    {"mma_r2_wn2_wk4", kFamilyMma, 2, 2, 4},
+    {"mma_r1_wn2_wk4", kFamilyMma, 1, 2, 4},
+    {"mma_r4_wn1_wk8", kFamilyMma, 4, 1, 8},
+};
+constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
+constexpr int kMaxSplits = 16;
+
+thread_local int g_last_cuda_error = 0;
+
+// One measured choice: the variant and split count for an exact problem shape.
+struct TableEntry {
+  int M, N, K, bits, gs;
+  int variant, splits;
+};
+
+const TableEntry kTable[] = {
+#include "qmm_dispatch_table.inc"
+};
+constexpr int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
+
+bool env_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+}
+
+// Variant id from QMM_FORCE_VARIANT (a name or an index), or -1.
+int forced_variant() {
+  const char* v = std::getenv("QMM_FORCE_VARIANT");
+  if (v == nullptr || v[0] == '\0') return -1;
+  for (int i = 0; i < kNumVariants; ++i)
+    if (std::strcmp(v, kVariants[i].name) == 0) return i;
+  char* end = nullptr;
+  const long id = std::strtol(v, &end, 10);
+  if (end != v && *end == '\0' && id >= 0 && id < kNumVariants) return static_cast<int>(id);
+  return -2;  // set but unknown
+}
+
+int forced_splits() {
+  const char* v = std::getenv("QMM_FORCE_SPLITS");
+  if (v == nullptr || v[0] == '\0') return -1;
+  const int s = std::atoi(v);
+  return (s >= 1 && s <= kMaxSplits) ? s : -2;
+}
+
+// Split count for shapes the sweep did not cover: enough CTAs for about two per
+// SM, at most 8 (portable cluster size), and at least one group per K-warp.
+int rule_splits(const VariantDesc& d, int N, int K, int gs) {
+  const int rows = variant_rows_per_cta(d);
+  const int tiles = (N + rows - 1) / rows;
+  const int target = 2 * device_sm_count();
+  int s = (target + tiles / 2) / (tiles > 0 ? tiles : 1);
+  const int groups = K / gs;
+  int cap = groups / d.WK;
+  if (cap > 8) cap = 8;
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  return s;
+}
+
+// The sweep's entry for this exact shape, or -1.
+int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
+  for (int i = 0; i < kTableSize; ++i) {
+    const TableEntry& e = kTable[i];
+    if (e.M == M && e.N == N && e.K == K && e.bits == bits && e.gs == gs && e.variant >= 0) {
+      *splits = e.splits;
+      return e.variant;
+    }
+  }
+  return -1;
+}
+
+int select_variant(int M, int N, int K, int bits, int gs, int* splits) {
+  int s = -1;
+  const int v = table_lookup(M, N, K, bits, gs, &s);
+  if (v >= 0 && v < kNumVariants && s >= 1 && s <= kMaxSplits) {
+    *splits = s;
+    return v;
+  }
+  *splits = rule_splits(kVariants[0], N, K, gs);
+  return 0;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qmm_status fail_cuda(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return QMM_ERR_CUDA;
+}
+
+}  // namespace
+
+const VariantDesc* variant_desc(int v) { return (v >= 0 && v < kNumVariants) ? &kVariants[v] : nullptr; }
+int variant_count() { return kNumVariants; }
+int variant_rows_per_cta(const VariantDesc& d) { return d.family == kFamilyMma ? 16 * d.R * d.WN : d.R * d.WN; }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+cudaError_t launch_mma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
+  switch (a.bits * 1000 + a.gs) {
+    case 4032: return launch_mma_bg<4, 32>(a, d, splits, stream);
+    case 4064: return launch_mma_bg<4, 64>(a, d, splits, stream);
+    case 4128: return launch_mma_bg<4, 128>(a, d, splits, stream);
+    case 2032: return launch_mma_bg<2, 32>(a, d, splits, stream);
+    case 2064: return launch_mma_bg<2, 64>(a, d, splits, stream);
+    case 2128: return launch_mma_bg<2, 128>(a, d, splits, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+const char* qmm_version(void) { return "qmm 0.1 (sm_103a)"; }
+
+const char* qmm_status_string(int s) {
+  switch (s) {
+    case QMM_OK: return "ok";
+    case QMM_ERR_NULL: return "null pointer";
+    case QMM_ERR_SHAPE: return "bad shape";
+    case QMM_ERR_UNSUPPORTED: return "unsupported bits, group size, variant, split count or output dtype";
+    case QMM_ERR_ALIGN: return "misaligned pointer";
+    case QMM_ERR_CUDA: return "CUDA runtime error";
+    case QMM_ERR_TABLE: return "no usable dispatch table entry";
+    default: return "unknown status";
+  }
+}
+
+int qmm_last_cuda_error(void) { return g_last_cuda_error; }
+int qmm_num_variants(void) { return kNumVariants; }
+const char* qmm_variant_name(int v) { return (v >= 0 && v < kNumVariants) ? kVariants[v].name : nullptr; }
+
+size_t qmm_packed_words(int64_t N, int64_t K, int bits) {
+  if ((bits != 2 && bits != 4 && bits != 8) || N < 0 || K < 0 || (K * bits) % 32 != 0) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K * bits / 32);
+}
+
+int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* splits) {
+  if (M < 1 || M > 16 || N < 1 || K < 1) return -1;
+  if ((bits != 2 && bits != 4) || (group_size != 32 && group_size != 64 && group_size != 128)) return -1;
+  if (K % group_size != 0) return -1;
+  int s = 1;
+  const int v = select_variant(M, N, K, bits, group_size, &s);
+  if (splits) *splits = s;
+  return v;
+}
+
+qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N,
+                          int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,
+                          void* stream) {
+  if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
+  if (bits != 2 && bits != 4) return QMM_ERR_UNSUPPORTED;
+  if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
+  if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
+  if (variant < -1 || variant >= kNumVariants) return QMM_ERR_UNSUPPORTED;
+  if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
+  if (K % group_size != 0) return QMM_ERR_SHAPE;
+  if (M == 0 || N == 0) return QMM_OK;
+  const size_t esize = out_dtype == QMM_OUT_F32 ? 4 : 2;
+  if (Y == nullptr) return QMM_ERR_NULL;
+  if (!aligned(Y, esize)) return QMM_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * static_cast<size_t>(N) * esize, st);
+    return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+  }
+  if (X == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
+
+  int v = variant;
+  int s = splits;
+  const int fv = forced_variant();
+  const int fs = forced_splits();
+  if (fv == -2 || fs == -2) return QMM_ERR_UNSUPPORTED;
+  if (v < 0 && fv >= 0) v = fv;
+  if (s < 0 && fs >= 0) s = fs;
+  if (v < 0) {
+    int ts = 1;
+    v = select_variant(M, N, K, bits, group_size, &ts);
+    if (s < 0) s = ts;
+  }
+  const VariantDesc& d = kVariants[v];
+  if (s < 0) s = rule_splits(d, N, K, group_size);
+  if (env_flag("QMM_LOG"))
+    std::fprintf(stderr, "qmm: M=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", M, N, K, bits, group_size, d.name, s);
+
+  // Host-side fault injection for the error-path tests: the launch reports a
+  // CUDA error without touching the device.
+  const char* inject = std::getenv("QMM_TEST_INJECT");
+  if (inject != nullptr && std::strcmp(inject, "launch_fail") == 0) return fail_cuda(cudaErrorLaunchFailure);
+
+  CallArgs a;
+  a.X = static_cast<const uint16_t*>(X);
+  a.Wq = Wq;
+  a.S = static_cast<const uint16_t*>(scales);
+  a.B = static_cast<const uint16_t*>(biases);
+  a.Y = Y;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.gs = group_size;
+  a.out_f32 = out_dtype == QMM_OUT_F32;
+  const cudaError_t e = (d.family == kFamilyMma) ? launch_mma(a, d, s, st) : cudaErrorInvalidValue;
+  return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
+
+qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N, int K,
+                       int bits, int group_size, void* Y, void* stream) {
+  return qmm_small_m_ex(X, Wq, scales, biases, M, N, K, bits, group_size, Y, QMM_OUT_BF16, -1, -1, stream);
+}
+
+// Packing, host side.  Word j of a row collects codes j*per .. j*per+per-1,
+// code i of the word at bits [bits*i, bits*i + bits).
+qmm_status qmm_pack(const uint8_t* q, int64_t N, int64_t K, int bits, uint32_t* Wq) {
+  if ((N > 0 && K > 0) && (q == nullptr || Wq == nullptr)) return QMM_ERR_NULL;
+  if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
+  if (N < 0 || K < 0 || (K * bits) % 32 != 0) return QMM_ERR_SHAPE;
+  const int per = 32 / bits;
+  const uint32_t limit = 1u << bits;
+  const uint8_t* src = q;
+  uint32_t* dst = Wq;
+  const int64_t words = N * (K / per);
+  for (int64_t w = 0; w < words; ++w) {
+    uint32_t acc = 0;
+    for (int i = per - 1; i >= 0; --i) {
+      const uint32_t c = src[i];
+      if (c >= limit) return QMM_ERR_SHAPE;
+      acc = (acc << bits) | c;
+    }
+    *dst++ = acc;
+    src += per;
+  }
+  return QMM_OK;
+}
+
+qmm_status qmm_unpack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint8_t* q) {
+  if ((N > 0 && K > 0) && (q == nullptr || Wq == nullptr)) return QMM_ERR_NULL;
+  if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
+  if (N < 0 || K < 0 || (K * bits) % 32 != 0) return QMM_ERR_SHAPE;
+  const int per = 32 / bits;
+  const uint32_t mask = (1u << bits) - 1u;
+  const int64_t words = N * (K / per);
+  for (int64_t w = 0; w < words; ++w) {
+    uint32_t word = Wq[w];
+    for (int i = 0; i < per; ++i) {
+      *q++ = static_cast<uint8_t>(word & mask);
+      word >>= bits;
+    }
+  }
+  return QMM_OK;
+}
+
+}  // extern "C"

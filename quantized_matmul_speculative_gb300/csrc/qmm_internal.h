@@ -1,0 +1,44 @@
+// Internal interface between the C ABI (qmm_api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+// Arguments of one call after host-side validation.
+struct CallArgs {
+  const uint16_t* X;   // bf16 [M, K]
+  const uint32_t* Wq;  // packed codes [N, K*bits/32]
+  const uint16_t* S;   // fp16 [N, K/gs]
+  const uint16_t* B;   // fp16 [N, K/gs]
+  void* Y;             // bf16 or fp32 [M, N]
+  int M, N, K, bits, gs, out_f32;
+};
+
+enum Family { kFamilyMma = 0, kFamilySimt = 1 };
+
+// One kernel variant: a family and its CTA tiling.
+struct VariantDesc {
+  const char* name;
+  int family;
+  int R;   // m16 row tiles per warp (mma) / rows per warp (simt)
+  int WN;  // warps along N
+  int WK;  // warps along K (intra-CTA split-K)
+};
+
+const VariantDesc* variant_desc(int v);
+int variant_count();
+
+// Rows of W one CTA of variant `v` covers.
+int variant_rows_per_cta(const VariantDesc& d);
+
+// Launch variant `d` with `splits` CTAs per cluster along K.  Returns the CUDA
+// error of the launch (cudaSuccess when it was queued).
+cudaError_t launch_mma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
+cudaError_t launch_simt(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace qmm

@@ -1,0 +1,91 @@
+// Host-side launcher of the tensor-core kernel family (see qmm_mma.cuh).
+#pragma once
+
+#include <mutex>
+
+#include "qmm_internal.h"
+#include "qmm_mma.cuh"
+#include "qmm_tiles.h"
+
+namespace qmm {
+
+// Shared memory one CTA may use; keeps two 256-thread CTAs resident per SM.
+constexpr int kMmaSmemBudget = 100 * 1024;
+
+template <int BITS, int GS, int NB, int R, int WN, int WK>
+cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) {
+  using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
+  MmaParams p;
+  p.X = a.X;
+  p.Wq = a.Wq;
+  p.S = a.S;
+  p.B = a.B;
+  p.Y = a.Y;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.out_f32 = a.out_f32;
+  p.G = a.K / GS;
+  p.gpc = (p.G + splits - 1) / splits;
+  // Largest chunk that fits the budget, then even chunks across the K-range.
+  int cmax = p.gpc;
+  while (cmax > 1 && MmaSmem<C>(cmax).total > kMmaSmemBudget) --cmax;
+  const int nchunks = (p.gpc + cmax - 1) / cmax;
+  p.chunk = (p.gpc + nchunks - 1) / nchunks;
+  if (p.chunk < 1) p.chunk = 1;
+  const int smem = MmaSmem<C>(p.chunk).total;
+
+  auto kern = qmm_mma_kernel<BITS, GS, NB, R, WN, WK>;
+  static std::mutex mu;
+  static int smem_set = 0;
+  static bool nonportable_set = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (smem > smem_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      smem_set = smem;
+    }
+    if (splits > 8 && !nonportable_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable_set = true;
+    }
+  }
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.N + C::NT - 1) / C::NT, splits, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (splits > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = splits;
+    attr[0].val.clusterDim.z = 1;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int BITS, int GS, int NB>
+cudaError_t launch_mma_tile(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
+#define QMM_TRY_TILE(r, wn, wk)                                                     \
+  if (d.R == (r) && d.WN == (wn) && d.WK == (wk))                                   \
+    return launch_mma_impl<BITS, GS, NB, r, wn, wk>(a, splits, stream);
+  QMM_MMA_TILES(QMM_TRY_TILE)
+#undef QMM_TRY_TILE
+  return cudaErrorInvalidValue;
+}
+
+// Entry for one (bits, group size): picks the activation-tile count from M.
+template <int BITS, int GS>
+cudaError_t launch_mma_bg(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
+  if (a.M <= 8) return launch_mma_tile<BITS, GS, 1>(a, d, splits, stream);
+  return launch_mma_tile<BITS, GS, 2>(a, d, splits, stream);
+}
+
+}  // namespace qmm

@@ -1,0 +1,8 @@
+// CTA tilings compiled for each kernel family: X(R, WN, WK).
+//   mma:  R 16-row tiles per warp, WN warps along N, WK warps along K.
+#pragma once
+
+#define QMM_MMA_TILES(X) \
+  X(2, 2, 4)             \
+  X(1, 2, 4)             \
+  X(4, 1, 8)

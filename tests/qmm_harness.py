@@ -1,0 +1,85 @@
+"""Shared helpers of the GPU tests: upload a synthetic problem through the
+library's own packer, run it through the C ABI, and judge it against the
+oracle with the acceptance bound |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5."""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import oracle
+from quantized_matmul_speculative_gb300 import binding, synth
+
+REL_TOL = 2e-3
+ABS_TOL = 1e-5
+
+
+class DeviceProblem:
+    """A synth.Problem with its tensors resident on the GPU (product packing)."""
+
+    def __init__(self, p: synth.Problem, device="cuda"):
+        import torch
+
+        self.p = p
+        wq = binding.pack(p.q, p.bits)
+        self.wq = torch.from_numpy(wq.view(np.int32)).to(device)
+        self.s = torch.from_numpy(p.scales.view(np.float16)).to(device)
+        self.b = torch.from_numpy(p.biases.view(np.float16)).to(device)
+        self.x = torch.from_numpy(p.x.view(np.int16)).to(device).view(torch.bfloat16)
+        self.device = device
+
+    def run(self, M: int, out_dtype=None, variant: int = -1, splits: int = -1, out=None):
+        import torch
+
+        out_dtype = out_dtype or torch.bfloat16
+        x = self.x[:M].contiguous()
+        return binding.small_m(x, self.wq, self.s, self.b, self.p.bits, self.p.group_size, out=out,
+                               out_dtype=out_dtype, variant=variant, splits=splits)
+
+
+def to_f64(y) -> np.ndarray:
+    import torch
+
+    return y.detach().to(torch.float64).cpu().numpy()
+
+
+class OracleRef:
+    """Oracle results for one problem (the oracle packs the codes itself)."""
+
+    def __init__(self, p: synth.Problem):
+        self.p = p
+        self.lib = oracle.load()
+        self.wq = self.lib.pack(p.q, p.bits)
+        self._full = None
+
+    def full(self, M: int = synth.MAX_ROWS):
+        if self._full is None or self._full[0].shape[0] < M:
+            self._full = self.lib.qmm(self.p.x_rows(M), self.wq, self.p.scales, self.p.biases, self.p.bits,
+                                      self.p.group_size)
+        y, a = self._full
+        return y[:M], a[:M]
+
+    def sampled(self, M: int, ms, ns):
+        return self.lib.qmm_sampled(self.p.x_rows(M), self.wq, self.p.scales, self.p.biases, self.p.bits,
+                                    self.p.group_size, ms, ns)
+
+
+def assert_within(y, y_ref, a_ref, what: str):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - y_ref)
+    bound = REL_TOL * a_ref + ABS_TOL
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; first at {idx}: "
+                             f"gpu={y[idx]!r} ref={y_ref[idx]!r} bound={bound[idx]!r}; "
+                             f"max err/bound={float((err / bound).max()):.3f}")
+    return float((err / bound).max()) if err.size else 0.0
+
+
+def sample_positions(M: int, N: int, count: int, seed: int = 0):
+    rng = np.random.default_rng(seed)
+    ms = rng.integers(0, M, size=count)
+    ns = rng.integers(0, N, size=count)
+    # always include the corners and the last row tile
+    ms = np.concatenate([ms, [0, M - 1, 0, M - 1]])
+    ns = np.concatenate([ns, [0, 0, N - 1, N - 1]])
+    return ms, ns

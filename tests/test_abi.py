@@ -1,0 +1,89 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+packs bit-exactly like the oracle's packer, and rejects bad arguments on the
+host before touching the device."""
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+from oracle import oracle
+from quantized_matmul_speculative_gb300 import binding, build
+
+HEADER = Path(__file__).resolve().parents[1] / "include" / "qmm.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(qmm_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "qmm_small_m" in names and "qmm_pack" in names
+    raw = ctypes.CDLL(str(binding.LIBRARY))
+    for name in names:
+        assert hasattr(raw, name), f"{name} declared in qmm.h but not exported"
+    assert set(names) == set(binding.SIGNATURES), "binding signatures out of sync with qmm.h"
+
+
+def test_pack_matches_oracle_bit_exact(lib):
+    ol = oracle.load()
+    rng = np.random.default_rng(11)
+    for bits in (2, 4, 8):
+        for N, K in ((1, 32), (3, 64), (17, 256), (64, 1024)):
+            q = rng.integers(0, 1 << bits, size=(N, K), dtype=np.uint8)
+            ours = binding.pack(q, bits)
+            assert np.array_equal(ours, ol.pack(q, bits)), (bits, N, K)
+            assert np.array_equal(binding.unpack(ours, K, bits), q)
+    assert int(binding.pack(np.arange(8, dtype=np.uint8).reshape(1, 8), 4)[0, 0]) == 0x76543210
+    assert int(binding.pack(np.tile(np.arange(4, dtype=np.uint8), 4).reshape(1, 16), 2)[0, 0]) == 0xE4E4E4E4
+
+
+def test_pack_rejects_bad_input(lib):
+    with pytest.raises(binding.QmmError):
+        binding.pack(np.full((1, 8), 16, dtype=np.uint8), 4)  # code out of range
+    with pytest.raises(binding.QmmError):
+        binding.pack(np.zeros((1, 12), dtype=np.uint8), 4)  # K does not fill whole words
+    assert binding.packed_words(10, 64, 4) == 80
+    assert binding.packed_words(10, 64, 3) == 0
+
+
+def test_validation_before_launch(lib):
+    call = lib.qmm_small_m_ex
+    # (X, Wq, S, B, M, N, K, bits, gs, Y, out, variant, splits, stream); bogus but aligned pointers
+    p = 0x10000
+    base = [p, p, p, p, 4, 64, 256, 4, 64, p, 0, -1, -1, None]
+
+    def rc(**kw):
+        a = list(base)
+        pos = {"M": 4, "N": 5, "K": 6, "bits": 7, "gs": 8, "out": 10, "variant": 11, "splits": 12,
+               "X": 0, "Wq": 1, "Y": 9}
+        for k, v in kw.items():
+            a[pos[k]] = v
+        return call(*a)
+
+    assert rc(M=17) == 2 and rc(M=-1) == 2 and rc(N=-3) == 2
+    assert rc(bits=3) == 3 and rc(bits=8) == 3 and rc(gs=48) == 3 and rc(gs=256) == 3
+    assert rc(K=96) == 2
+    assert rc(out=2) == 3 and rc(variant=lib.qmm_num_variants()) == 3 and rc(splits=0) == 3 and rc(splits=17) == 3
+    assert rc(X=None) == 1 and rc(Wq=None) == 1 and rc(Y=None) == 1
+    assert rc(X=p + 2) == 4 and rc(Wq=p + 8) == 4 and rc(Y=p + 1) == 4
+    assert rc(M=0) == 0 and rc(N=0) == 0  # nothing to compute
+
+
+def test_variant_registry(lib):
+    names = binding.variant_names()
+    assert len(names) == lib.qmm_num_variants() >= 1
+    assert lib.qmm_variant_name(len(names)) is None
+    v, s = binding.select_variant(4, 5120, 5120, 4, 64)
+    assert 0 <= v < len(names) and 1 <= s <= 16
+    assert binding.select_variant(17, 5120, 5120, 4, 64) == (None, None)
+    assert lib.qmm_status_string(4) == b"misaligned pointer"

@@ -1,0 +1,220 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every output must satisfy |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5.  Small
+shapes are checked element by element against the full oracle; full-size
+workload shapes are checked on sampled outputs the oracle computes one by one,
+in the same launch configuration the benchmark uses (the dispatcher's choice).
+"""
+import numpy as np
+import pytest
+
+from qmm_harness import DeviceProblem, OracleRef, assert_within, sample_positions, to_f64
+from quantized_matmul_speculative_gb300 import binding, synth, workloads
+
+pytestmark = pytest.mark.gpu
+
+BITS_GS = [(4, 32), (4, 64), (4, 128), (2, 32), (2, 64), (2, 128)]
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_matmul_speculative_gb300 import build
+
+    build.build()
+    binding.lib()
+    return torch
+
+
+def variants():
+    return list(range(len(binding.variant_names())))
+
+
+# ------------------------------------------------------------- small shapes
+@pytest.mark.parametrize("bits,gs", BITS_GS)
+def test_small_shapes_all_m(torch_cuda, bits, gs):
+    """Several tiles and a ragged N tail, M = 1..16, every variant, split 1 and 2."""
+    torch = torch_cuda
+    N, K = 200, 8 * gs
+    p = synth.make_problem(7000 + bits * 1000 + gs, N, K, bits, gs)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    y_ref, a_ref = ref.full(16)
+    for v in variants():
+        for splits in (1, 2):
+            for M in range(1, 17):
+                y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits)
+                assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"v{v} s{splits} M={M} f32")
+            y = dp.run(16, variant=v, splits=splits)
+            assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} M=16 bf16")
+
+
+@pytest.mark.parametrize("N", [1, 7, 15, 17, 129])
+@pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (4, 128)])
+def test_ragged_n_and_one_group(torch_cuda, N, bits, gs):
+    torch = torch_cuda
+    for K in (gs, 3 * gs):
+        p = synth.make_problem(8000 + N + K, N, K, bits, gs)
+        dp, ref = DeviceProblem(p), OracleRef(p)
+        y_ref, a_ref = ref.full(16)
+        for v in variants():
+            for M in (1, 8, 9, 16):
+                for splits in (1, 3):
+                    y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits)
+                    assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"N={N} K={K} v{v} M={M} s{splits}")
+
+
+def test_single_layer_workload_full(torch_cuda):
+    """1024x1024 4-bit g64 at M=4: every output, every variant and split 1..8, both dtypes."""
+    torch = torch_cuda
+    w = workloads.SINGLE_LAYER
+    sh = w.shapes[0]
+    p = synth.make_problem(workloads.shape_seed(w, 0), sh.N, sh.K, w.bits, w.group_size)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    y_ref, a_ref = ref.full(4)
+    y = dp.run(4)
+    assert_within(to_f64(y), y_ref, a_ref, "dispatcher")
+    for v in variants():
+        for splits in (1, 2, 4, 8):
+            for dt in (torch.bfloat16, torch.float32):
+                y = dp.run(4, out_dtype=dt, variant=v, splits=splits)
+                assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} {dt}")
+
+
+def test_m_sweep_5120_full(torch_cuda):
+    """5120x5120 4-bit g64, M = 1..16 through the dispatcher: every output."""
+    w = workloads.M_SWEEP
+    sh = w.shapes[0]
+    p = synth.make_problem(workloads.shape_seed(w, 0), sh.N, sh.K, w.bits, w.group_size)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    y_ref, a_ref = ref.full(16)
+    for M in w.ms:
+        y = dp.run(M)
+        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"M={M}")
+
+
+@pytest.mark.parametrize("shape_index", range(4))
+def test_dense27b_layer_sampled(torch_cuda, shape_index):
+    w = workloads.DENSE_27B_LAYER
+    sh = w.shapes[shape_index]
+    p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    for M in w.ms:
+        y = to_f64(dp.run(M))
+        ms, ns = sample_positions(M, sh.N, 192, seed=M)
+        y_ref, a_ref = ref.sampled(M, ms, ns)
+        assert_within(y[ms, ns], y_ref, a_ref, f"{sh.name} M={M}")
+
+
+@pytest.mark.parametrize("bits,gs", workloads.GROUP_BIT_SWEEP.variants)
+def test_group_bit_sweep_sampled(torch_cuda, bits, gs):
+    w = workloads.GROUP_BIT_SWEEP
+    sh = w.shapes[0]
+    p = synth.make_problem(workloads.shape_seed(w, 0, bits=bits, group_size=gs), sh.N, sh.K, bits, gs)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    for M in w.ms:
+        y = to_f64(dp.run(M))
+        ms, ns = sample_positions(M, sh.N, 96, seed=M)
+        y_ref, a_ref = ref.sampled(M, ms, ns)
+        assert_within(y[ms, ns], y_ref, a_ref, f"{bits}b g{gs} M={M}")
+
+
+@pytest.mark.parametrize("shape_index", range(4))
+def test_verify_step_shapes_sampled(torch_cuda, shape_index):
+    w = workloads.VERIFY_STEP
+    sh = w.shapes[shape_index]
+    p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    for M in w.ms:
+        y = to_f64(dp.run(M))
+        ms, ns = sample_positions(M, sh.N, 96, seed=M)
+        y_ref, a_ref = ref.sampled(M, ms, ns)
+        assert_within(y[ms, ns], y_ref, a_ref, f"{sh.name} M={M}")
+
+
+# ------------------------------------------------------------- properties
+def test_determinism_and_batch_invariance(torch_cuda):
+    torch = torch_cuda
+    p = synth.make_problem(9100, 777, 2048, 4, 64)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    y_ref, a_ref = ref.full(16)
+    for v in variants():
+        first = dp.run(16, out_dtype=torch.float32, variant=v, splits=4)
+        for _ in range(4):
+            again = dp.run(16, out_dtype=torch.float32, variant=v, splits=4)
+            assert torch.equal(first, again), f"variant {v} not deterministic"
+        assert_within(to_f64(first), y_ref, a_ref, f"variant {v} M=16")
+        # each row of the 16-row call against a 1-row call on that row alone
+        for m in (0, 5, 15):
+            x1 = dp.x[m:m + 1].contiguous()
+            single = binding.small_m(x1, dp.wq, dp.s, dp.b, 4, 64, out_dtype=torch.float32, variant=v, splits=4)
+            assert_within(to_f64(single)[0], y_ref[m], a_ref[m], f"variant {v} row {m} alone")
+            bitwise = torch.equal(single[0], first[m])
+            print(f"variant {v} row {m}: bit-identical across M: {bitwise}")
+
+
+def test_output_guard_bands(torch_cuda):
+    """Writes stay inside Y: canaries around the output are untouched."""
+    torch = torch_cuda
+    p = synth.make_problem(9200, 129, 512, 4, 64)
+    dp = DeviceProblem(p)
+    for M in (1, 7, 16):
+        for dt in (torch.bfloat16, torch.float32):
+            pad = 64
+            buf = torch.full((M * 129 + 2 * pad,), -12345.0, dtype=dt, device="cuda")
+            out = buf[pad:pad + M * 129].view(M, 129)
+            for v in variants():
+                dp.run(M, out_dtype=dt, variant=v, splits=2, out=out)
+                torch.cuda.synchronize()
+                assert bool((buf[:pad] == -12345.0).all()) and bool((buf[-pad:] == -12345.0).all())
+
+
+def test_empty_and_degenerate(torch_cuda):
+    torch = torch_cuda
+    dev = "cuda"
+    x = torch.zeros((4, 0), dtype=torch.bfloat16, device=dev)
+    wq = torch.zeros((5, 0), dtype=torch.int32, device=dev)
+    s = torch.zeros((5, 0), dtype=torch.float16, device=dev)
+    y = torch.full((4, 5), 7.0, dtype=torch.float32, device=dev)
+    binding.small_m(x, wq, s, s, 4, 64, out=y)  # K = 0: empty sum
+    assert bool((y == 0).all())
+    # M = 0 and N = 0 launch nothing and succeed
+    binding.small_m_ptr(0, 0, 0, 0, 0, 5, 64, 4, 64, 0)
+    binding.small_m_ptr(0, 0, 0, 0, 3, 0, 64, 4, 64, 0)
+
+
+def test_error_paths_launch_nothing(torch_cuda, monkeypatch):
+    torch = torch_cuda
+    p = synth.make_problem(9300, 64, 256, 4, 64)
+    dp = DeviceProblem(p)
+    y = torch.full((2, 64), 3.0, dtype=torch.float32, device="cuda")
+    x = dp.x[:2].contiguous()
+    args = [x.data_ptr(), dp.wq.data_ptr(), dp.s.data_ptr(), dp.b.data_ptr(), 2, 64, 256, 4, 64, y.data_ptr()]
+    cases = {
+        "misaligned X": (dict(idx=0, delta=2), 4),
+        "misaligned Wq": (dict(idx=1, delta=4), 4),
+    }
+    for name, (mod, code) in cases.items():
+        a = list(args)
+        a[mod["idx"]] += mod["delta"]
+        with pytest.raises(binding.QmmError) as ei:
+            binding.small_m_ptr(*a, out_dtype=binding.OUT_F32)
+        assert ei.value.status == code, name
+    for bad, code in (({"M": 17}, 2), ({"bits": 3}, 3), ({"gs": 48}, 3), ({"K": 96}, 2)):
+        a = list(args)
+        key = {"M": 4, "bits": 7, "gs": 8, "K": 6}[next(iter(bad))]
+        a[key] = next(iter(bad.values()))
+        with pytest.raises(binding.QmmError) as ei:
+            binding.small_m_ptr(*a, out_dtype=binding.OUT_F32)
+        assert ei.value.status == code, bad
+    monkeypatch.setenv("QMM_TEST_INJECT", "launch_fail")
+    with pytest.raises(binding.QmmError) as ei:
+        binding.small_m_ptr(*args, out_dtype=binding.OUT_F32)
+    assert ei.value.status == 5
+    monkeypatch.delenv("QMM_TEST_INJECT")
+    torch.cuda.synchronize()
+    assert bool((y == 3.0).all()), "a rejected call wrote to Y"
+    # the context is still healthy
+    binding.small_m_ptr(*args, out_dtype=binding.OUT_F32)
+    torch.cuda.synchronize()
