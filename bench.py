@@ -1,0 +1,417 @@
+"""Benchmark of the small-M quantized matmul on GB300.
+
+Default workload: M sweep on one 5120x5120 4-bit affine g64 layer.  One step
+is the whole hot path over one batch of synthetic input: 16 calls, M = 1..16,
+each reading the previous call's output as its activations (a dependent
+chain, as decode is), each streaming a different copy of the weights so that
+the copies in rotation (> 4x L2) keep every call's weights cold in HBM.  The
+step is captured in a CUDA graph and replayed.
+
+``value`` is weight+metadata GB/s over the timed steps: the bytes each call
+must stream (N*K*bits/8 + 4*N*K/g), summed over the step's calls and over all
+ranks, divided by the max-over-ranks step time.  ``e2e`` is the same metric
+through the C ABI with the activations copied in from pinned host memory and
+the outputs read back, every call.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference that
+exists for this path) on the host cores, on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import shutil
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from quantized_matmul_speculative_gb300 import synth, workloads  # noqa: E402
+
+METRIC = "weight GB/s and % of HBM peak per call vs M=1..16 (4-bit affine g64)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("qmm_tma.cuh", "qmm_tma_launch.cuh", "qmm_device.cuh", "qmm_tiles.h", "qmm_geometry.h")
+
+
+# ------------------------------------------------------------------ helpers
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "quantized_matmul_speculative_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    f = ROOT / "profiles" / f"qmm_tma_{workload}.md"
+    if not f.exists():
+        return None
+    text = f.read_text()
+    mh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    mt = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not mh or not mt or mh.group(1) != kernel_hash():
+        return None
+    return float(mt.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = Path(os.environ.get("TMPDIR", "/tmp")) / f"qmm_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi"):
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path.exists():
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.path.read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        self.path.unlink(missing_ok=True)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ the workload
+def make_m_sweep_problem():
+    w = workloads.M_SWEEP
+    sh = w.shapes[0]
+    p = synth.make_problem(workloads.shape_seed(w, 0), sh.N, sh.K, w.bits, w.group_size)
+    return w, sh, p
+
+
+def cpu_oracle_sample(p: synth.Problem, rows: int, ms):
+    """Time the fp64 oracle on the first `rows` weight rows for each M in `ms`;
+    returns (weight+meta bytes processed, seconds)."""
+    from oracle import oracle
+
+    lib = oracle.load()
+    q = np.ascontiguousarray(p.q[:rows])
+    wq = lib.pack(q, p.bits)
+    s = np.ascontiguousarray(p.scales[:rows])
+    b = np.ascontiguousarray(p.biases[:rows])
+    t0 = time.perf_counter()
+    for M in ms:
+        lib.qmm(p.x_rows(M), wq, s, b, p.bits, p.group_size)
+    dt = time.perf_counter() - t0
+    nbytes = len(ms) * workloads.call_bytes(rows, p.K, p.bits, p.group_size)
+    return nbytes, dt
+
+
+def run_reference(args, world, rank):
+    """The oracle arm: host cores, a bounded sample of the same workload per step.
+
+    The rows per step are sized from a short calibration so that warm-up plus
+    the timed steps take about ``--ref-budget`` seconds of CPU work."""
+    if rank != 0:
+        return 0
+    w, sh, p = make_m_sweep_problem()
+    ms = list(w.ms)
+    nb, dt = cpu_oracle_sample(p, 16, ms)
+    per_row = dt / 16
+    rows = int(args.ref_budget / max(1, args.steps + args.warmup) / per_row)
+    rows = max(1, min(sh.N, rows))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(p, rows, ms)
+    total_b, total_t = 0, 0.0
+    for _ in range(args.steps):
+        nb, dt = cpu_oracle_sample(p, rows, ms)
+        total_b += nb
+        total_t += dt
+    value = total_b / total_t / 1e9
+    sample = (f"each step: M=1..16 over the first {rows} of {sh.N} weight rows of the "
+              f"{sh.N}x{sh.K} 4-bit g64 layer, fp64 oracle, 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "N": sh.N, "K": sh.K, "bits": w.bits,
+                                        "group_size": w.group_size, "M": "1..16", "rows_sampled": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from quantized_matmul_speculative_gb300 import binding, build
+
+    build.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w, sh, p = make_m_sweep_problem()
+    N, K, bits, gs = sh.N, sh.K, w.bits, w.group_size
+    ms = list(w.ms)
+    call_b = workloads.call_bytes(N, K, bits, gs)
+
+    # weights: distinct copies whose total exceeds 4x L2, so each call reads cold HBM
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ncopy = max(args.min_copies, int(np.ceil(4 * l2 / call_b)) + 1)
+    wq_h = torch.from_numpy(binding.pack(p.q, bits).view(np.int32))
+    s_h = torch.from_numpy(p.scales.view(np.float16))
+    b_h = torch.from_numpy(p.biases.view(np.float16))
+    copies = [(wq_h.to(dev), s_h.to(dev), b_h.to(dev)) for _ in range(ncopy)]
+    x0 = torch.from_numpy(p.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    bufs = [x0.clone(), torch.empty_like(x0)]
+    stream = torch.cuda.Stream(dev)
+    handle = stream.cuda_stream
+
+    def call(M, ci, xb, yb):
+        wq, s, b = copies[ci % ncopy]
+        binding.small_m_ptr(xb.data_ptr(), wq.data_ptr(), s.data_ptr(), b.data_ptr(), M, N, K, bits, gs,
+                            yb.data_ptr(), binding.OUT_BF16, -1, -1, handle)
+
+    calls_per_step = len(ms)
+    # Graph of `reps` steps: the copy index advances every call, the chain
+    # ping-pongs between two activation buffers.
+    reps = max(1, int(np.ceil(ncopy / calls_per_step)))
+    with torch.cuda.stream(stream):
+        for i, M in enumerate(ms * 2):  # eager warm-up (kernel attributes, module load)
+            call(M, i, bufs[i % 2], bufs[(i + 1) % 2])
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ci = 0
+        for r in range(reps):
+            for M in ms:
+                call(M, ci, bufs[ci % 2], bufs[(ci + 1) % 2])
+                ci += 1
+    stream.synchronize()
+
+    # timed region: K steps = ceil(K/reps) replays of the `reps`-step graph
+    replays_w = max(1, int(np.ceil(args.warmup / reps)))
+    replays = max(1, int(np.ceil(args.steps / reps)))
+    steps_timed = replays * reps
+    with torch.cuda.stream(stream):
+        for _ in range(replays_w):
+            graph.replay()
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            end.record(stream)
+        end.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    ms_per_step = ms_total / steps_timed
+    step_bytes = calls_per_step * call_b
+    value = world * step_bytes * steps_timed / (ms_total * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # per-M: graph of 64 calls at one M over rotating copies, median of 5 replays
+    per_m = []
+    for M in ms:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(64):
+                call(M, i, bufs[i % 2], bufs[(i + 1) % 2])
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            for _ in range(5):
+                a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b2.record(stream)
+                b2.synchronize()
+                times.append(a.elapsed_time(b2) * 1e3 / 64)
+        us = float(np.median(times))
+        gbs = call_b / (us * 1e-6) / 1e9
+        variant, splits = binding.select_variant(M, N, K, bits, gs)
+        per_m.append({"M": M, "us_per_call": round(us, 3), "weight_gbs": round(gbs, 1),
+                      "frac_hbm": round(gbs / peak, 4), "variant": binding.variant_names()[variant],
+                      "splits": splits, "spread_us": round(max(times) - min(times), 3)})
+        del g
+
+    # e2e: public API with host buffers; H2D of the activations and D2H of the output every call
+    x_host = torch.from_numpy(p.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty((16, N), dtype=torch.bfloat16).pin_memory()
+    xd, yd = torch.empty_like(x0), torch.empty_like(x0)
+    e2e_steps = max(3, min(args.steps, 200))
+    h2d = sum(2 * M * K for M in ms)
+    d2h = sum(2 * M * N for M in ms)
+
+    def e2e_step(ci0):
+        for i, M in enumerate(ms):
+            xd[:M].copy_(x_host[:M], non_blocking=True)
+            call(M, ci0 + i, xd, yd)
+            y_host[:M].copy_(yd[:M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step(0)
+        stream.synchronize()
+        barrier(world)
+        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for st in range(e2e_steps):
+            e2e_step(st * calls_per_step)
+        b2.record(stream)
+        b2.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b2), world, dev)
+    e2e_value = world * step_bytes * e2e_steps / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        nb, dt = cpu_oracle_sample(p, args.cpu_rows, ms)
+        cpu = {"value": nb / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"M=1..16 over the first {args.cpu_rows} of {N} rows, fp64 oracle, 1 thread, "
+                         f"{dt:.1f} s"}
+
+    clk = clocks.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps_timed,
+            "warmup": replays_w * reps, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "N": N, "K": K, "bits": bits, "group_size": gs, "M": "1..16",
+                       "calls_per_step": calls_per_step, "chain": "dependent (each call reads the previous output)",
+                       "l2": f"inputs larger than L2: {ncopy} rotating weight copies, "
+                             f"{ncopy * call_b / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
+                       "timing": "CUDA graph replays, CUDA events on the launching stream",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(value / world / peak, 4), "traffic": profiled_traffic(w.name),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s", "kernel": "qmm_tma_kernel",
+                         "achieved_def": "weight+metadata bytes per launch / mean launch time over the timed region"},
+            "per_m": per_m,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "note": "weights resident (model state); activations H2D from pinned memory and outputs D2H "
+                            "every call"},
+            "gpu_launches": steps_timed * calls_per_step,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--min-copies", type=int, default=36)
+    ap.add_argument("--cpu-rows", type=int, default=5120)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+    world, rank, local = dist_setup(args)
+    try:
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

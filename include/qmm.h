@@ -76,8 +76,11 @@ qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, co
 
 /* Same, with the output dtype and an optional forced kernel variant
  * (variant = -1: dispatch table; 0 .. qmm_num_variants()-1: that variant) and
- * split-K count across a thread-block cluster (splits = -1: the table's or the
- * variant's default; 1..16 otherwise).                                          */
+ * the number of CTAs that split K inside one thread-block cluster (splits = -1:
+ * the table's or the variant's default; 1..16 otherwise).  A (variant, splits)
+ * pair the shape cannot use returns QMM_ERR_UNSUPPORTED and launches nothing:
+ * the "tma" variants need K/group_size even, divisible by splits with an even
+ * quotient, and 4-byte aligned scales and biases.                              */
 qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
                           int M, int N, int K, int bits, int group_size, void* Y,
                           int out_dtype, int variant, int splits, void* stream);
@@ -102,6 +105,14 @@ int qmm_num_variants(void);
 const char* qmm_variant_name(int variant);     /* NULL for an unknown id          */
 const char* qmm_status_string(int status);
 int qmm_last_cuda_error(void);                 /* cudaError_t of the last failure */
+
+/* Device status word of the kernels, OR-ed over all kernel units: bit 0 = a
+ * consumer gave up waiting for a weight tile, bit 1 = the producer gave up
+ * waiting for a free stage, bit 2 = copies still in flight at exit gave up.
+ * Every wait is bounded (about 2 s), so a fault shows up here instead of as a
+ * hang.  Synchronizes with the device; clears the word when `clear` != 0.
+ * 0xFFFFFFFF if the word could not be read.                                    */
+unsigned int qmm_device_status(int clear);
 const char* qmm_version(void);
 
 #ifdef __cplusplus

@@ -39,6 +39,7 @@ SIGNATURES = {
     "qmm_variant_name": (ctypes.c_char_p, [_i32]),
     "qmm_status_string": (ctypes.c_char_p, [_i32]),
     "qmm_last_cuda_error": (_i32, []),
+    "qmm_device_status": (ctypes.c_uint, [_i32]),
     "qmm_version": (ctypes.c_char_p, []),
 }
 
@@ -102,6 +103,11 @@ def select_variant(M: int, N: int, K: int, bits: int, group_size: int):
     s = ctypes.c_int(0)
     v = lib().qmm_select_variant(M, N, K, bits, group_size, ctypes.byref(s))
     return (v, s.value) if v >= 0 else (None, None)
+
+
+def device_status(clear: bool = True) -> int:
+    """OR of the kernels' device status words (0 = no bounded wait gave up)."""
+    return int(lib().qmm_device_status(1 if clear else 0))
 
 
 def variant_names():

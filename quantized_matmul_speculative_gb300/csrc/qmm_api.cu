@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/qmm.h"
+#include "qmm_geometry.h"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -29,14 +30,36 @@ extern template cudaError_t launch_mma_bg<4, 128>(const CallArgs&, const Variant
 extern template cudaError_t launch_mma_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template <int BITS, int GS>
+cudaError_t launch_tma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<4, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<4, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template <int BITS, int GS>
+unsigned int read_device_status(int clear);
+extern template unsigned int read_device_status<4, 32>(int);
+extern template unsigned int read_device_status<4, 64>(int);
+extern template unsigned int read_device_status<4, 128>(int);
+extern template unsigned int read_device_status<2, 32>(int);
+extern template unsigned int read_device_status<2, 64>(int);
+extern template unsigned int read_device_status<2, 128>(int);
 
 namespace {
 
+// mma: {R, WN, WK}; tma: {stages, consumer warps, CTAs per SM}.
 const VariantDesc kVariants[] = {
     {"mma_r2_wn2_wk4", kFamilyMma, 2, 2, 4},
     {"mma_r1_wn2_wk4", kFamilyMma, 1, 2, 4},
     {"mma_r4_wn1_wk8", kFamilyMma, 4, 1, 8},
+    {"tma_w8_2cta", kFamilyTma, 8, 8, 2},
+    {"tma_w4_2cta", kFamilyTma, 8, 4, 2},
+    {"tma_w8_1cta", kFamilyTma, 8, 8, 1},
 };
+constexpr int kDefaultTma = 3;     // two CTAs per SM
+constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 constexpr int kMaxSplits = 16;
 
@@ -104,14 +127,45 @@ int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
   return -1;
 }
 
-int select_variant(int M, int N, int K, int bits, int gs, int* splits) {
+// Cluster size for the TMA family on shapes the sweep did not cover: the
+// candidate (8, 4, 2, 1) with the best tile balance over the clusters that fit
+// two CTAs per SM, larger clusters first on ties.
+int rule_tma_cluster(const CallArgs& a, const VariantDesc& d) {
+  const int tiles = (a.N + 15) / 16;
+  const int sms = device_sm_count();
+  int best = -1;
+  double best_cost = 1e30;
+  for (int c : {8, 4, 2, 1}) {
+    if (!tma_supported(a, c, d)) continue;
+    int ncl = (d.WK * sms) / c;
+    if (ncl > tiles) ncl = tiles;
+    if (ncl < 1) ncl = 1;
+    // work of the busiest CTA: its tiles times its share of K
+    const double per = static_cast<double>((tiles + ncl - 1) / ncl);
+    const double cost = per / c + 1e-9 * (8 - c);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+    }
+  }
+  return best;
+}
+
+int select_variant(const CallArgs& a, int* splits) {
   int s = -1;
-  const int v = table_lookup(M, N, K, bits, gs, &s);
+  const int v = table_lookup(a.M, a.N, a.K, a.bits, a.gs, &s);
   if (v >= 0 && v < kNumVariants && s >= 1 && s <= kMaxSplits) {
     *splits = s;
     return v;
   }
-  *splits = rule_splits(kVariants[0], N, K, gs);
+  for (int v : {kDefaultTma, kDefaultTma1}) {
+    const int c = rule_tma_cluster(a, kVariants[v]);
+    if (c > 0) {
+      *splits = c;
+      return v;
+    }
+  }
+  *splits = rule_splits(kVariants[0], a.N, a.K, a.gs);
   return 0;
 }
 
@@ -126,7 +180,40 @@ qmm_status fail_cuda(cudaError_t e) {
 
 const VariantDesc* variant_desc(int v) { return (v >= 0 && v < kNumVariants) ? &kVariants[v] : nullptr; }
 int variant_count() { return kNumVariants; }
-int variant_rows_per_cta(const VariantDesc& d) { return d.family == kFamilyMma ? 16 * d.R * d.WN : d.R * d.WN; }
+int variant_rows_per_cta(const VariantDesc& d) { return d.family == kFamilyMma ? 16 * d.R * d.WN : 16; }
+
+bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
+  int gp, pw, bw, nb;
+  if (!tma_geometry(a.K, a.bits, a.gs, csize, &gp, &pw, &bw, &nb)) return false;
+  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 3) return false;
+  // the CTA's stages, activations and at least one partial tile must fit
+  static int sm_bytes = 0, optin = 0;
+  if (sm_bytes == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sm_bytes = 233472;  // sm_103a
+      optin = 232448;
+    }
+  }
+  const int mp = a.M <= 8 ? 8 : 16;
+  const TmaLayout L(pw, gp, a.gs, mp, 2, 1);  // two stages and one partial tile at least
+  return L.total <= tma_smem_budget(sm_bytes, optin, d.WK);
+}
+
+cudaError_t launch_tma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
+  switch (a.bits * 1000 + a.gs) {
+    case 4032: return launch_tma_bg<4, 32>(a, d, splits, stream);
+    case 4064: return launch_tma_bg<4, 64>(a, d, splits, stream);
+    case 4128: return launch_tma_bg<4, 128>(a, d, splits, stream);
+    case 2032: return launch_tma_bg<2, 32>(a, d, splits, stream);
+    case 2064: return launch_tma_bg<2, 64>(a, d, splits, stream);
+    case 2128: return launch_tma_bg<2, 128>(a, d, splits, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 int device_sm_count() {
   static std::mutex mu;
@@ -188,9 +275,26 @@ int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* split
   if (M < 1 || M > 16 || N < 1 || K < 1) return -1;
   if ((bits != 2 && bits != 4) || (group_size != 32 && group_size != 64 && group_size != 128)) return -1;
   if (K % group_size != 0) return -1;
+  CallArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.gs = group_size;
   int s = 1;
-  const int v = select_variant(M, N, K, bits, group_size, &s);
+  const int v = select_variant(a, &s);
   if (splits) *splits = s;
+  return v;
+}
+
+unsigned int qmm_device_status(int clear) {
+  unsigned int v = 0;
+  v |= read_device_status<4, 32>(clear);
+  v |= read_device_status<4, 64>(clear);
+  v |= read_device_status<4, 128>(clear);
+  v |= read_device_status<2, 32>(clear);
+  v |= read_device_status<2, 64>(clear);
+  v |= read_device_status<2, 128>(clear);
   return v;
 }
 
@@ -216,28 +320,6 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
   if (X == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
   if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
 
-  int v = variant;
-  int s = splits;
-  const int fv = forced_variant();
-  const int fs = forced_splits();
-  if (fv == -2 || fs == -2) return QMM_ERR_UNSUPPORTED;
-  if (v < 0 && fv >= 0) v = fv;
-  if (s < 0 && fs >= 0) s = fs;
-  if (v < 0) {
-    int ts = 1;
-    v = select_variant(M, N, K, bits, group_size, &ts);
-    if (s < 0) s = ts;
-  }
-  const VariantDesc& d = kVariants[v];
-  if (s < 0) s = rule_splits(d, N, K, group_size);
-  if (env_flag("QMM_LOG"))
-    std::fprintf(stderr, "qmm: M=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", M, N, K, bits, group_size, d.name, s);
-
-  // Host-side fault injection for the error-path tests: the launch reports a
-  // CUDA error without touching the device.
-  const char* inject = std::getenv("QMM_TEST_INJECT");
-  if (inject != nullptr && std::strcmp(inject, "launch_fail") == 0) return fail_cuda(cudaErrorLaunchFailure);
-
   CallArgs a;
   a.X = static_cast<const uint16_t*>(X);
   a.Wq = Wq;
@@ -250,7 +332,33 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
   a.bits = bits;
   a.gs = group_size;
   a.out_f32 = out_dtype == QMM_OUT_F32;
-  const cudaError_t e = (d.family == kFamilyMma) ? launch_mma(a, d, s, st) : cudaErrorInvalidValue;
+
+  int v = variant;
+  int s = splits;
+  const int fv = forced_variant();
+  const int fs = forced_splits();
+  if (fv == -2 || fs == -2) return QMM_ERR_UNSUPPORTED;
+  if (v < 0 && fv >= 0) v = fv;
+  if (s < 0 && fs >= 0) s = fs;
+  if (v < 0) {
+    int ts = 1;
+    v = select_variant(a, &ts);
+    if (s < 0) s = ts;
+  }
+  const VariantDesc& d = kVariants[v];
+  if (s < 0) s = (d.family == kFamilyTma) ? rule_tma_cluster(a, d) : rule_splits(d, N, K, group_size);
+  if (d.family == kFamilyTma && (s < 1 || !tma_supported(a, s, d))) return QMM_ERR_UNSUPPORTED;
+  if (env_flag("QMM_LOG"))
+    std::fprintf(stderr, "qmm: M=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", M, N, K, bits, group_size, d.name, s);
+
+  // Host-side fault injection for the error-path tests: the launch reports a
+  // CUDA error without touching the device.
+  const char* inject = std::getenv("QMM_TEST_INJECT");
+  if (inject != nullptr && std::strcmp(inject, "launch_fail") == 0) return fail_cuda(cudaErrorLaunchFailure);
+
+  const cudaError_t e = (d.family == kFamilyMma)   ? launch_mma(a, d, s, st)
+                        : (d.family == kFamilyTma) ? launch_tma(a, d, s, st)
+                                                   : cudaErrorInvalidValue;
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
 }
 

@@ -16,15 +16,15 @@ struct CallArgs {
   int M, N, K, bits, gs, out_f32;
 };
 
-enum Family { kFamilyMma = 0, kFamilySimt = 1 };
+enum Family { kFamilyMma = 0, kFamilySimt = 1, kFamilyTma = 2 };
 
 // One kernel variant: a family and its CTA tiling.
 struct VariantDesc {
   const char* name;
   int family;
-  int R;   // m16 row tiles per warp (mma) / rows per warp (simt)
-  int WN;  // warps along N
-  int WK;  // warps along K (intra-CTA split-K)
+  int R;   // mma: m16 row tiles per warp; tma: ring stages
+  int WN;  // mma: warps along N; tma: consumer warps
+  int WK;  // mma: warps along K (intra-CTA split-K); tma: CTAs per SM targeted
 };
 
 const VariantDesc* variant_desc(int v);
@@ -36,7 +36,10 @@ int variant_rows_per_cta(const VariantDesc& d);
 // Launch variant `d` with `splits` CTAs per cluster along K.  Returns the CUDA
 // error of the launch (cudaSuccess when it was queued).
 cudaError_t launch_mma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
-cudaError_t launch_simt(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
+cudaError_t launch_tma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
+
+// Whether the TMA family can run (K, bits, gs) split across `csize` CTAs.
+bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -6,3 +6,8 @@
   X(2, 2, 4)             \
   X(1, 2, 4)             \
   X(4, 1, 8)
+
+//   tma:  X(W consumer warps, maximum ring stages)
+#define QMM_TMA_TILES(X) \
+  X(8, 8)                \
+  X(4, 8)

@@ -1,0 +1,172 @@
+// Host-side launcher of the warp-specialized TMA family (see qmm_tma.cuh).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "qmm_geometry.h"
+#include "qmm_internal.h"
+#include "qmm_tma.cuh"
+
+namespace qmm {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Maximum co-resident clusters of `csize` CTAs for a kernel and shared-memory
+// size, cached per (device, kernel, csize, smem).
+inline int max_active_clusters(const void* kern, int threads, int smem, int csize) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, int>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, kern, csize, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
+template <int BITS, int GS, int NB, int W, int S>
+cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaStream_t stream) {
+  using Cfg = TmaCfg<BITS, GS, NB, W, S>;
+  TmaParams p;
+  p.X = a.X;
+  p.S = a.S;
+  p.B = a.B;
+  p.Y = a.Y;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.G = a.K / GS;
+  p.out_f32 = a.out_f32;
+  if (!tma_geometry(a.K, BITS, GS, csize, &p.gp, &p.pw, &p.box_words, &p.nbox)) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 3) return cudaErrorInvalidValue;
+  p.tiles = (a.N + 15) / 16;
+
+  auto kern = qmm_tma_kernel<BITS, GS, NB, W, S>;
+  // Shared memory: what remains of the SM's budget for ctas_per_sm CTAs goes to
+  // the partial tiles of one reduction round.
+  int sm_bytes = 0, optin = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const int budget = tma_smem_budget(sm_bytes, optin, ctas_per_sm);
+  const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0);
+  const int per_tile = Cfg::MP * 16 * 4;
+  // Ring depth: up to S stages, leaving room for up to 16 partial tiles.
+  int stages = (budget - base.total - 16 * per_tile) / base.stage_bytes;
+  if (stages > S) stages = S;
+  if (stages < 2) stages = (budget - base.total - per_tile) / base.stage_bytes;
+  if (stages < 2) return cudaErrorInvalidValue;
+  if (stages > S) stages = S;
+  p.stages = stages;
+  p.wact = 1;  // largest divisor of the ring depth that is <= W
+  for (int d = 1; d <= W; ++d)
+    if (stages % d == 0) p.wact = d;
+  const int rt_max = (budget - base.total - stages * base.stage_bytes) / per_tile;
+  if (rt_max < 1) return cudaErrorInvalidValue;
+
+  static std::mutex mu;
+  static int smem_set = 0;
+  static bool nonportable = false;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (budget > smem_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+      if (e != cudaSuccess) return e;
+      smem_set = budget;
+    }
+    if (csize > 8 && !nonportable) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable = true;
+    }
+  }
+  // Clusters: as many as fit at the largest shared-memory size, no more than tiles.
+  int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget, csize);
+  if (ncl < 1) return cudaErrorInvalidConfiguration;
+  if (ncl > p.tiles) ncl = p.tiles;
+  p.ncl = ncl;
+  const int nt_max = (p.tiles + ncl - 1) / ncl;
+  p.rt = nt_max < rt_max ? nt_max : rt_max;
+  const int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt).total;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.box_words), 16u};
+  const cuuint32_t estride[2] = {1u, 1u};
+  const CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wq), gdim, gstride,
+                             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize, ncl, 1);
+  cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+}
+
+template <int BITS, int GS, int NB>
+cudaError_t launch_tma_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream) {
+#define QMM_TRY_TMA(w, s)                                                   \
+  if (d.WN == (w) && d.R == (s))                                            \
+    return launch_tma_impl<BITS, GS, NB, w, s>(a, csize, d.WK, stream);
+  QMM_TMA_TILES(QMM_TRY_TMA)
+#undef QMM_TRY_TMA
+  return cudaErrorInvalidValue;
+}
+
+template <int BITS, int GS>
+cudaError_t launch_tma_bg(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream) {
+  if (a.M <= 8) return launch_tma_tile<BITS, GS, 1>(a, d, csize, stream);
+  return launch_tma_tile<BITS, GS, 2>(a, d, csize, stream);
+}
+
+}  // namespace qmm

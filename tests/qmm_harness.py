@@ -26,13 +26,20 @@ class DeviceProblem:
         self.x = torch.from_numpy(p.x.view(np.int16)).to(device).view(torch.bfloat16)
         self.device = device
 
-    def run(self, M: int, out_dtype=None, variant: int = -1, splits: int = -1, out=None):
+    def run(self, M: int, out_dtype=None, variant: int = -1, splits: int = -1, out=None, allow_unsupported=False):
+        """Run through the C ABI.  With ``allow_unsupported``, a forced
+        (variant, splits) pair the shape cannot use returns None."""
         import torch
 
         out_dtype = out_dtype or torch.bfloat16
         x = self.x[:M].contiguous()
-        return binding.small_m(x, self.wq, self.s, self.b, self.p.bits, self.p.group_size, out=out,
-                               out_dtype=out_dtype, variant=variant, splits=splits)
+        try:
+            return binding.small_m(x, self.wq, self.s, self.b, self.p.bits, self.p.group_size, out=out,
+                                   out_dtype=out_dtype, variant=variant, splits=splits)
+        except binding.QmmError as e:
+            if allow_unsupported and e.status == 3:
+                return None
+            raise
 
 
 def to_f64(y) -> np.ndarray:

@@ -32,6 +32,19 @@ def variants():
     return list(range(len(binding.variant_names())))
 
 
+def is_tma(v):
+    return binding.variant_names()[v].startswith("tma")
+
+
+@pytest.fixture(autouse=True)
+def no_device_faults(torch_cuda):
+    """Every GPU test ends with a clean device status word (no bounded wait gave up)."""
+    binding.device_status(clear=True)
+    yield
+    torch_cuda.cuda.synchronize()
+    assert binding.device_status(clear=True) == 0
+
+
 # ------------------------------------------------------------- small shapes
 @pytest.mark.parametrize("bits,gs", BITS_GS)
 def test_small_shapes_all_m(torch_cuda, bits, gs):
@@ -41,27 +54,35 @@ def test_small_shapes_all_m(torch_cuda, bits, gs):
     p = synth.make_problem(7000 + bits * 1000 + gs, N, K, bits, gs)
     dp, ref = DeviceProblem(p), OracleRef(p)
     y_ref, a_ref = ref.full(16)
+    ran_tma = False
     for v in variants():
-        for splits in (1, 2):
+        for splits in ((1, 2, 4) if is_tma(v) else (1, 2)):
             for M in range(1, 17):
-                y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits)
+                y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits, allow_unsupported=is_tma(v))
+                if y is None:
+                    break
+                ran_tma |= is_tma(v)
                 assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"v{v} s{splits} M={M} f32")
-            y = dp.run(16, variant=v, splits=splits)
-            assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} M=16 bf16")
+            y = dp.run(16, variant=v, splits=splits, allow_unsupported=is_tma(v))
+            if y is not None:
+                assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} M=16 bf16")
+    assert ran_tma, "no TMA variant ran on this shape"
 
 
 @pytest.mark.parametrize("N", [1, 7, 15, 17, 129])
 @pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (4, 128)])
 def test_ragged_n_and_one_group(torch_cuda, N, bits, gs):
     torch = torch_cuda
-    for K in (gs, 3 * gs):
+    for K in (gs, 2 * gs, 6 * gs):
         p = synth.make_problem(8000 + N + K, N, K, bits, gs)
         dp, ref = DeviceProblem(p), OracleRef(p)
         y_ref, a_ref = ref.full(16)
         for v in variants():
             for M in (1, 8, 9, 16):
                 for splits in (1, 3):
-                    y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits)
+                    y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits, allow_unsupported=is_tma(v))
+                    if y is None:
+                        continue
                     assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"N={N} K={K} v{v} M={M} s{splits}")
 
 
@@ -78,8 +99,9 @@ def test_single_layer_workload_full(torch_cuda):
     for v in variants():
         for splits in (1, 2, 4, 8):
             for dt in (torch.bfloat16, torch.float32):
-                y = dp.run(4, out_dtype=dt, variant=v, splits=splits)
-                assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} {dt}")
+                y = dp.run(4, out_dtype=dt, variant=v, splits=splits, allow_unsupported=is_tma(v))
+                if y is not None:
+                    assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} {dt}")
 
 
 def test_m_sweep_5120_full(torch_cuda):
@@ -140,7 +162,9 @@ def test_determinism_and_batch_invariance(torch_cuda):
     dp, ref = DeviceProblem(p), OracleRef(p)
     y_ref, a_ref = ref.full(16)
     for v in variants():
-        first = dp.run(16, out_dtype=torch.float32, variant=v, splits=4)
+        first = dp.run(16, out_dtype=torch.float32, variant=v, splits=4, allow_unsupported=is_tma(v))
+        if first is None:
+            continue
         for _ in range(4):
             again = dp.run(16, out_dtype=torch.float32, variant=v, splits=4)
             assert torch.equal(first, again), f"variant {v} not deterministic"
@@ -165,7 +189,7 @@ def test_output_guard_bands(torch_cuda):
             buf = torch.full((M * 129 + 2 * pad,), -12345.0, dtype=dt, device="cuda")
             out = buf[pad:pad + M * 129].view(M, 129)
             for v in variants():
-                dp.run(M, out_dtype=dt, variant=v, splits=2, out=out)
+                dp.run(M, out_dtype=dt, variant=v, splits=2, out=out, allow_unsupported=is_tma(v))
                 torch.cuda.synchronize()
                 assert bool((buf[:pad] == -12345.0).all()) and bool((buf[-pad:] == -12345.0).all())
 
