@@ -79,8 +79,8 @@ qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, co
  * the number of CTAs that split K inside one thread-block cluster (splits = -1:
  * the table's or the variant's default; 1..16 otherwise).  A (variant, splits)
  * pair the shape cannot use returns QMM_ERR_UNSUPPORTED and launches nothing:
- * the "tma" variants need K/group_size even, divisible by splits with an even
- * quotient, and 4-byte aligned scales and biases.                              */
+ * the "tma" variants need K/group_size to be a multiple of 8 and of splits,
+ * and 16-byte aligned scales and biases.                                       */
 qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
                           int M, int N, int K, int bits, int group_size, void* Y,
                           int out_dtype, int variant, int splits, void* stream);

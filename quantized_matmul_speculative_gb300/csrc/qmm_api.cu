@@ -183,9 +183,9 @@ int variant_count() { return kNumVariants; }
 int variant_rows_per_cta(const VariantDesc& d) { return d.family == kFamilyMma ? 16 * d.R * d.WN : 16; }
 
 bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
-  int gp, pw, bw, nb;
-  if (!tma_geometry(a.K, a.bits, a.gs, csize, &gp, &pw, &bw, &nb)) return false;
-  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 3) return false;
+  int gp, pw, bw, nb, mbw;
+  if (!tma_geometry(a.K, a.bits, a.gs, csize, &gp, &pw, &bw, &nb, &mbw)) return false;
+  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return false;
   // the CTA's stages, activations and at least one partial tile must fit
   static int sm_bytes = 0, optin = 0;
   if (sm_bytes == 0) {
@@ -199,7 +199,7 @@ bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
     }
   }
   const int mp = a.M <= 8 ? 8 : 16;
-  const TmaLayout L(pw, gp, a.gs, mp, 2, 1);  // two stages and one partial tile at least
+  const TmaLayout L(pw, gp, a.gs, mp, 2, 1, d.WN, mbw);  // two stages, one tile, every warp a slot  // two stages, one tile
   return L.total <= tma_smem_budget(sm_bytes, optin, d.WK);
 }
 

@@ -7,6 +7,13 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+// Trace points: a build that defines QMM_TRACE_POINT(id) (for instance to
+// record %globaltimer per CTA) sees the phases of the kernels; the library
+// build compiles them to nothing.
+#ifndef QMM_TRACE_POINT
+#define QMM_TRACE_POINT(id) ((void)0)
+#endif
+
 namespace qmm {
 
 // ---------------------------------------------------------------------------
@@ -135,22 +142,25 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Test the phase with the given parity; a thread whose phase is not complete
+// is suspended by the hardware until it completes or `hint_ns` elapses, so a
+// waiting warp does not spin on the issue slots.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
 
 // Wait for the phase with the given parity to complete; gives up after
 // kWaitLimitNs, sets `flag` in the status word and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity, 20000u)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, 20000u)) return true;
+    __nanosleep(64);
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(&g_qmm_status, flag);
       return false;
@@ -207,6 +217,37 @@ __device__ __forceinline__ void ld_shared_words(uint32_t (&d)[N], const uint32_t
   } else {
     d[0] = p[0];
   }
+}
+
+// Packed fp32 FMA on two lanes of a register pair (sm_100+):
+// (a0, a1) = (b0 * c0 + a0, b1 * c1 + a1), each rounded once.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float b0, float b1, float c0, float c1) {
+  asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n mov.b64 c, {%4, %5};\n"
+      " fma.rn.f32x2 a, b, c, a;\n mov.b64 {%0, %1}, a;\n}\n"
+      : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// Split cluster barrier: arrive (release) now, wait (acquire) later.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+// 16-byte store into the shared memory of a CTA of this cluster; completion is
+// counted in bytes on that CTA's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      :: "r"(remote_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar) : "memory");
 }
 
 }  // namespace qmm

@@ -4,17 +4,27 @@
 
 namespace qmm {
 
-// Whether (K, bits, gs, csize) fits the TMA family's constraints: the K-piece
-// of each CTA holds an even number of groups, G is even, and the piece's
-// packed words split into equal TMA boxes of <= 256 words, 16-byte multiples,
-// each holding whole groups.
-inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, int* box_words, int* nbox) {
+// Whether (K, bits, gs, csize) fits the TMA family's constraints: G = K/gs is
+// a multiple of 8 (the fp16 scale/bias rows are 16-byte strided for TMA) and
+// of csize; the piece of each CTA (gp = G/csize groups) splits its packed
+// words into equal TMA boxes of <= 256 words, 16-byte multiples, each holding
+// whole groups.  *mbw = width in halves of the scale/bias TMA box: it starts
+// at the CTA's first group rounded down to 8 halves (16 bytes) and covers the
+// whole piece for every rank.
+inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, int* box_words, int* nbox,
+                         int* mbw) {
   const int G = K / gs;
-  if (G % 2 != 0 || G % csize != 0) return false;
+  if (G % 8 != 0 || G % csize != 0) return false;
   *gp = G / csize;
-  if (*gp % 2 != 0) return false;
   const int gw = gs * bits / 32;
   *pw = *gp * gw;
+  int lead = 0;  // largest (first group mod 8) over the ranks
+  for (int r = 0; r < csize; ++r) {
+    const int l = (r * *gp) % 8;
+    if (l > lead) lead = l;
+  }
+  *mbw = (lead + *gp + 7) / 8 * 8;
+  if (*mbw > 256) return false;
   for (int nb = 1; nb <= *gp; ++nb) {
     if (*gp % nb != 0) continue;
     const int bw = *pw / nb;
@@ -29,21 +39,36 @@ inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, i
 
 // Shared-memory layout of one CTA of the TMA family (bytes); the kernel and
 // the launcher both use it.  `mp` = activation rows held (8 or 16), `rt` =
-// partial tiles held for one reduction round.
+// tiles per reduction round, `slots` = partial tiles kept per tile.
 struct TmaLayout {
-  int stage_bytes, w_bytes, rsx;
-  int stage_off, x_off, xs_off, part_off, total;
-  __host__ __device__ TmaLayout(int pw, int gp, int gs, int mp, int stages, int rt) {
+  int stage_bytes, w_bytes, meta_bytes, rsx;
+  int stage_off, x_off, xs_off, part_off, recv_off, total;
+  // `recv_tiles` = tiles one CTA owns in the push reduction (0 = not used),
+  // `csize` = CTAs per cluster.
+  __host__ __device__ TmaLayout(int pw, int gp, int gs, int mp, int stages, int rt, int slots, int mbw,
+                                int recv_tiles = 0, int csize = 1) {
     w_bytes = 16 * pw * 4;
-    stage_bytes = (w_bytes + 16 * gp * 2 * 2 + 127) & ~127;  // + scales and biases, 16 rows x gp halves each
+    meta_bytes = 2 * 16 * mbw * 2;  // scales then biases, 16 rows x mbw halves each
+    stage_bytes = (w_bytes + meta_bytes + 127) & ~127;
     rsx = gp * gs + 4;
-    stage_off = 128;  // the 2 * stages mbarriers live below
+    stage_off = 256;  // mbarriers live below
     x_off = stage_off + stages * stage_bytes;
     xs_off = (x_off + mp * rsx * 2 + 15) & ~15;
-    part_off = (xs_off + mp * gp * 4 + 15) & ~15;
-    total = part_off + rt * mp * 16 * 4;
+    part_off = (xs_off + gp * mp * 4 + 15) & ~15;
+    recv_off = (part_off + rt * slots * mp * 16 * 4 + 15) & ~15;
+    total = recv_off + recv_tiles * csize * mp * 16 * 4;
   }
 };
+
+// Partial-tile slots per tile: with units = tiles * gp groups cut into w equal
+// ranges, a tile (gp units) meets at most ceil(gp / floor(units / w)) + 1
+// ranges, and never more than w.
+inline int tma_slots(int tiles, int gp, int w) {
+  const int per = (tiles * gp) / w;
+  if (per < 1) return w;
+  const int s = (gp + per - 1) / per + 1;
+  return s < w ? s : w;
+}
 
 // Shared memory one CTA may use when `ctas_per_sm` share an SM of
 // `smem_per_sm` bytes (1 KB per CTA is reserved by the hardware), capped at

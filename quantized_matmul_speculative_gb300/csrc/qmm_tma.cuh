@@ -14,22 +14,26 @@
 //    (groups [r*G/C, (r+1)*G/C)) of every one of those tiles.  The split of K
 //    across the CTAs of a block group follows "Fix family 2" (split K across
 //    the simdgroups) one level up.
-//  * Producer warp.  One warp streams tile after tile into a ring of S
-//    shared-memory stages: the tile's packed words through a 2-D TMA copy
-//    (cp.async.bulk.tensor), its fp16 scales and biases through 4-byte
-//    cp.async, both completing on the stage's "full" mbarrier.  Weights are
+//  * Producer warp.  One elected thread streams tile after tile into a ring
+//    of S shared-memory stages with 2-D TMA copies (cp.async.bulk.tensor):
+//    the tile's packed words, and its fp16 scales and biases (a box from the
+//    CTA's first group rounded down to 16 bytes; the overlap with the
+//    neighbouring rank is served by L2), all completing on the stage's
+//    "full" mbarrier.  Weights are
 //    read once per call whatever M is ("Stock qmv streams the weight matrix
 //    once per input row": the fix is to stream it once).
-//  * Consumer warps.  Each takes every wact-th tile of the cluster's range
-//    (wact = the largest divisor of S that is <= W; warp w owns the stages
-//    congruent to w mod wact, S/wact of them, as its private buffers),
-//    computes the tile's partial Y for its K-piece from the stage, releases
-//    the stage ("empty" mbarrier) and parks the partial in shared memory.
-//    The activations of the CTA's K-piece are staged once per kernel, in
-//    unpack order, with their per-group sums.
-//  * Reduction.  After the last tile, one cluster barrier; CTA r then sums
-//    the C partials of tiles r, r+C, ... over distributed shared memory in
-//    rank order and writes Y.  Deterministic, no atomics, no global scratch.
+//  * Consumer warps.  The (tile, group) work of a round is cut into W equal
+//    contiguous ranges, one per consumer warp, so every warp does the same
+//    number of whole groups (two at a time: two independent MMA chains) and
+//    pays per-tile costs about once.  Each warp parks its partial of every
+//    tile it meets in that tile's slot for it.  Every warp walks every stage
+//    in order and releases it ("empty" mbarrier, W arrivals).  The
+//    activations of the CTA's K-piece are staged once per kernel, in unpack
+//    order, with their per-group sums.
+//  * Reduction.  After the last tile, the partials of each tile are summed in
+//    slot (warp) order; one cluster barrier; CTA r then sums the C
+//    partials of tiles r, r+C, ... over distributed shared memory in rank
+//    order and writes Y.  Deterministic, no atomics, no global scratch.
 //  * Programmatic dependent launch.  The producer starts streaming weights
 //    before griddepcontrol.wait; activations are read and Y is written only
 //    after it, so a chain of calls overlaps one call's tail with the next
@@ -63,7 +67,10 @@ struct TmaParams {
   int ncl;        // clusters in the grid
   int rt;         // tiles per reduction round
   int stages;     // ring depth (<= template maximum)
-  int wact;       // consumer warps that take tiles (<= stages, see below)
+  int slots;      // partial-tile slots per tile (most warps that can meet one tile)
+  int push;       // 1: one reduction round, partials pushed to their owner (st.async)
+  int recv_tiles; // tiles one CTA owns in the push reduction
+  int mbw;        // scale/bias TMA box width in halves
   int out_f32;
 };
 
@@ -84,16 +91,18 @@ struct TmaCfg {
 
 template <int BITS, int GS, int NB, int W, int SMAX>
 __global__ void __launch_bounds__(32 * (W + 1), 1)
-qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
+qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
+               const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
   using C = TmaCfg<BITS, GS, NB, W, SMAX>;
-  static_assert(2 * SMAX * 8 <= 128, "mbarriers must fit below the stages");
+  static_assert((2 * SMAX + 1) * 8 <= 256, "mbarriers must fit below the stages");
   const int S = p.stages;
   extern __shared__ __align__(128) unsigned char tma_smem[];
   unsigned char* smem = tma_smem;
-  const TmaLayout L(p.pw, p.gp, GS, C::MP, p.stages, p.rt);
+  const TmaLayout L(p.pw, p.gp, GS, C::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, static_cast<int>(gridDim.x));
   const uint32_t sbase = smem_addr(smem);
   auto full_bar = [&](int s) { return sbase + 8u * s; };
   auto empty_bar = [&](int s) { return sbase + 8u * (SMAX + s); };
+  const uint32_t recv_bar = sbase + 8u * (2 * SMAX);
   uint16_t* Xs = reinterpret_cast<uint16_t*>(smem + L.x_off);
   float* xsum = reinterpret_cast<float*>(smem + L.xs_off);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
@@ -110,21 +119,30 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
   const int nrounds = (nt + p.rt - 1) / p.rt;
   const int g0 = rank * p.gp;  // first group of this CTA's K-piece
 
+  QMM_TRACE_POINT(0);
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), W);  // every consumer warp reads every stage
     }
+    mbar_init(recv_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
+  // Push reduction: tell the cluster this CTA's barriers exist (the matching
+  // wait comes right before the first remote store).
+  if (p.push) cluster_arrive();
   griddep_launch_dependents();
 
   if (warp == W) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) prefetch_tmap(&tmap);
-    const int meta_copies = 16 * p.gp;  // 4-byte words: 16 rows x (gp/2) x {scales, biases}
-    const int words_per_row = p.gp / 2;
+    if (lane == 0) {
+      prefetch_tmap(&tmap);
+      prefetch_tmap(&tmap_s);
+      prefetch_tmap(&tmap_b);
+    }
+    const int mx0 = (g0 / 8) * 8;  // first scale/bias column of the box (16-byte aligned)
+    const uint32_t tx_bytes = static_cast<uint32_t>(L.w_bytes + L.meta_bytes);
     int done_round = 0;
     for (int i = 0; i < nt; ++i) {
       // Before running S tiles into the next round, take part in the
@@ -135,30 +153,18 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
         ++done_round;
       }
       const int s = i % S;
-      if (i >= S) mbar_wait(empty_bar(s), ((i / S) - 1) & 1, kStatusTimeoutEmpty);
-      const int n0 = (t_begin + i) * 16;
-      unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
-      const uint32_t meta_dst = smem_addr(stage + L.w_bytes);
-      for (int c = lane; c < meta_copies; c += 32) {
-        const int arr = c / (8 * p.gp);          // 0: scales, 1: biases
-        const int rem = c - arr * 8 * p.gp;
-        const int row = rem / words_per_row;
-        const int wd = rem - row * words_per_row;
-        const int n = n0 + row;
-        if (n < p.N) {
-          const uint16_t* src = (arr ? p.B : p.S) + static_cast<int64_t>(n) * p.G + g0 + 2 * wd;
-          cp_async_4(meta_dst + 4u * (arr * 8 * p.gp + row * words_per_row + wd), src);
-        }
-      }
-      cp_async_mbar_arrive(full_bar(s));
-      __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(full_bar(s), static_cast<uint32_t>(L.w_bytes));
-        const uint32_t wdst = smem_addr(stage);
+        if (i >= S) mbar_wait(empty_bar(s), ((i / S) - 1) & 1, kStatusTimeoutEmpty);
+        const int n0 = (t_begin + i) * 16;
+        const uint32_t dst = smem_addr(smem + L.stage_off + s * L.stage_bytes);
+        mbar_arrive_expect_tx(full_bar(s), tx_bytes);
         for (int b = 0; b < p.nbox; ++b)
-          tma_load_2d(wdst + static_cast<uint32_t>(b * p.box_words * 4 * 16), &tmap,
-                      rank * p.pw + b * p.box_words, n0, full_bar(s));
+          tma_load_2d(dst + static_cast<uint32_t>(b * p.box_words * 4 * 16), &tmap, rank * p.pw + b * p.box_words,
+                      n0, full_bar(s));
+        tma_load_2d(dst + L.w_bytes, &tmap_s, mx0, n0, full_bar(s));
+        tma_load_2d(dst + L.w_bytes + L.meta_bytes / 2, &tmap_b, mx0, n0, full_bar(s));
       }
+      __syncwarp();
     }
     // Drain: every copy this warp issued has landed before the CTA can exit
     // (the consumers wait on the same phases; this only matters if one of
@@ -168,6 +174,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
       for (int i = first; i < nt; ++i) mbar_wait(full_bar(i % S), (i / S) & 1, kStatusTimeoutDrain);
     }
     __syncwarp();
+    if (p.push) {
+      cluster_wait();
+      return;
+    }
     while (done_round < nrounds) {
       cluster_sync_all();
       cluster_sync_all();
@@ -178,23 +188,23 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
 
   // -------------------------------------------------------------- consumers
   griddep_wait();  // X may be the previous call's output; Y may still be read by it
+  QMM_TRACE_POINT(1);
   const int cthreads = C::CONSUMER_THREADS;
-  // Stage this CTA's K-piece of X in unpack order, with per-group sums.
+  // Stage this CTA's K-piece of X in unpack order: within each word's chunk
+  // of 32/b codes, 32-bit element i holds (x[i], x[i + 16/b]).  One unit is
+  // (row m, group j): all its loads are issued first, then permuted, stored
+  // and summed (xsum[j * MP + m] = sum of x[m, k] over group j).
   for (int u = tid; u < C::MP * p.gp; u += cthreads) {
     const int m = u / p.gp;
-    const int jl = u - m * p.gp;
-    const int64_t k0 = static_cast<int64_t>(g0 + jl) * GS;
-    uint16_t* dst = Xs + m * L.rsx + jl * GS;
+    const int j = u - m * p.gp;
+    const uint16_t* src = p.X + static_cast<int64_t>(m) * p.K + static_cast<int64_t>(g0 + j) * GS;
+    uint4 v[GS / 8];
+#pragma unroll
+    for (int q8 = 0; q8 < GS / 8; ++q8) v[q8] = (m < p.M) ? ld_nc_v4(src + 8 * q8) : make_uint4(0, 0, 0, 0);
     float sum = 0.f;
 #pragma unroll
     for (int wc = 0; wc < C::GW; ++wc) {
-      uint4 v[C::VPW / 8];
-#pragma unroll
-      for (int qq = 0; qq < C::VPW / 8; ++qq) {
-        if (m < p.M) v[qq] = ld_nc_v4(p.X + static_cast<int64_t>(m) * p.K + k0 + wc * C::VPW + 8 * qq);
-        else v[qq] = make_uint4(0, 0, 0, 0);
-      }
-      const uint32_t* e = reinterpret_cast<const uint32_t*>(v);
+      const uint32_t* e = reinterpret_cast<const uint32_t*>(v + wc * (C::VPW / 8));
       uint32_t out[C::HALF];
 #pragma unroll
       for (int i = 0; i < C::HALF; ++i) {
@@ -203,112 +213,220 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
         out[i] = (i % 2 == 0) ? prmt_lo(a, b) : prmt_hi(a, b);
       }
 #pragma unroll
-      for (int j = 0; j < C::VPW / 2; ++j) sum += bf16_lo(e[j]) + bf16_hi(e[j]);
-      uint2* d2 = reinterpret_cast<uint2*>(dst + wc * C::VPW);
+      for (int i = 0; i < C::VPW / 2; ++i) sum += bf16_lo(e[i]) + bf16_hi(e[i]);
+      uint2* d2 = reinterpret_cast<uint2*>(Xs + m * L.rsx + j * GS + wc * C::VPW);
 #pragma unroll
       for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
     }
-    xsum[m * p.gp + jl] = sum;
+    xsum[j * C::MP + m] = sum;
   }
   asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");  // consumers only
+  QMM_TRACE_POINT(2);
 
   const int g = lane >> 2;
   const int t = lane & 3;
   const int wofs = (C::TPW == 1) ? t * C::LW : t / C::TPW;
+  // This thread's activation row g at the first code of its first word; for
+  // words shared by TPW threads, the first MMA step this thread feeds.
+  const int tsub = (C::TPW == 1) ? 0 : (t % C::TPW) * (C::SPW / C::TPW);
+  const uint16_t* xrow = Xs + g * L.rsx + wofs * C::VPW + ((C::TPW == 1) ? 0 : 4 * tsub);
+  const int gpb = p.box_words / C::GW;  // groups per TMA box
 
+  // MMAs of group j (packed words of this thread's rows at wp) into tmp (fresh per group).
+  auto group_mma = [&](const uint32_t* wp, int j, float (&tmp)[NB][4]) {
+    uint32_t wl[C::LW], wh[C::LW];
+    ld_shared_words<C::LW>(wl, wp);
+    ld_shared_words<C::LW>(wh, wp + 8 * p.box_words);
+    const uint16_t* xg = xrow + j * GS;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tmp[nb][e] = 0.f;
+#pragma unroll
+    for (int st = 0; st < C::STEPS; ++st) {
+      const int lwi = (C::TPW == 1) ? st / C::SPW : 0;
+      const int sub = (C::TPW == 1) ? st % C::SPW : tsub + st;
+      uint32_t a[4];
+      a[0] = unpack_pair<BITS>(wl[lwi], 2 * sub);
+      a[1] = unpack_pair<BITS>(wh[lwi], 2 * sub);
+      a[2] = unpack_pair<BITS>(wl[lwi], 2 * sub + 1);
+      a[3] = unpack_pair<BITS>(wh[lwi], 2 * sub + 1);
+      const int ko = (C::TPW == 1) ? (lwi * C::VPW + 4 * sub) : 4 * st;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint2 xb = *reinterpret_cast<const uint2*>(xg + nb * 8 * L.rsx + ko);
+        mma_bf16_16816(tmp[nb], a, xb.x, xb.y);
+      }
+    }
+  };
+  // Fold group j's scale and bias (b' = b - 128 s) into acc.
+  auto group_fold = [&](const uint16_t* meta, int j, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
+    const float s_lo = __half2float(__ushort_as_half(meta[j]));
+    const float s_hi = __half2float(__ushort_as_half(meta[8 * p.mbw + j]));
+    const float b_lo = fmaf(-128.f, s_lo, __half2float(__ushort_as_half(meta[16 * p.mbw + j])));
+    const float b_hi = fmaf(-128.f, s_hi, __half2float(__ushort_as_half(meta[24 * p.mbw + j])));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const float2 xs = *reinterpret_cast<const float2*>(xsum + j * C::MP + 8 * nb + 2 * t);
+      ffma2(acc[nb][0], acc[nb][1], b_lo, b_lo, xs.x, xs.y);
+      ffma2(acc[nb][0], acc[nb][1], s_lo, s_lo, tmp[nb][0], tmp[nb][1]);
+      ffma2(acc[nb][2], acc[nb][3], b_hi, b_hi, xs.x, xs.y);
+      ffma2(acc[nb][2], acc[nb][3], s_hi, s_hi, tmp[nb][2], tmp[nb][3]);
+    }
+  };
+
+  int s = 0, ph = 0;  // stage and phase parity of tile i
   for (int round = 0; round < nrounds; ++round) {
     const int i_lo = round * p.rt;
     const int i_hi = (i_lo + p.rt < nt) ? i_lo + p.rt : nt;
-    // Tile i goes to warp i % wact and stage i % S, and wact divides S: warp
-    // w owns the stages congruent to w mod wact, so the previous phase of the
-    // stage it waits on was its own earlier tile, already complete.  (An
-    // mbarrier parity wait cannot tell a phase from the one two ahead.)
-    for (int i = i_lo + warp; warp < p.wact && i < i_hi; i += p.wact) {
-      const int s = i % S;
-      mbar_wait(full_bar(s), (i / S) & 1, kStatusTimeoutFull);
-      const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
-      // Stage layout of the packed words: [box][16 rows][box_words]; a group
-      // never straddles two boxes (box_words is a multiple of the group's words).
-      const uint32_t* wbase = reinterpret_cast<const uint32_t*>(stage) + g * p.box_words + wofs;
-      const int gpb = p.box_words / C::GW;  // groups per box
-      const uint16_t* sc = reinterpret_cast<const uint16_t*>(stage + L.w_bytes);
-      const uint16_t* bi = sc + 16 * p.gp;
+    // The round's work, flattened to units (tile, group) in tile-major order,
+    // is cut into W contiguous, equal ranges; warp w takes [ua, ub).  A tile
+    // is computed by the warps whose ranges meet it; warp w parks its partial
+    // of the tile in slot w - (first warp meeting the tile).
+    const int U = (i_hi - i_lo) * p.gp;
+    const int ua = warp * U / W;
+    const int ub = (warp + 1) * U / W;
+    for (int i = i_lo; i < i_hi; ++i) {
+      // Every consumer warp waits on every stage in tile order and arrives on
+      // it, so a wait is never more than one phase ahead of its stage.
+      mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
+      QMM_TRACE_POINT(20 + i);
+      const int t0u = (i - i_lo) * p.gp;
+      const int ja = (ua > t0u ? ua : t0u) - t0u;
+      const int jb = (ub < t0u + p.gp ? ub : t0u + p.gp) - t0u;
+      if (ja < jb) {
+        const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
+        // Stage layout of the packed words: [box][16 rows][box_words]; a group
+        // never straddles two boxes (box_words is a multiple of the group's words).
+        const uint32_t* wstage = reinterpret_cast<const uint32_t*>(stage) + g * p.box_words + wofs;
+        // scale/bias boxes: [16 rows][mbw halves] each, the piece starting at column g0 % 8;
+        // meta[j] = scale(row g), meta[8 mbw + j] = scale(row g+8), then the biases.
+        const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + g * p.mbw + (g0 % 8);
 
-      float acc[NB][4];
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
-
-      for (int jl = 0; jl < p.gp; ++jl) {
-        const int bj = jl / gpb;
-        const uint32_t* wlo = wbase + bj * 16 * p.box_words + (jl - bj * gpb) * C::GW;
-        const uint32_t* whi = wlo + 8 * p.box_words;
-        uint32_t wl[C::LW], wh[C::LW];
-        ld_shared_words<C::LW>(wl, wlo);
-        ld_shared_words<C::LW>(wh, whi);
-        float tmp[NB][4];
+        float acc[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) tmp[nb][e] = 0.f;
-#pragma unroll
-        for (int st = 0; st < C::STEPS; ++st) {
-          const int lwi = (C::TPW == 1) ? st / C::SPW : 0;
-          const int sub = (C::TPW == 1) ? st % C::SPW : (t % C::TPW) * (C::SPW / C::TPW) + st;
-          const int wi = (C::TPW == 1) ? t * C::LW + lwi : t / C::TPW;
-          const int koff = (jl * C::GW + wi) * C::VPW + 4 * sub;
-          uint32_t a[4];
-          a[0] = unpack_pair<BITS>(wl[lwi], 2 * sub);
-          a[1] = unpack_pair<BITS>(wh[lwi], 2 * sub);
-          a[2] = unpack_pair<BITS>(wl[lwi], 2 * sub + 1);
-          a[3] = unpack_pair<BITS>(wh[lwi], 2 * sub + 1);
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb) {
-            const uint2 xb = *reinterpret_cast<const uint2*>(Xs + (8 * nb + g) * L.rsx + koff);
-            mma_bf16_16816(tmp[nb], a, xb.x, xb.y);
+          for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+        // word pointer of group j, advanced group by group across the boxes
+        int bj = ja / gpb, jj = ja - (ja / gpb) * gpb;
+        auto next_words = [&]() {
+          const uint32_t* wp = wstage + bj * 16 * p.box_words + jj * C::GW;
+          if (++jj == gpb) {
+            jj = 0;
+            ++bj;
           }
+          return wp;
+        };
+        int j = ja;
+        for (; j + 1 < jb; j += 2) {  // two independent MMA chains
+          float tmp0[NB][4], tmp1[NB][4];
+          const uint32_t* wp0 = next_words();
+          const uint32_t* wp1 = next_words();
+          group_mma(wp0, j, tmp0);
+          group_mma(wp1, j + 1, tmp1);
+          group_fold(meta, j, tmp0, acc);
+          group_fold(meta, j + 1, tmp1, acc);
         }
-        const float s_lo = __half2float(__ushort_as_half(sc[g * p.gp + jl]));
-        const float s_hi = __half2float(__ushort_as_half(sc[(g + 8) * p.gp + jl]));
-        const float b_lo = fmaf(-128.f, s_lo, __half2float(__ushort_as_half(bi[g * p.gp + jl])));
-        const float b_hi = fmaf(-128.f, s_hi, __half2float(__ushort_as_half(bi[(g + 8) * p.gp + jl])));
+        if (j < jb) {
+          float tmp0[NB][4];
+          group_mma(next_words(), j, tmp0);
+          group_fold(meta, j, tmp0, acc);
+        }
+        // slot of this warp in the tile: warps before it that meet the tile
+        int first = warp;
+        while (first > 0 && (first * U / W) > t0u) --first;
+        float* pt = part + ((i - i_lo) * p.slots + (warp - first)) * (C::MP * 16);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const float x0 = xsum[(8 * nb + 2 * t) * p.gp + jl];
-          const float x1 = xsum[(8 * nb + 2 * t + 1) * p.gp + jl];
-          acc[nb][0] = fmaf(s_lo, tmp[nb][0], fmaf(b_lo, x0, acc[nb][0]));
-          acc[nb][1] = fmaf(s_lo, tmp[nb][1], fmaf(b_lo, x1, acc[nb][1]));
-          acc[nb][2] = fmaf(s_hi, tmp[nb][2], fmaf(b_hi, x0, acc[nb][2]));
-          acc[nb][3] = fmaf(s_hi, tmp[nb][3], fmaf(b_hi, x1, acc[nb][3]));
+          const int m = 8 * nb + 2 * t;
+          pt[m * 16 + g] = acc[nb][0];
+          pt[(m + 1) * 16 + g] = acc[nb][1];
+          pt[m * 16 + g + 8] = acc[nb][2];
+          pt[(m + 1) * 16 + g + 8] = acc[nb][3];
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));
-      // partial tile: part[slot][m][row]
-      float* pt = part + (i - i_lo) * (C::MP * 16);
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int m = 8 * nb + 2 * t;
-        pt[m * 16 + g] = acc[nb][0];
-        pt[(m + 1) * 16 + g] = acc[nb][1];
-        pt[m * 16 + g + 8] = acc[nb][2];
-        pt[(m + 1) * 16 + g + 8] = acc[nb][3];
+      QMM_TRACE_POINT(8 + i);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
       }
     }
 
-    cluster_sync_all();  // every CTA's partials of this round are complete
-    // CTA `rank` reduces tiles rank, rank + C, ... of the round.
+    // Sum the partials of each tile of the round in slot order (4 elements at
+    // a time); with the push reduction, send the sum straight to the tile's
+    // owner (CTA slot % C of the cluster), else park it in slot 0.
+    asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");
     const int per_tile = p.M * 16;
+    const int nslots = i_hi - i_lo;
+    if (p.push) cluster_wait();  // every CTA of the cluster has initialized its barriers
+    for (int e4 = tid; e4 < nslots * (per_tile / 4); e4 += cthreads) {
+      const int slot = e4 / (per_tile / 4);
+      const int r = (e4 - slot * (per_tile / 4)) * 4;  // m * 16 + row
+      const int t0u = slot * p.gp;
+      // owner of the tile's first unit: the last warp whose range starts at or before it
+      int first = W - 1;
+      while (first > 0 && (first * U / W) > t0u) --first;
+      float* base = part + slot * p.slots * (C::MP * 16) + r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w2 = first; w2 < W; ++w2) {
+        const int a2 = w2 * U / W, b2 = (w2 + 1) * U / W;
+        if (a2 >= t0u + p.gp) break;
+        if (a2 < b2) {
+          const float4 x4 = *reinterpret_cast<const float4*>(base + (w2 - first) * C::MP * 16);
+          v.x += x4.x;
+          v.y += x4.y;
+          v.z += x4.z;
+          v.w += x4.w;
+        }
+      }
+      if (p.push) {
+        const uint32_t q = static_cast<uint32_t>(slot % csize);
+        const int o = slot / csize;
+        const uint32_t dst = smem_addr(smem + L.recv_off) + 4u * static_cast<uint32_t>((o * csize + rank) * C::MP * 16 + r);
+        st_async_v4(mapa_shared(dst, q), v, mapa_shared(recv_bar, q));
+      } else {
+        *reinterpret_cast<float4*>(base) = v;
+      }
+    }
+    if (p.push) {
+      // Owned tiles: slot % C == rank.  Wait for every peer's bytes, sum the
+      // C partials in rank order, write Y.
+      const int owned = (nslots > rank) ? (nslots - rank + csize - 1) / csize : 0;
+      if (tid == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(owned * csize * per_tile * 4));
+      if (owned > 0) mbar_wait(recv_bar, 0, kStatusTimeoutFull);
+      const float* recv = reinterpret_cast<const float*>(smem + L.recv_off);
+      for (int e = tid; e < owned * per_tile; e += cthreads) {
+        const int o = e / per_tile;
+        const int r = e - o * per_tile;
+        float v = 0.f;
+        for (int r2 = 0; r2 < csize; ++r2) v += recv[(o * csize + r2) * C::MP * 16 + r];
+        const int i = i_lo + o * csize + rank;
+        const int m = r >> 4;
+        const int n = (t_begin + i) * 16 + (r & 15);
+        if (n < p.N) {
+          const int64_t off = static_cast<int64_t>(m) * p.N + n;
+          if (p.out_f32) static_cast<float*>(p.Y)[off] = v;
+          else static_cast<__nv_bfloat16*>(p.Y)[off] = __float2bfloat16_rn(v);
+        }
+      }
+      QMM_TRACE_POINT(6);
+      return;  // one round only
+    }
+    QMM_TRACE_POINT(3);
+    cluster_sync_all();  // every CTA's partials of this round are complete
+    QMM_TRACE_POINT(4);
+    // CTA `rank` reduces tiles rank, rank + C, ... of the round.
     for (int i = i_lo + rank; i < i_hi; i += csize) {
       const int slot = i - i_lo;
       for (int e = tid; e < per_tile; e += cthreads) {
-        const int m = e >> 4;
-        const int row = e & 15;
-        const float* src = part + slot * (C::MP * 16) + m * 16 + row;
+        const float* src = part + slot * p.slots * (C::MP * 16) + e;
         float v = 0.f;
         for (int r2 = 0; r2 < csize; ++r2) v += ld_dsmem_f32(src, static_cast<uint32_t>(r2));
-        const int n = (t_begin + i) * 16 + row;
+        const int m = e >> 4;
+        const int n = (t_begin + i) * 16 + (e & 15);
         if (n < p.N) {
           const int64_t o = static_cast<int64_t>(m) * p.N + n;
           if (p.out_f32) static_cast<float*>(p.Y)[o] = v;
@@ -316,7 +434,9 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const TmaParams p) {
         }
       }
     }
+    QMM_TRACE_POINT(5);
     cluster_sync_all();  // peers are done reading this CTA's partials
+    QMM_TRACE_POINT(6);
   }
 }
 

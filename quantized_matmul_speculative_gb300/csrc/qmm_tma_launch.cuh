@@ -9,6 +9,7 @@
 
 #include "qmm_geometry.h"
 #include "qmm_internal.h"
+#include "qmm_tiles.h"
 #include "qmm_tma.cuh"
 
 namespace qmm {
@@ -72,10 +73,12 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.K = a.K;
   p.G = a.K / GS;
   p.out_f32 = a.out_f32;
-  if (!tma_geometry(a.K, BITS, GS, csize, &p.gp, &p.pw, &p.box_words, &p.nbox)) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 3) return cudaErrorInvalidValue;
+  if (!tma_geometry(a.K, BITS, GS, csize, &p.gp, &p.pw, &p.box_words, &p.nbox, &p.mbw)) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorInvalidValue;
   p.tiles = (a.N + 15) / 16;
 
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
   auto kern = qmm_tma_kernel<BITS, GS, NB, W, S>;
   // Shared memory: what remains of the SM's budget for ctas_per_sm CTAs goes to
   // the partial tiles of one reduction round.
@@ -84,21 +87,6 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   const int budget = tma_smem_budget(sm_bytes, optin, ctas_per_sm);
-  const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0);
-  const int per_tile = Cfg::MP * 16 * 4;
-  // Ring depth: up to S stages, leaving room for up to 16 partial tiles.
-  int stages = (budget - base.total - 16 * per_tile) / base.stage_bytes;
-  if (stages > S) stages = S;
-  if (stages < 2) stages = (budget - base.total - per_tile) / base.stage_bytes;
-  if (stages < 2) return cudaErrorInvalidValue;
-  if (stages > S) stages = S;
-  p.stages = stages;
-  p.wact = 1;  // largest divisor of the ring depth that is <= W
-  for (int d = 1; d <= W; ++d)
-    if (stages % d == 0) p.wact = d;
-  const int rt_max = (budget - base.total - stages * base.stage_bytes) / per_tile;
-  if (rt_max < 1) return cudaErrorInvalidValue;
-
   static std::mutex mu;
   static int smem_set = 0;
   static bool nonportable = false;
@@ -115,26 +103,67 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
       nonportable = true;
     }
   }
-  // Clusters: as many as fit at the largest shared-memory size, no more than tiles.
+  // Clusters: as many as fit at the budget's shared-memory size, no more than tiles.
   int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget, csize);
   if (ncl < 1) return cudaErrorInvalidConfiguration;
   if (ncl > p.tiles) ncl = p.tiles;
   p.ncl = ncl;
   const int nt_max = (p.tiles + ncl - 1) / ncl;
-  p.rt = nt_max < rt_max ? nt_max : rt_max;
-  const int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt).total;
+  const int nt_min = p.tiles / ncl;
 
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
-  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.box_words), 16u};
-  const cuuint32_t estride[2] = {1u, 1u};
-  const CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wq), gdim, gstride,
-                             box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // Ring depth (up to S stages) and reduction round (up to all of a cluster's
+  // tiles): prefer one round; give up stages down to 4 for it.
+  const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
+  int stages = S, rt = 0, slots = 0;
+  for (; stages >= 2; --stages) {
+    const int room = budget - base.total - stages * base.stage_bytes;
+    for (rt = nt_max; rt >= 1; --rt) {
+      const int rest = nt_min % rt ? nt_min % rt : rt;  // smallest round a cluster can have
+      const int sa = tma_slots(rt, p.gp, W), sb = tma_slots(rest, p.gp, W);
+      slots = sa > sb ? sa : sb;
+      if (rt * slots * Cfg::MP * 16 * 4 <= room) break;
+    }
+    if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
+  }
+  if (stages < 2 || rt < 1) return cudaErrorInvalidValue;
+  p.stages = stages;
+  p.rt = rt;
+  p.slots = slots;
+  // One round for every cluster: reduce by pushing partials to their owners,
+  // if the receive buffer still fits.
+  p.push = 0;
+  p.recv_tiles = 0;
+  if (rt == nt_max) {
+    const int recv_tiles = (rt + csize - 1) / csize;
+    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, recv_tiles, csize).total <= budget) {
+      p.push = 1;
+      p.recv_tiles = recv_tiles;
+    }
+  }
+  const int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
+
+  CUtensorMap tmap, tmap_s, tmap_b;
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.box_words), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wq), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  for (int arr = 0; arr < 2; ++arr) {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.G), static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.G) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    void* base = const_cast<uint16_t*>(arr ? a.B : a.S);
+    if (encode(arr ? &tmap_b : &tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, ncl, 1);
@@ -150,7 +179,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tmap, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_s, tmap_b, p);
 }
 
 template <int BITS, int GS, int NB>

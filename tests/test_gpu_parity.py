@@ -73,7 +73,7 @@ def test_small_shapes_all_m(torch_cuda, bits, gs):
 @pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (4, 128)])
 def test_ragged_n_and_one_group(torch_cuda, N, bits, gs):
     torch = torch_cuda
-    for K in (gs, 2 * gs, 6 * gs):
+    for K in (gs, 2 * gs, 8 * gs):
         p = synth.make_problem(8000 + N + K, N, K, bits, gs)
         dp, ref = DeviceProblem(p), OracleRef(p)
         y_ref, a_ref = ref.full(16)
