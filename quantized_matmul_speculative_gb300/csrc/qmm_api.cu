@@ -115,16 +115,24 @@ int rule_splits(const VariantDesc& d, int N, int K, int gs) {
   return s;
 }
 
-// The sweep's entry for this exact shape, or -1.
+// The sweep's entry for this shape: exact M if measured, else the nearest
+// measured M of the same (N, K, bits, gs) that uses the same number of 8-row
+// activation tiles; -1 if the shape was not swept.
 int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
+  int best = -1, best_d = 1 << 30;
   for (int i = 0; i < kTableSize; ++i) {
     const TableEntry& e = kTable[i];
-    if (e.M == M && e.N == N && e.K == K && e.bits == bits && e.gs == gs && e.variant >= 0) {
-      *splits = e.splits;
-      return e.variant;
+    if (e.variant < 0 || e.N != N || e.K != K || e.bits != bits || e.gs != gs) continue;
+    if ((e.M <= 8) != (M <= 8)) continue;
+    const int d = e.M > M ? e.M - M : M - e.M;
+    if (d < best_d) {
+      best_d = d;
+      best = i;
     }
   }
-  return -1;
+  if (best < 0) return -1;
+  *splits = kTable[best].splits;
+  return kTable[best].variant;
 }
 
 // Cluster size for the TMA family on shapes the sweep did not cover: the

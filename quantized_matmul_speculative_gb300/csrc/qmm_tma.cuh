@@ -22,10 +22,11 @@
 //    "full" mbarrier.  Weights are
 //    read once per call whatever M is ("Stock qmv streams the weight matrix
 //    once per input row": the fix is to stream it once).
-//  * Consumer warps.  The (tile, group) work of a round is cut into W equal
-//    contiguous ranges, one per consumer warp, so every warp does the same
-//    number of whole groups (two at a time: two independent MMA chains) and
-//    pays per-tile costs about once.  Each warp parks its partial of every
+//  * Consumer warps.  Tiles are taken in windows of ws <= S/2 tiles (the
+//    next window streams in meanwhile); a window's (tile, group) work is cut
+//    into W equal contiguous ranges, one per consumer warp, so every warp
+//    does the same number of whole groups (two at a time: two independent
+//    MMA chains).  Each warp parks its partial of every
 //    tile it meets in that tile's slot for it.  Every warp walks every stage
 //    in order and releases it ("empty" mbarrier, W arrivals).  The
 //    activations of the CTA's K-piece are staged once per kernel, in unpack
@@ -68,6 +69,7 @@ struct TmaParams {
   int rt;         // tiles per reduction round
   int stages;     // ring depth (<= template maximum)
   int slots;      // partial-tile slots per tile (most warps that can meet one tile)
+  int ws;         // tiles per work window (the warps split each window's groups evenly)
   int push;       // 1: one reduction round, partials pushed to their owner (st.async)
   int recv_tiles; // tiles one CTA owns in the push reduction
   int mbw;        // scale/bias TMA box width in halves
@@ -90,7 +92,7 @@ struct TmaCfg {
 };
 
 template <int BITS, int GS, int NB, int W, int SMAX>
-__global__ void __launch_bounds__(32 * (W + 1), 1)
+__global__ void __launch_bounds__(32 * (W + 1), 2)
 qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
   using C = TmaCfg<BITS, GS, NB, W, SMAX>;
@@ -279,79 +281,84 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   for (int round = 0; round < nrounds; ++round) {
     const int i_lo = round * p.rt;
     const int i_hi = (i_lo + p.rt < nt) ? i_lo + p.rt : nt;
-    // The round's work, flattened to units (tile, group) in tile-major order,
-    // is cut into W contiguous, equal ranges; warp w takes [ua, ub).  A tile
-    // is computed by the warps whose ranges meet it; warp w parks its partial
-    // of the tile in slot w - (first warp meeting the tile).
-    const int U = (i_hi - i_lo) * p.gp;
-    const int ua = warp * U / W;
-    const int ub = (warp + 1) * U / W;
-    for (int i = i_lo; i < i_hi; ++i) {
-      // Every consumer warp waits on every stage in tile order and arrives on
-      // it, so a wait is never more than one phase ahead of its stage.
-      mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
-      QMM_TRACE_POINT(20 + i);
-      const int t0u = (i - i_lo) * p.gp;
-      const int ja = (ua > t0u ? ua : t0u) - t0u;
-      const int jb = (ub < t0u + p.gp ? ub : t0u + p.gp) - t0u;
-      if (ja < jb) {
-        const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
-        // Stage layout of the packed words: [box][16 rows][box_words]; a group
-        // never straddles two boxes (box_words is a multiple of the group's words).
-        const uint32_t* wstage = reinterpret_cast<const uint32_t*>(stage) + g * p.box_words + wofs;
-        // scale/bias boxes: [16 rows][mbw halves] each, the piece starting at column g0 % 8;
-        // meta[j] = scale(row g), meta[8 mbw + j] = scale(row g+8), then the biases.
-        const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + g * p.mbw + (g0 % 8);
+    // The round's tiles are processed in windows of ws tiles (ws <= S/2, so
+    // the next window streams in while this one is computed).  A window's
+    // work, flattened to units (tile, group) in tile-major order, is cut into
+    // W contiguous, equal ranges; warp w takes [ua, ub).  A tile is computed
+    // by the warps whose ranges meet it; warp w parks its partial of the tile
+    // in slot w - (first warp meeting the tile).
+    for (int w0 = i_lo; w0 < i_hi; w0 += p.ws) {
+      const int w1 = (w0 + p.ws < i_hi) ? w0 + p.ws : i_hi;
+      const int U = (w1 - w0) * p.gp;
+      const int ua = warp * U / W;
+      const int ub = (warp + 1) * U / W;
+      for (int i = w0; i < w1; ++i) {
+        // Every consumer warp waits on every stage in tile order and arrives
+        // on it, so a wait is never more than one phase ahead of its stage.
+        mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
+        QMM_TRACE_POINT(20 + i);
+        const int t0u = (i - w0) * p.gp;
+        const int ja = (ua > t0u ? ua : t0u) - t0u;
+        const int jb = (ub < t0u + p.gp ? ub : t0u + p.gp) - t0u;
+        if (ja < jb) {
+          const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
+          // Stage layout of the packed words: [box][16 rows][box_words]; a group
+          // never straddles two boxes (box_words is a multiple of the group's words).
+          const uint32_t* wstage = reinterpret_cast<const uint32_t*>(stage) + g * p.box_words + wofs;
+          // scale/bias boxes: [16 rows][mbw halves] each, the piece starting at column g0 % 8;
+          // meta[j] = scale(row g), meta[8 mbw + j] = scale(row g+8), then the biases.
+          const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + g * p.mbw + (g0 % 8);
 
-        float acc[NB][4];
+          float acc[NB][4];
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
+          for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
-        // word pointer of group j, advanced group by group across the boxes
-        int bj = ja / gpb, jj = ja - (ja / gpb) * gpb;
-        auto next_words = [&]() {
-          const uint32_t* wp = wstage + bj * 16 * p.box_words + jj * C::GW;
-          if (++jj == gpb) {
-            jj = 0;
-            ++bj;
+            for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+          // word pointer of group j, advanced group by group across the boxes
+          int bj = ja / gpb, jj = ja - (ja / gpb) * gpb;
+          auto next_words = [&]() {
+            const uint32_t* wp = wstage + bj * 16 * p.box_words + jj * C::GW;
+            if (++jj == gpb) {
+              jj = 0;
+              ++bj;
+            }
+            return wp;
+          };
+          int j = ja;
+          for (; j + 1 < jb; j += 2) {  // two independent MMA chains
+            float tmp0[NB][4], tmp1[NB][4];
+            const uint32_t* wp0 = next_words();
+            const uint32_t* wp1 = next_words();
+            group_mma(wp0, j, tmp0);
+            group_mma(wp1, j + 1, tmp1);
+            group_fold(meta, j, tmp0, acc);
+            group_fold(meta, j + 1, tmp1, acc);
           }
-          return wp;
-        };
-        int j = ja;
-        for (; j + 1 < jb; j += 2) {  // two independent MMA chains
-          float tmp0[NB][4], tmp1[NB][4];
-          const uint32_t* wp0 = next_words();
-          const uint32_t* wp1 = next_words();
-          group_mma(wp0, j, tmp0);
-          group_mma(wp1, j + 1, tmp1);
-          group_fold(meta, j, tmp0, acc);
-          group_fold(meta, j + 1, tmp1, acc);
-        }
-        if (j < jb) {
-          float tmp0[NB][4];
-          group_mma(next_words(), j, tmp0);
-          group_fold(meta, j, tmp0, acc);
-        }
-        // slot of this warp in the tile: warps before it that meet the tile
-        int first = warp;
-        while (first > 0 && (first * U / W) > t0u) --first;
-        float* pt = part + ((i - i_lo) * p.slots + (warp - first)) * (C::MP * 16);
+          if (j < jb) {
+            float tmp0[NB][4];
+            group_mma(next_words(), j, tmp0);
+            group_fold(meta, j, tmp0, acc);
+          }
+          // slot of this warp in the tile: warps before it that meet the tile
+          int first = warp;
+          while (first > 0 && (first * U / W) > t0u) --first;
+          float* pt = part + ((i - i_lo) * p.slots + (warp - first)) * (C::MP * 16);
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const int m = 8 * nb + 2 * t;
-          pt[m * 16 + g] = acc[nb][0];
-          pt[(m + 1) * 16 + g] = acc[nb][1];
-          pt[m * 16 + g + 8] = acc[nb][2];
-          pt[(m + 1) * 16 + g + 8] = acc[nb][3];
+          for (int nb = 0; nb < NB; ++nb) {
+            const int m = 8 * nb + 2 * t;
+            pt[m * 16 + g] = acc[nb][0];
+            pt[(m + 1) * 16 + g] = acc[nb][1];
+            pt[m * 16 + g + 8] = acc[nb][2];
+            pt[(m + 1) * 16 + g + 8] = acc[nb][3];
+          }
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
-      QMM_TRACE_POINT(8 + i);
-      if (++s == S) {
-        s = 0;
-        ph ^= 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+        QMM_TRACE_POINT(8 + i);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
 
@@ -365,7 +372,11 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     for (int e4 = tid; e4 < nslots * (per_tile / 4); e4 += cthreads) {
       const int slot = e4 / (per_tile / 4);
       const int r = (e4 - slot * (per_tile / 4)) * 4;  // m * 16 + row
-      const int t0u = slot * p.gp;
+      // the tile's window and its units
+      const int w0 = (slot / p.ws) * p.ws;
+      const int w1 = (w0 + p.ws < nslots) ? w0 + p.ws : nslots;
+      const int U = (w1 - w0) * p.gp;
+      const int t0u = (slot - w0) * p.gp;
       // owner of the tile's first unit: the last warp whose range starts at or before it
       int first = W - 1;
       while (first > 0 && (first * U / W) > t0u) --first;

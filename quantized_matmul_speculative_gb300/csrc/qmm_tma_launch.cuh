@@ -3,6 +3,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -111,16 +113,23 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   const int nt_max = (p.tiles + ncl - 1) / ncl;
   const int nt_min = p.tiles / ncl;
 
-  // Ring depth (up to S stages) and reduction round (up to all of a cluster's
-  // tiles): prefer one round; give up stages down to 4 for it.
+  // Ring depth (up to S stages), work window (half the ring) and reduction
+  // round (up to all of a cluster's tiles): prefer one round; give up stages
+  // down to 4 for it.
   const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
-  int stages = S, rt = 0, slots = 0;
+  int stages = S, rt = 0, slots = 0, ws = 1;
   for (; stages >= 2; --stages) {
+    ws = stages / 2 > 0 ? stages / 2 : 1;
     const int room = budget - base.total - stages * base.stage_bytes;
     for (rt = nt_max; rt >= 1; --rt) {
-      const int rest = nt_min % rt ? nt_min % rt : rt;  // smallest round a cluster can have
-      const int sa = tma_slots(rt, p.gp, W), sb = tma_slots(rest, p.gp, W);
-      slots = sa > sb ? sa : sb;
+      // windows of a round: full ones of ws tiles and one remainder
+      int sl = 0;
+      for (int n : {ws < rt ? ws : rt, rt % ws, nt_min % rt % ws, (nt_min % rt ? nt_min % rt : rt) % ws}) {
+        if (n <= 0) continue;
+        const int x = tma_slots(n, p.gp, W);
+        sl = x > sl ? x : sl;
+      }
+      slots = sl;
       if (rt * slots * Cfg::MP * 16 * 4 <= room) break;
     }
     if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
@@ -129,6 +138,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.stages = stages;
   p.rt = rt;
   p.slots = slots;
+  p.ws = ws;
   // One round for every cluster: reduce by pushing partials to their owners,
   // if the receive buffer still fits.
   p.push = 0;
@@ -165,6 +175,15 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
       return cudaErrorInvalidValue;
   }
 
+  {
+    const char* lg = std::getenv("QMM_LOG");
+    if (lg != nullptr && lg[0] != '\0' && lg[0] != '0')
+      std::fprintf(stderr,
+                   "qmm tma: grid %dx%d (clusters of %d) threads %d smem %d budget %d stages %d window %d round %d slots %d "
+                   "push %d gp %d pw %d boxes %d\n",
+                   csize, ncl, csize, Cfg::THREADS, smem, budget, p.stages, p.ws, p.rt, p.slots, p.push, p.gp,
+                   p.pw, p.nbox);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, ncl, 1);
   cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
