@@ -25,16 +25,25 @@ inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, i
   }
   *mbw = (lead + *gp + 7) / 8 * 8;
   if (*mbw > 256) return false;
+  // Prefer a box width whose rows fall on different shared-memory banks
+  // (width = 8, 16 or 24 words mod 32): the 8 fragment rows of a warp then
+  // spread over the banks instead of all hitting the same ones.
+  int fallback = 0;
   for (int nb = 1; nb <= *gp; ++nb) {
     if (*gp % nb != 0) continue;
     const int bw = *pw / nb;
-    if (bw <= 256 && bw % 4 == 0) {
+    if (bw > 256 || bw % 4 != 0) continue;
+    if (bw % 32 != 0) {
       *nbox = nb;
       *box_words = bw;
       return true;
     }
+    if (fallback == 0) fallback = nb;
   }
-  return false;
+  if (fallback == 0) return false;
+  *nbox = fallback;
+  *box_words = *pw / fallback;
+  return true;
 }
 
 // Shared-memory layout of one CTA of the TMA family (bytes); the kernel and

@@ -80,7 +80,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", required=True)
     ap.add_argument("--quick", action="store_true")
-    ap.add_argument("--only-n", type=int, default=None)
+    ap.add_argument("--only-n", type=int, default=None, help="sweep only shapes with this N (repeatable)",
+                    action="append")
     args = ap.parse_args()
     import torch
 
@@ -92,7 +93,7 @@ def main():
     names = binding.variant_names()
     out = open(args.out, "w")
     for N, K, bits, gs, ms in shapes(args.quick):
-        if args.only_n and N != args.only_n:
+        if args.only_n and N not in args.only_n:
             continue
         p = synth.make_problem(1, N, K, bits, gs)
         call_b = workloads.call_bytes(N, K, bits, gs)
