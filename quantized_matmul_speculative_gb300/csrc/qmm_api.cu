@@ -54,9 +54,10 @@ const VariantDesc kVariants[] = {
     {"mma_r2_wn2_wk4", kFamilyMma, 2, 2, 4},
     {"mma_r1_wn2_wk4", kFamilyMma, 1, 2, 4},
     {"mma_r4_wn1_wk8", kFamilyMma, 4, 1, 8},
-    {"tma_w8_2cta", kFamilyTma, 8, 8, 2},
-    {"tma_w4_2cta", kFamilyTma, 8, 4, 2},
-    {"tma_w8_1cta", kFamilyTma, 8, 8, 1},
+    {"tma_w8_2cta", kFamilyTma, 16, 8, 2},
+    {"tma_w4_2cta", kFamilyTma, 16, 4, 2},
+    {"tma_w8_1cta", kFamilyTma, 16, 8, 1},
+    {"tma_w16_1cta", kFamilyTma, 16, 16, 1},
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces

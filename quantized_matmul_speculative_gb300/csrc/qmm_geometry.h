@@ -4,6 +4,40 @@
 
 namespace qmm {
 
+// Shared-memory wavefronts of one warp's load of its weight fragment words
+// from a stage whose rows are `bw` words apart, for `gw` words per group: lane
+// (g = lane / 4, t = lane % 4) reads row g, lw = max(1, gw / 4) consecutive
+// words at word t * lw (or word t / (4 / gw) when several lanes share a word).
+// A 4-, 8- or 16-byte load is served 32, 16 or 8 lanes at a time; each such
+// phase takes as many wavefronts as the most distinct words on one bank.
+inline int tma_box_wavefronts(int bw, int gw) {
+  const int lw = gw >= 4 ? gw / 4 : 1;
+  const int tpw = gw >= 4 ? 1 : 4 / gw;
+  const int per_phase = 32 / lw;
+  int total = 0;
+  for (int p0 = 0; p0 < 32; p0 += per_phase) {
+    int words[32 * 4];
+    int n = 0;
+    for (int lane = p0; lane < p0 + per_phase; ++lane) {
+      const int g = lane >> 2, t = lane & 3;
+      const int w0 = g * bw + (tpw == 1 ? t * lw : t / tpw);
+      for (int k = 0; k < lw; ++k) {
+        bool seen = false;
+        for (int i = 0; i < n; ++i) seen = seen || words[i] == w0 + k;
+        if (!seen) words[n++] = w0 + k;
+      }
+    }
+    int worst = 0;
+    for (int bank = 0; bank < 32; ++bank) {
+      int c = 0;
+      for (int i = 0; i < n; ++i) c += (words[i] % 32 == bank);
+      worst = c > worst ? c : worst;
+    }
+    total += worst;
+  }
+  return total;
+}
+
 // Whether (K, bits, gs, csize) fits the TMA family's constraints: G = K/gs is
 // a multiple of 8 (the fp16 scale/bias rows are 16-byte strided for TMA) and
 // of csize; the piece of each CTA (gp = G/csize groups) splits its packed
@@ -25,24 +59,22 @@ inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, i
   }
   *mbw = (lead + *gp + 7) / 8 * 8;
   if (*mbw > 256) return false;
-  // Prefer a box width whose rows fall on different shared-memory banks
-  // (width = 8, 16 or 24 words mod 32): the 8 fragment rows of a warp then
-  // spread over the banks instead of all hitting the same ones.
-  int fallback = 0;
+  // Among the box widths, take the one whose weight-fragment loads need the
+  // fewest shared-memory wavefronts (fewer boxes on ties).
+  int best = 0, best_cost = 1 << 30;
   for (int nb = 1; nb <= *gp; ++nb) {
     if (*gp % nb != 0) continue;
     const int bw = *pw / nb;
     if (bw > 256 || bw % 4 != 0) continue;
-    if (bw % 32 != 0) {
-      *nbox = nb;
-      *box_words = bw;
-      return true;
+    const int cost = tma_box_wavefronts(bw, gw);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = nb;
     }
-    if (fallback == 0) fallback = nb;
   }
-  if (fallback == 0) return false;
-  *nbox = fallback;
-  *box_words = *pw / fallback;
+  if (best == 0) return false;
+  *nbox = best;
+  *box_words = *pw / best;
   return true;
 }
 
@@ -60,7 +92,7 @@ struct TmaLayout {
     meta_bytes = 2 * 16 * mbw * 2;  // scales then biases, 16 rows x mbw halves each
     stage_bytes = (w_bytes + meta_bytes + 127) & ~127;
     rsx = gp * gs + 4;
-    stage_off = 256;  // mbarriers live below
+    stage_off = 512;  // mbarriers live below
     x_off = stage_off + stages * stage_bytes;
     xs_off = (x_off + mp * rsx * 2 + 15) & ~15;
     part_off = (xs_off + gp * mp * 4 + 15) & ~15;

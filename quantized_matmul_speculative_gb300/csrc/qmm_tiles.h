@@ -9,5 +9,6 @@
 
 //   tma:  X(W consumer warps, maximum ring stages)
 #define QMM_TMA_TILES(X) \
-  X(8, 8)                \
-  X(4, 8)
+  X(8, 16)               \
+  X(4, 16)               \
+  X(16, 16)

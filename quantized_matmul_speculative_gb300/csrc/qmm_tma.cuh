@@ -70,6 +70,8 @@ struct TmaParams {
   int stages;     // ring depth (<= template maximum)
   int slots;      // partial-tile slots per tile (most warps that can meet one tile)
   int ws;         // tiles per work window (the warps split each window's groups evenly)
+  int single;     // 1: every tile has a stage of its own (no stage is reused): a warp
+                  // waits only on the tiles it computes and never releases a stage
   int push;       // 1: one reduction round, partials pushed to their owner (st.async)
   int recv_tiles; // tiles one CTA owns in the push reduction
   int mbw;        // scale/bias TMA box width in halves
@@ -92,11 +94,11 @@ struct TmaCfg {
 };
 
 template <int BITS, int GS, int NB, int W, int SMAX>
-__global__ void __launch_bounds__(32 * (W + 1), 2)
+__global__ void __launch_bounds__(32 * (W + 1), (W <= 8) ? 2 : 1)
 qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
   using C = TmaCfg<BITS, GS, NB, W, SMAX>;
-  static_assert((2 * SMAX + 1) * 8 <= 256, "mbarriers must fit below the stages");
+  static_assert((2 * SMAX + 1) * 8 <= 512, "mbarriers must fit below the stages");
   const int S = p.stages;
   extern __shared__ __align__(128) unsigned char tma_smem[];
   unsigned char* smem = tma_smem;
@@ -193,34 +195,60 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   QMM_TRACE_POINT(1);
   const int cthreads = C::CONSUMER_THREADS;
   // Stage this CTA's K-piece of X in unpack order: within each word's chunk
-  // of 32/b codes, 32-bit element i holds (x[i], x[i + 16/b]).  One unit is
-  // (row m, group j): all its loads are issued first, then permuted, stored
-  // and summed (xsum[j * MP + m] = sum of x[m, k] over group j).
-  for (int u = tid; u < C::MP * p.gp; u += cthreads) {
-    const int m = u / p.gp;
-    const int j = u - m * p.gp;
-    const uint16_t* src = p.X + static_cast<int64_t>(m) * p.K + static_cast<int64_t>(g0 + j) * GS;
-    uint4 v[GS / 8];
+  // of 32/b codes, 32-bit element i holds (x[i], x[i + 16/b]).  A task is one
+  // such chunk of one row (16 or 32 bytes); the tasks of a unit (row m,
+  // group j) sit in adjacent lanes, which add up their sums by shuffles
+  // (xsum[j * MP + m] = sum of x[m, k] over group j).  Loads are issued a
+  // batch at a time before any is used.  Rows m >= M are not staged: an MMA
+  // output column depends only on its own activation row, and the columns of
+  // rows >= M are never stored.
+  {
+    constexpr int CH = GS / C::VPW;  // tasks per unit (2..16, divides 32)
+    constexpr int TQ = C::VPW / 8;   // 16-byte loads per task
+    constexpr int BATCH = 4;
+    static_assert(32 % CH == 0, "a unit's tasks must share a warp");
+    const int ntask = p.M * p.gp * CH;
+    for (int base = 0; base < ntask; base += BATCH * cthreads) {
+      uint4 v[BATCH][TQ];
 #pragma unroll
-    for (int q8 = 0; q8 < GS / 8; ++q8) v[q8] = (m < p.M) ? ld_nc_v4(src + 8 * q8) : make_uint4(0, 0, 0, 0);
-    float sum = 0.f;
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * cthreads + tid;
+        const int unit = u / CH;
+        const int m = unit / p.gp;
+        const int j = unit - m * p.gp;
+        const uint16_t* src =
+            p.X + static_cast<int64_t>(m) * p.K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * C::VPW;
 #pragma unroll
-    for (int wc = 0; wc < C::GW; ++wc) {
-      const uint32_t* e = reinterpret_cast<const uint32_t*>(v + wc * (C::VPW / 8));
-      uint32_t out[C::HALF];
-#pragma unroll
-      for (int i = 0; i < C::HALF; ++i) {
-        const uint32_t a = e[i / 2];
-        const uint32_t b = e[(i + C::HALF) / 2];
-        out[i] = (i % 2 == 0) ? prmt_lo(a, b) : prmt_hi(a, b);
+        for (int q8 = 0; q8 < TQ; ++q8) v[b][q8] = (u < ntask) ? ld_nc_v4(src + 8 * q8) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int i = 0; i < C::VPW / 2; ++i) sum += bf16_lo(e[i]) + bf16_hi(e[i]);
-      uint2* d2 = reinterpret_cast<uint2*>(Xs + m * L.rsx + j * GS + wc * C::VPW);
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * cthreads + tid;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
+        const int m = unit / p.gp;
+        const int j = unit - m * p.gp;
+        const uint32_t* e = reinterpret_cast<const uint32_t*>(v[b]);
+        float sum = 0.f;
 #pragma unroll
-      for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
+        for (int i = 0; i < C::VPW / 2; ++i) sum += bf16_lo(e[i]) + bf16_hi(e[i]);
+        if (u < ntask) {
+          uint32_t out[C::HALF];
+#pragma unroll
+          for (int i = 0; i < C::HALF; ++i) {
+            const uint32_t a = e[i / 2];
+            const uint32_t bb = e[(i + C::HALF) / 2];
+            out[i] = (i % 2 == 0) ? prmt_lo(a, bb) : prmt_hi(a, bb);
+          }
+          uint2* d2 = reinterpret_cast<uint2*>(Xs + m * L.rsx + j * GS + c * C::VPW);
+#pragma unroll
+          for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
+        }
+#pragma unroll
+        for (int o = CH / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (u < ntask && c == 0) xsum[j * C::MP + m] = sum;
+      }
     }
-    xsum[j * C::MP + m] = sum;
   }
   asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");  // consumers only
   QMM_TRACE_POINT(2);
@@ -293,13 +321,22 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       const int ua = warp * U / W;
       const int ub = (warp + 1) * U / W;
       for (int i = w0; i < w1; ++i) {
-        // Every consumer warp waits on every stage in tile order and arrives
-        // on it, so a wait is never more than one phase ahead of its stage.
-        mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
-        QMM_TRACE_POINT(20 + i);
         const int t0u = (i - w0) * p.gp;
         const int ja = (ua > t0u ? ua : t0u) - t0u;
         const int jb = (ub < t0u + p.gp ? ub : t0u + p.gp) - t0u;
+        if (p.single && ja >= jb) {  // a stage of its own that this warp does not read
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+          continue;
+        }
+        // With stage reuse, every consumer warp waits on every stage in tile
+        // order and arrives on it, so a wait is never more than one phase
+        // ahead of its stage.
+        QMM_TRACE_POINT(40);
+        mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
+        QMM_TRACE_POINT(20 + i);
         if (ja < jb) {
           const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
           // Stage layout of the packed words: [box][16 rows][box_words]; a group
@@ -339,6 +376,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
             group_mma(next_words(), j, tmp0);
             group_fold(meta, j, tmp0, acc);
           }
+          QMM_TRACE_POINT(41);
           // slot of this warp in the tile: warps before it that meet the tile
           int first = warp;
           while (first > 0 && (first * U / W) > t0u) --first;
@@ -352,8 +390,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
             pt[(m + 1) * 16 + g + 8] = acc[nb][3];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
+        if (!p.single) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(s));
+        }
         QMM_TRACE_POINT(8 + i);
         if (++s == S) {
           s = 0;

@@ -113,28 +113,48 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   const int nt_max = (p.tiles + ncl - 1) / ncl;
   const int nt_min = p.tiles / ncl;
 
-  // Ring depth (up to S stages), work window (half the ring) and reduction
-  // round (up to all of a cluster's tiles): prefer one round; give up stages
-  // down to 4 for it.
   const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
-  int stages = S, rt = 0, slots = 0, ws = 1;
-  for (; stages >= 2; --stages) {
-    ws = stages / 2 > 0 ? stages / 2 : 1;
-    const int room = budget - base.total - stages * base.stage_bytes;
-    for (rt = nt_max; rt >= 1; --rt) {
-      // windows of a round: full ones of ws tiles and one remainder
-      int sl = 0;
-      for (int n : {ws < rt ? ws : rt, rt % ws, nt_min % rt % ws, (nt_min % rt ? nt_min % rt : rt) % ws}) {
-        if (n <= 0) continue;
-        const int x = tma_slots(n, p.gp, W);
-        sl = x > sl ? x : sl;
-      }
-      slots = sl;
-      if (rt * slots * Cfg::MP * 16 * 4 <= room) break;
+  // Partial slots per tile for rounds of rt tiles cut into windows of ws
+  // tiles: full windows and the remainders of either cluster size.
+  auto round_slots = [&](int ws, int rt) {
+    int sl = 0;
+    for (int n : {ws < rt ? ws : rt, rt % ws, nt_min % rt % ws, (nt_min % rt ? nt_min % rt : rt) % ws}) {
+      if (n <= 0) continue;
+      const int x = tma_slots(n, p.gp, W);
+      sl = x > sl ? x : sl;
     }
-    if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
+    return sl;
+  };
+  int stages = 0, rt = 0, slots = 0, ws = 1;
+  p.single = 0;
+  // Single shot: when every tile of a cluster fits, each gets a stage of its
+  // own, all copies are issued at once and the warps split all the tiles'
+  // groups evenly (one window, one round).
+  if (nt_max <= S) {
+    const int sl = round_slots(nt_max, nt_max);
+    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget) {
+      p.single = 1;
+      stages = nt_max;
+      ws = nt_max;
+      rt = nt_max;
+      slots = sl;
+    }
   }
-  if (stages < 2 || rt < 1) return cudaErrorInvalidValue;
+  if (!p.single) {
+    // Ring of up to 8 stages, work window half the ring, reduction round up
+    // to all of a cluster's tiles: prefer one round; give up stages down to 4
+    // for it.
+    for (stages = S < 8 ? S : 8; stages >= 2; --stages) {
+      ws = stages / 2 > 0 ? stages / 2 : 1;
+      const int room = budget - base.total - stages * base.stage_bytes;
+      for (rt = nt_max; rt >= 1; --rt) {
+        slots = round_slots(ws, rt);
+        if (rt * slots * Cfg::MP * 16 * 4 <= room) break;
+      }
+      if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
+    }
+    if (stages < 2 || rt < 1) return cudaErrorInvalidValue;
+  }
   p.stages = stages;
   p.rt = rt;
   p.slots = slots;
@@ -180,9 +200,9 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
     if (lg != nullptr && lg[0] != '\0' && lg[0] != '0')
       std::fprintf(stderr,
                    "qmm tma: grid %dx%d (clusters of %d) threads %d smem %d budget %d stages %d window %d round %d slots %d "
-                   "push %d gp %d pw %d boxes %d\n",
-                   csize, ncl, csize, Cfg::THREADS, smem, budget, p.stages, p.ws, p.rt, p.slots, p.push, p.gp,
-                   p.pw, p.nbox);
+                   "single %d push %d gp %d pw %d boxes %d\n",
+                   csize, ncl, csize, Cfg::THREADS, smem, budget, p.stages, p.ws, p.rt, p.slots, p.single, p.push,
+                   p.gp, p.pw, p.nbox);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, ncl, 1);
