@@ -100,6 +100,16 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   return v;
 }
 
+// s + lo(v) + hi(v) in fp32, evaluated as hi + (lo + s): the two bf16 halves
+// of v are widened exactly and each add rounds to fp32 (one mixed-precision
+// add per half, sm_100+).
+__device__ __forceinline__ float add_bf16x2_f32(uint32_t v, float s) {
+  float d;
+  asm("{\n .reg .b16 lo, hi;\n .reg .f32 t;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 t, lo, %2;\n"
+      " add.rn.f32.bf16 %0, hi, t;\n}\n"
+      : "=f"(d) : "r"(v), "f"(s));
+  return d;
+}
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

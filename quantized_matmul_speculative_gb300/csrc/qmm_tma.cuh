@@ -61,6 +61,7 @@ struct TmaParams {
   int M, N, K;
   int G;          // groups per row
   int gp;         // groups per K-piece (G / C), even
+  unsigned long long gp_magic;  // ceil(2^32 / gp): u / gp = (u * gp_magic) >> 32 for u * gp < 2^32
   int pw;         // packed words per row and K-piece
   int box_words;  // TMA box width (pw = nbox * box_words)
   int nbox;
@@ -214,7 +215,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * cthreads + tid;
         const int unit = u / CH;
-        const int m = unit / p.gp;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * p.gp_magic) >> 32);
         const int j = unit - m * p.gp;
         const uint16_t* src =
             p.X + static_cast<int64_t>(m) * p.K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * C::VPW;
@@ -226,12 +227,12 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         const int u = base + b * cthreads + tid;
         const int unit = u / CH;
         const int c = u - unit * CH;
-        const int m = unit / p.gp;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * p.gp_magic) >> 32);
         const int j = unit - m * p.gp;
         const uint32_t* e = reinterpret_cast<const uint32_t*>(v[b]);
         float sum = 0.f;
 #pragma unroll
-        for (int i = 0; i < C::VPW / 2; ++i) sum += bf16_lo(e[i]) + bf16_hi(e[i]);
+        for (int i = 0; i < C::VPW / 2; ++i) sum = add_bf16x2_f32(e[i], sum);
         if (u < ntask) {
           uint32_t out[C::HALF];
 #pragma unroll
@@ -262,11 +263,13 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const uint16_t* xrow = Xs + g * L.rsx + wofs * C::VPW + ((C::TPW == 1) ? 0 : 4 * tsub);
   const int gpb = p.box_words / C::GW;  // groups per TMA box
 
-  // MMAs of group j (packed words of this thread's rows at wp) into tmp (fresh per group).
-  auto group_mma = [&](const uint32_t* wp, int j, float (&tmp)[NB][4]) {
-    uint32_t wl[C::LW], wh[C::LW];
+  // Packed words of this thread's rows g and g + 8 for the group at wp.
+  auto load_words = [&](const uint32_t* wp, uint32_t (&wl)[C::LW], uint32_t (&wh)[C::LW]) {
     ld_shared_words<C::LW>(wl, wp);
     ld_shared_words<C::LW>(wh, wp + 8 * p.box_words);
+  };
+  // MMAs of group j (its packed words in wl, wh) into tmp (fresh per group).
+  auto group_mma_w = [&](const uint32_t (&wl)[C::LW], const uint32_t (&wh)[C::LW], int j, float (&tmp)[NB][4]) {
     const uint16_t* xg = xrow + j * GS;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
@@ -288,6 +291,11 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         mma_bf16_16816(tmp[nb], a, xb.x, xb.y);
       }
     }
+  };
+  auto group_mma = [&](const uint32_t* wp, int j, float (&tmp)[NB][4]) {
+    uint32_t wl[C::LW], wh[C::LW];
+    load_words(wp, wl, wh);
+    group_mma_w(wl, wh, j, tmp);
   };
   // Fold group j's scale and bias (b' = b - 128 s) into acc.
   auto group_fold = [&](const uint16_t* meta, int j, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
@@ -362,7 +370,24 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
             return wp;
           };
           int j = ja;
-          for (; j + 1 < jb; j += 2) {  // two independent MMA chains
+          // Four independent MMA chains per step with one activation tile, two
+          // with two tiles (register budget).
+          for (; NB == 1 && j + 3 < jb; j += 4) {
+            float tmp0[NB][4], tmp1[NB][4], tmp2[NB][4], tmp3[NB][4];
+            const uint32_t* wp0 = next_words();
+            const uint32_t* wp1 = next_words();
+            const uint32_t* wp2 = next_words();
+            const uint32_t* wp3 = next_words();
+            group_mma(wp0, j, tmp0);
+            group_mma(wp1, j + 1, tmp1);
+            group_mma(wp2, j + 2, tmp2);
+            group_mma(wp3, j + 3, tmp3);
+            group_fold(meta, j, tmp0, acc);
+            group_fold(meta, j + 1, tmp1, acc);
+            group_fold(meta, j + 2, tmp2, acc);
+            group_fold(meta, j + 3, tmp3, acc);
+          }
+          for (; j + 1 < jb; j += 2) {
             float tmp0[NB][4], tmp1[NB][4];
             const uint32_t* wp0 = next_words();
             const uint32_t* wp1 = next_words();

@@ -76,6 +76,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.G = a.K / GS;
   p.out_f32 = a.out_f32;
   if (!tma_geometry(a.K, BITS, GS, csize, &p.gp, &p.pw, &p.box_words, &p.nbox, &p.mbw)) return cudaErrorInvalidValue;
+  p.gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p.gp) - 1) / static_cast<unsigned long long>(p.gp);
   if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorInvalidValue;
   p.tiles = (a.N + 15) / 16;
 
