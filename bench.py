@@ -20,7 +20,6 @@ workload.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import re
@@ -36,11 +35,11 @@ ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
 from quantized_matmul_speculative_gb300 import synth, workloads  # noqa: E402
+from quantized_matmul_speculative_gb300.tuning.ncu_summary import kernel_hash  # noqa: E402
 
 METRIC = "weight GB/s and % of HBM peak per call vs M=1..16 (4-bit affine g64)"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("qmm_tma.cuh", "qmm_tma_launch.cuh", "qmm_device.cuh", "qmm_tiles.h", "qmm_geometry.h")
 
 
 # ------------------------------------------------------------------ helpers
@@ -52,13 +51,6 @@ def hbm_peak():
         except Exception:
             pass
     return FALLBACK_HBM_GBS, "fallback"
-
-
-def kernel_hash() -> str:
-    h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
-        h.update((ROOT / "quantized_matmul_speculative_gb300" / "csrc" / name).read_bytes())
-    return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload: str):

@@ -39,6 +39,14 @@ extern template cudaError_t launch_tma_bg<2, 32>(const CallArgs&, const VariantD
 extern template cudaError_t launch_tma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_tma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template <int BITS, int GS>
+cudaError_t launch_own_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<4, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<4, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+template <int BITS, int GS>
 unsigned int read_device_status(int clear);
 extern template unsigned int read_device_status<4, 32>(int);
 extern template unsigned int read_device_status<4, 64>(int);
@@ -49,7 +57,8 @@ extern template unsigned int read_device_status<2, 128>(int);
 
 namespace {
 
-// mma: {R, WN, WK}; tma: {stages, consumer warps, CTAs per SM}.
+// mma: {R, WN, WK}; tma: {stages, consumer warps, CTAs per SM}; own: {stages per warp,
+// consumer warps, CTAs per SM}.
 const VariantDesc kVariants[] = {
     {"mma_r2_wn2_wk4", kFamilyMma, 2, 2, 4},
     {"mma_r1_wn2_wk4", kFamilyMma, 1, 2, 4},
@@ -58,6 +67,10 @@ const VariantDesc kVariants[] = {
     {"tma_w4_2cta", kFamilyTma, 16, 4, 2},
     {"tma_w8_1cta", kFamilyTma, 16, 8, 1},
     {"tma_w16_1cta", kFamilyTma, 16, 16, 1},
+    {"tma_own_w8_d3_1cta", kFamilyOwn, 3, 8, 1},
+    {"tma_own_w16_d2_1cta", kFamilyOwn, 2, 16, 1},
+    {"tma_own_w8_d3_2cta", kFamilyOwn, 3, 8, 2},
+    {"tma_own_w4_d4_2cta", kFamilyOwn, 4, 4, 2},
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
@@ -212,6 +225,18 @@ bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
   return L.total <= tma_smem_budget(sm_bytes, optin, d.WK);
 }
 
+cudaError_t launch_own(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream, bool plan_only) {
+  switch (a.bits * 1000 + a.gs) {
+    case 4032: return launch_own_bg<4, 32>(a, d, splits, stream, plan_only);
+    case 4064: return launch_own_bg<4, 64>(a, d, splits, stream, plan_only);
+    case 4128: return launch_own_bg<4, 128>(a, d, splits, stream, plan_only);
+    case 2032: return launch_own_bg<2, 32>(a, d, splits, stream, plan_only);
+    case 2064: return launch_own_bg<2, 64>(a, d, splits, stream, plan_only);
+    case 2128: return launch_own_bg<2, 128>(a, d, splits, stream, plan_only);
+    default: return cudaErrorNotSupported;
+  }
+}
+
 cudaError_t launch_tma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
   switch (a.bits * 1000 + a.gs) {
     case 4032: return launch_tma_bg<4, 32>(a, d, splits, stream);
@@ -355,8 +380,26 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
     if (s < 0) s = ts;
   }
   const VariantDesc& d = kVariants[v];
+  if (s < 0 && d.family == kFamilyOwn) {
+    // the first cluster size (4, 2, 1, 8) the planner accepts
+    for (int c : {4, 2, 1, 8}) {
+      const cudaError_t pe = launch_own(a, d, c, st, true);
+      if (pe == cudaSuccess) {
+        s = c;
+        break;
+      }
+      if (pe != cudaErrorNotSupported) return fail_cuda(pe);
+    }
+    if (s < 0) return QMM_ERR_UNSUPPORTED;
+  }
   if (s < 0) s = (d.family == kFamilyTma) ? rule_tma_cluster(a, d) : rule_splits(d, N, K, group_size);
   if (d.family == kFamilyTma && (s < 1 || !tma_supported(a, s, d))) return QMM_ERR_UNSUPPORTED;
+  if (d.family == kFamilyOwn) {
+    if (s < 1) return QMM_ERR_UNSUPPORTED;
+    const cudaError_t pe = launch_own(a, d, s, st, true);
+    if (pe == cudaErrorNotSupported) return QMM_ERR_UNSUPPORTED;
+    if (pe != cudaSuccess) return fail_cuda(pe);
+  }
   if (env_flag("QMM_LOG"))
     std::fprintf(stderr, "qmm: M=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", M, N, K, bits, group_size, d.name, s);
 
@@ -367,6 +410,7 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
 
   const cudaError_t e = (d.family == kFamilyMma)   ? launch_mma(a, d, s, st)
                         : (d.family == kFamilyTma) ? launch_tma(a, d, s, st)
+                        : (d.family == kFamilyOwn) ? launch_own(a, d, s, st, false)
                                                    : cudaErrorInvalidValue;
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
 }

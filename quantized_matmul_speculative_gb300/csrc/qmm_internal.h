@@ -16,14 +16,14 @@ struct CallArgs {
   int M, N, K, bits, gs, out_f32;
 };
 
-enum Family { kFamilyMma = 0, kFamilySimt = 1, kFamilyTma = 2 };
+enum Family { kFamilyMma = 0, kFamilySimt = 1, kFamilyTma = 2, kFamilyOwn = 3 };
 
 // One kernel variant: a family and its CTA tiling.
 struct VariantDesc {
   const char* name;
   int family;
-  int R;   // mma: m16 row tiles per warp; tma: ring stages
-  int WN;  // mma: warps along N; tma: consumer warps
+  int R;   // mma: m16 row tiles per warp; tma: ring stages; own: ring stages per warp
+  int WN;  // mma: warps along N; tma, own: consumer warps
   int WK;  // mma: warps along K (intra-CTA split-K); tma: CTAs per SM targeted
 };
 
@@ -37,6 +37,9 @@ int variant_rows_per_cta(const VariantDesc& d);
 // error of the launch (cudaSuccess when it was queued).
 cudaError_t launch_mma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
 cudaError_t launch_tma(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream);
+// With plan_only, nothing is launched: cudaSuccess if the shape can run,
+// cudaErrorNotSupported if it cannot.
+cudaError_t launch_own(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream, bool plan_only);
 
 // Whether the TMA family can run (K, bits, gs) split across `csize` CTAs.
 bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d);

@@ -1,6 +1,7 @@
 // One translation unit per (bits, group size), chosen by -DQMM_BITS / -DQMM_GS,
 // so the kernel instantiations compile in parallel.
 #include "qmm_mma_launch.cuh"
+#include "qmm_own_launch.cuh"
 #include "qmm_tma_launch.cuh"
 
 #ifndef QMM_BITS
@@ -27,4 +28,5 @@ unsigned int read_device_status(int clear) {
 template unsigned int read_device_status<QMM_BITS, QMM_GS>(int);
 template cudaError_t launch_mma_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template cudaError_t launch_tma_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template cudaError_t launch_own_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 }

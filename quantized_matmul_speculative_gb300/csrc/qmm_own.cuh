@@ -1,0 +1,347 @@
+// Warp-owned TMA kernel family ("own"): every consumer warp streams its own
+// work through a private ring of shared-memory stages, filled by 2-D TMA
+// copies that the warp issues itself.
+//
+// Work.  A cluster of C CTAs takes a contiguous range of 16-row tiles of W;
+// CTA `rank` of the cluster covers the K-piece of groups [rank*gp, (rank+1)*gp)
+// for all of them.  Within the CTA, a tile's K-piece is cut into kp parts of
+// gq groups; the (tile, part) units, tile-major, are split into W contiguous,
+// equal ranges, one per warp.  A warp loads its units one by one (the copies
+// of its first D-1 units are issued before the kernel waits for the previous
+// call on the stream: the weights never depend on it) and keeps the running
+// sum of the tile it is in.
+//
+// Reduction.  Tile i of the cluster belongs to CTA i mod C and, there, to warp
+// (i div C) mod W.  When a warp leaves a tile it pushes its partial sums (the
+// m16n8 accumulator fragments, 16 bytes per lane per activation tile) into a
+// slot of the owner's receive area with st.async, which counts the bytes on the
+// owner's mbarrier for that tile.  The owner waits for exactly the bytes of all
+// contributors (every CTA of the cluster, every warp whose range meets the
+// tile), adds the slots in a fixed order (CTA rank, then warp order) and
+// writes Y.  A tile with a single contributor in a cluster of one is written
+// directly.  No atomics: results are deterministic for a given launch shape.
+//
+// Every wait is bounded (mbar_wait); one that gives up sets a flag in the
+// device status word instead of hanging.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "qmm_device.cuh"
+#include "qmm_group.cuh"
+
+namespace qmm {
+
+struct OwnParams {
+  const uint16_t* __restrict__ X;
+  void* __restrict__ Y;
+  int M, N, K;
+  int gp;                       // groups per CTA K-piece (G / C)
+  unsigned long long gp_magic;  // ceil(2^32 / gp), for u / gp = (u * gp_magic) >> 32
+  int kp;                       // parts per tile K-piece
+  int gq;                       // groups per part (gp / kp)
+  int bw, nbox;                 // weight box width (words) and boxes per unit: nbox * bw = gq * words per group
+  int mbw;                      // scale/bias box width (halves)
+  int tiles;                    // 16-row tiles of W
+  int ncl;                      // clusters in the grid
+  int maxw;                     // receive slots per (tile, CTA): most warps that meet one tile
+  int owned_max;                // most tiles one CTA owns
+  int out_f32;
+};
+
+// First unit of warp w when U units are split into W contiguous ranges.
+__host__ __device__ inline int own_unit_begin(int w, int U, int W) {
+  return static_cast<int>((static_cast<long long>(w) * U) / W);
+}
+
+// Warps whose (non-empty) unit range meets tile i (units [i*kp, (i+1)*kp)),
+// and the position of warp w among them in *slot (-1 if w is not one).
+__host__ __device__ inline int own_contributors(int i, int kp, int U, int W, int w, int* slot) {
+  int n = 0;
+  *slot = -1;
+  const int lo = i * kp, hi = (i + 1) * kp;
+  for (int v = 0; v < W; ++v) {
+    const int a = own_unit_begin(v, U, W), b = own_unit_begin(v + 1, U, W);
+    if (a < b && a < hi && b > lo) {
+      if (v == w) *slot = n;
+      ++n;
+    }
+  }
+  return n;
+}
+
+// Shared-memory layout of one CTA (bytes).  Only the M staged activation
+// rows are reserved: the MMA fragments of rows M..mp-1 read whatever lies
+// after them (still inside the CTA's shared memory, which `total` guarantees),
+// and those rows only feed output columns that are never stored.
+struct OwnLayout {
+  int x_off, xs_off, ring_off, w_bytes, stage_bytes, recv_off, slot_bytes, total, rsx;
+  __host__ __device__ OwnLayout(int W, int D, int gp, int gs, int mp, int nb, int nbox, int bw, int mbw,
+                                int owned_max, int csize, int maxw, int m) {
+    const int nbar = W * D + owned_max;  // full barriers of the rings, then one per owned tile
+    rsx = gp * gs + 4;                   // X row stride (halves): 8 bytes past a 16-byte multiple
+    x_off = (8 * nbar + 127) & ~127;
+    xs_off = (x_off + m * rsx * 2 + 15) & ~15;
+    ring_off = (xs_off + gp * mp * 4 + 127) & ~127;
+    w_bytes = nbox * 16 * bw * 4;
+    stage_bytes = (w_bytes + 2 * 16 * mbw * 2 + 127) & ~127;
+    recv_off = ring_off + W * D * stage_bytes;
+    slot_bytes = 32 * 16 * nb;  // 32 lanes x 4 floats x activation tiles
+    total = recv_off + owned_max * csize * maxw * slot_bytes;
+    const int x_end = x_off + mp * rsx * 2;  // the reads of all mp rows stay inside
+    if (total < x_end) total = x_end;
+  }
+};
+
+template <int BITS, int GS, int NB, int W, int D>
+__global__ void __launch_bounds__(32 * W, 1)
+qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
+               const __grid_constant__ CUtensorMap tmap_b, const OwnParams p) {
+  using GM = GroupMath<BITS, GS, NB>;
+  constexpr int MP = GM::MP;
+  constexpr int GW = GM::GW;
+  extern __shared__ __align__(128) unsigned char own_smem[];
+  unsigned char* smem = own_smem;
+  const int csize = static_cast<int>(gridDim.x);  // CTAs per cluster (cluster spans x)
+  const int rank = static_cast<int>(blockIdx.x);
+  const int q = static_cast<int>(blockIdx.y);
+  const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, p.mbw, p.owned_max, csize, p.maxw, p.M);
+  const uint32_t sbase = smem_addr(smem);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  auto full_bar = [&](int s) { return sbase + 8u * static_cast<uint32_t>(warp * D + s); };
+  auto recv_bar = [&](int o) { return sbase + 8u * static_cast<uint32_t>(W * D + o); };
+  uint16_t* Xs = reinterpret_cast<uint16_t*>(smem + L.x_off);
+  float* xsum = reinterpret_cast<float*>(smem + L.xs_off);
+
+  const int t_begin = static_cast<int>((static_cast<int64_t>(p.tiles) * q) / p.ncl);
+  const int t_end = static_cast<int>((static_cast<int64_t>(p.tiles) * (q + 1)) / p.ncl);
+  const int nt = t_end - t_begin;
+  const int g0 = rank * p.gp;
+  const int U = nt * p.kp;
+  const int ua = own_unit_begin(warp, U, W);
+  const int nu = own_unit_begin(warp + 1, U, W) - ua;
+  const int owned = (nt > rank) ? (nt - rank + csize - 1) / csize : 0;
+  const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + 2 * 16 * p.mbw * 2);
+
+  QMM_TRACE_POINT(0);
+  if (lane == 0)
+    for (int s = 0; s < D; ++s) mbar_init(full_bar(s), 1);
+  if (tid == 0)
+    for (int o = 0; o < owned; ++o) mbar_init(recv_bar(o), 1);
+  fence_mbar_init();
+  __syncthreads();
+  // Expected bytes of every owned tile, before any peer can push (peers push
+  // only after the cluster barrier below).
+  if (tid == 0) {
+    for (int o = 0; o < owned; ++o) {
+      int sl;
+      const int n = own_contributors(o * csize + rank, p.kp, U, W, -1, &sl);
+      if (!(csize == 1 && n == 1))
+        mbar_arrive_expect_tx(recv_bar(o), static_cast<uint32_t>(csize * n * L.slot_bytes));
+    }
+  }
+  cluster_arrive();
+  griddep_launch_dependents();
+
+  // Copy unit qq of this warp's range into its stage qq mod D.
+  auto issue = [&](int qq) {
+    const int u = ua + qq;
+    const int i = u / p.kp;
+    const int part = u - i * p.kp;
+    const int n0 = (t_begin + i) * 16;
+    const int gs0 = g0 + part * p.gq;
+    const int s = qq % D;
+    const uint32_t dst = sbase + static_cast<uint32_t>(L.ring_off + (warp * D + s) * L.stage_bytes);
+    mbar_arrive_expect_tx(full_bar(s), unit_bytes);
+    for (int b = 0; b < p.nbox; ++b)
+      tma_load_2d(dst + static_cast<uint32_t>(b * 16 * p.bw * 4), &tmap, gs0 * GW + b * p.bw, n0, full_bar(s));
+    const int mx0 = (gs0 / 8) * 8;  // 16-byte aligned start of the scale/bias box
+    tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+    tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 16 * p.mbw * 2), &tmap_b, mx0, n0, full_bar(s));
+  };
+  if (lane == 0) {
+    if (warp == 0) {
+      prefetch_tmap(&tmap);
+      prefetch_tmap(&tmap_s);
+      prefetch_tmap(&tmap_b);
+    }
+    for (int qq = 0; qq < D - 1 && qq < nu; ++qq) issue(qq);
+  }
+  __syncwarp();
+
+  griddep_wait();  // X may be the previous call's output; Y may still be read by it
+  QMM_TRACE_POINT(1);
+  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, 32 * W);
+  __syncthreads();
+  cluster_wait();  // every CTA of the cluster has initialized its barriers
+  QMM_TRACE_POINT(2);
+
+  const typename GM::Lane ln = GM::lane_geometry(lane);
+  const uint16_t* xrow = GM::x_row(Xs, L.rsx, ln);
+  const int gpb = p.bw / GW;  // groups per weight box
+
+  // Y[m, n] for this lane's fragment of tile i.
+  auto write_y = [&](int i, const float (&v)[NB][4]) {
+    const int n_lo = (t_begin + i) * 16 + ln.g;
+    const int n_hi = n_lo + 8;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 8 * nb + 2 * ln.t + (e & 1);
+        const int n = (e < 2) ? n_lo : n_hi;
+        if (m < p.M && n < p.N) {
+          const int64_t off = static_cast<int64_t>(m) * p.N + n;
+          if (p.out_f32) static_cast<float*>(p.Y)[off] = v[nb][e];
+          else static_cast<__nv_bfloat16*>(p.Y)[off] = __float2bfloat16_rn(v[nb][e]);
+        }
+      }
+    }
+  };
+  // Hand this warp's partial of tile i to the tile's owner.
+  auto push = [&](int i, const float (&acc)[NB][4]) {
+    int slot;
+    const int n = own_contributors(i, p.kp, U, W, warp, &slot);
+    if (csize == 1 && n == 1) {
+      write_y(i, acc);
+      return;
+    }
+    const uint32_t owner = static_cast<uint32_t>(i % csize);
+    const int o = i / csize;
+    const uint32_t dst = sbase + static_cast<uint32_t>(L.recv_off + ((o * csize + rank) * p.maxw + slot) * L.slot_bytes +
+                                                        lane * 16 * NB);
+    const uint32_t rbar = mapa_shared(recv_bar(o), owner);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+      st_async_v4(mapa_shared(dst + 16u * nb, owner), make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]),
+                  rbar);
+  };
+
+  float acc[NB][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+  int cur = -1;
+  bool waits_ok = true;
+  for (int qq = 0; qq < nu; ++qq) {
+    const int u = ua + qq;
+    const int i = u / p.kp;
+    const int part = u - i * p.kp;
+    if (i != cur) {
+      if (cur >= 0) {
+        push(cur, acc);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
+      }
+      cur = i;
+    }
+    // Refill the stage of unit qq - 1 with unit qq + D - 1: every lane's reads
+    // of it were consumed by its MMAs before the __syncwarp that closed unit
+    // qq - 1, and this lane issues the copy after that point.
+    if (lane == 0 && qq + D - 1 < nu) issue(qq + D - 1);
+    const int s = qq % D;
+    QMM_TRACE_POINT(40);
+    waits_ok = mbar_wait(full_bar(s), static_cast<uint32_t>((qq / D) & 1), kStatusTimeoutFull) && waits_ok;
+    QMM_TRACE_POINT(20);
+    const unsigned char* stage = smem + L.ring_off + (warp * D + s) * L.stage_bytes;
+    // Weights: [box][16 rows][bw words]; a group never straddles two boxes.
+    const uint32_t* wst = reinterpret_cast<const uint32_t*>(stage) + ln.g * p.bw + ln.wofs;
+    // Scales then biases: [16 rows][mbw halves] each, from group (g0 + part*gq) rounded down to 8.
+    const int gs0 = g0 + part * p.gq;
+    const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + ln.g * p.mbw + (gs0 % 8);
+    const int jr = part * p.gq;  // the unit's first group within the K-piece
+    const uint16_t* xu = xrow + jr * GS;
+    const float* xsu = xsum + jr * MP;
+    // word pointer of the next group, advanced group by group across the boxes
+    int bj = 0, jj = 0;
+    auto next_words = [&]() {
+      const uint32_t* wp = wst + bj * 16 * p.bw + jj * GW;
+      if (++jj == gpb) {
+        jj = 0;
+        ++bj;
+      }
+      return wp;
+    };
+    auto group = [&](int j, float (&tmp)[NB][4]) {
+      uint32_t wl[GM::LW], wh[GM::LW];
+      GM::load_words(next_words(), p.bw, wl, wh);
+      GM::mma(wl, wh, xu + j * GS, L.rsx, ln.tsub, tmp);
+    };
+    auto fold = [&](int j, const float (&tmp)[NB][4]) { GM::fold(meta + j, p.mbw, xsu + j * MP, ln.t, tmp, acc); };
+    int j = 0;
+    for (; NB == 1 && j + 3 < p.gq; j += 4) {  // four independent MMA chains
+      float t0[NB][4], t1[NB][4], t2[NB][4], t3[NB][4];
+      group(j, t0);
+      group(j + 1, t1);
+      group(j + 2, t2);
+      group(j + 3, t3);
+      fold(j, t0);
+      fold(j + 1, t1);
+      fold(j + 2, t2);
+      fold(j + 3, t3);
+    }
+    for (; j + 1 < p.gq; j += 2) {
+      float t0[NB][4], t1[NB][4];
+      group(j, t0);
+      group(j + 1, t1);
+      fold(j, t0);
+      fold(j + 1, t1);
+    }
+    if (j < p.gq) {
+      float t0[NB][4];
+      group(j, t0);
+      fold(j, t0);
+    }
+    QMM_TRACE_POINT(41);
+    __syncwarp();
+  }
+  if (cur >= 0) push(cur, acc);
+  QMM_TRACE_POINT(3);
+  // A wait that gave up may leave copies in flight: wait (bounded) for every
+  // copy this warp issued before the CTA can exit.
+  if (!waits_ok && lane == 0) {
+    const int first = nu > D ? nu - D : 0;
+    for (int qq = first; qq < nu; ++qq)
+      mbar_wait(full_bar(qq % D), static_cast<uint32_t>((qq / D) & 1), kStatusTimeoutDrain);
+  }
+  __syncwarp();
+
+  // Owned tiles: wait for every contributor's bytes, add the slots in order.
+  for (int o = warp; o < owned; o += W) {
+    const int i = o * csize + rank;
+    int sl;
+    const int n = own_contributors(i, p.kp, U, W, -1, &sl);
+    if (csize == 1 && n == 1) continue;  // written by its only contributor
+    mbar_wait(recv_bar(o), 0, kStatusTimeoutFull);
+    const float* rv = reinterpret_cast<const float*>(smem + L.recv_off) +
+                      static_cast<int64_t>(o * csize * p.maxw) * (L.slot_bytes / 4) + lane * 4 * NB;
+    float v[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[nb][e] = 0.f;
+    for (int r2 = 0; r2 < csize; ++r2)
+      for (int k = 0; k < n; ++k) {
+        const float* src = rv + (r2 * p.maxw + k) * (L.slot_bytes / 4);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const float4 x4 = *reinterpret_cast<const float4*>(src + 4 * nb);
+          v[nb][0] += x4.x;
+          v[nb][1] += x4.y;
+          v[nb][2] += x4.z;
+          v[nb][3] += x4.w;
+        }
+      }
+    write_y(i, v);
+  }
+  QMM_TRACE_POINT(6);
+}
+
+}  // namespace qmm

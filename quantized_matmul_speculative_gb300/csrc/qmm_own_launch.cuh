@@ -1,0 +1,187 @@
+// Host-side planner and launcher of the warp-owned TMA family (qmm_own.cuh).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "qmm_geometry.h"
+#include "qmm_internal.h"
+#include "qmm_own.cuh"
+#include "qmm_tiles.h"
+#include "qmm_tma_launch.cuh"
+
+namespace qmm {
+
+// Plan one call: K-piece, parts per tile, box widths, clusters, receive
+// slots and shared memory.  Returns cudaErrorNotSupported (and launches
+// nothing) when (W, D, csize, CTAs per SM) cannot run the shape.
+template <int BITS, int GS, int NB, int W, int D>
+cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, OwnParams* p, int* smem, int* budget) {
+  constexpr int GW = GroupMath<BITS, GS, NB>::GW;
+  constexpr int MP = 8 * NB;
+  const int G = a.K / GS;
+  if (G % 8 != 0 || G % csize != 0) return cudaErrorNotSupported;  // scale/bias rows must be 16-byte strided
+  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
+  p->X = a.X;
+  p->Y = a.Y;
+  p->M = a.M;
+  p->N = a.N;
+  p->K = a.K;
+  p->out_f32 = a.out_f32;
+  p->gp = G / csize;
+  p->gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p->gp) - 1) / static_cast<unsigned long long>(p->gp);
+  p->tiles = (a.N + 15) / 16;
+
+  auto kern = qmm_own_kernel<BITS, GS, NB, W, D>;
+  int sm_bytes = 0, optin = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  *budget = tma_smem_budget(sm_bytes, optin, ctas_per_sm);
+  {
+    static std::mutex mu;
+    static int smem_set = 0;
+    static bool nonportable = false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (*budget > smem_set) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, *budget);
+      if (e != cudaSuccess) return e;
+      smem_set = *budget;
+    }
+    if (csize > 8 && !nonportable) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      nonportable = true;
+    }
+  }
+  int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), 32 * W, *budget, csize);
+  if (ncl < 1) return cudaErrorNotSupported;
+  if (ncl > p->tiles) ncl = p->tiles;
+  p->ncl = ncl;
+  const int nt_max = (p->tiles + ncl - 1) / ncl;
+  const int nt_min = p->tiles / ncl;
+
+  // Parts per tile: the fewest (largest units) that give every warp at least
+  // two units and fit; failing that, the most that fit.
+  bool found = false;
+  for (int kp = 1; kp <= p->gp; ++kp) {
+    if (p->gp % kp != 0) continue;
+    const int gq = p->gp / kp;
+    // weight boxes of whole groups, 16-byte multiples of <= 256 words, fewest fragment-load wavefronts
+    int bw = 0, best_wf = 1 << 30;
+    for (int d = 1; d <= gq; ++d) {
+      if (gq % d != 0) continue;
+      const int w = d * GW;
+      if (w > 256 || w % 4 != 0) continue;
+      const int wf = tma_box_wavefronts(w, GW);
+      if (wf < best_wf || (wf == best_wf && w > bw)) {
+        best_wf = wf;
+        bw = w;
+      }
+    }
+    if (bw == 0) continue;
+    const int mbw = (7 + gq + 7) / 8 * 8;  // any start within 8 groups of the box start
+    if (mbw > 256) continue;
+    int maxw = 1;
+    for (int nt : {nt_min, nt_max}) {
+      if (nt < 1) continue;
+      for (int i = 0; i < nt; ++i) {
+        int sl;
+        const int n = own_contributors(i, kp, nt * kp, W, -1, &sl);
+        maxw = n > maxw ? n : maxw;
+      }
+    }
+    const int owned_max = (nt_max + csize - 1) / csize;
+    const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, mbw, owned_max, csize, maxw, a.M);
+    if (L.total > *budget) continue;
+    p->kp = kp;
+    p->gq = gq;
+    p->bw = bw;
+    p->nbox = gq * GW / bw;
+    p->mbw = mbw;
+    p->maxw = maxw;
+    p->owned_max = owned_max;
+    *smem = L.total;
+    found = true;
+    if (nt_min * kp >= 2 * W) break;
+  }
+  return found ? cudaSuccess : cudaErrorNotSupported;
+}
+
+template <int BITS, int GS, int NB, int W, int D>
+cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaStream_t stream, bool plan_only) {
+  OwnParams p;
+  int smem = 0, budget = 0;
+  const cudaError_t pe = own_plan<BITS, GS, NB, W, D>(a, csize, ctas_per_sm, &p, &smem, &budget);
+  if (pe != cudaSuccess || plan_only) return pe;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorUnknown;
+  CUtensorMap tmap, tmap_s, tmap_b;
+  {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.bw), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wq), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int G = a.K / GS;
+  for (int arr = 0; arr < 2; ++arr) {
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    void* base = const_cast<uint16_t*>(arr ? a.B : a.S);
+    if (encode(arr ? &tmap_b : &tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const char* lg = std::getenv("QMM_LOG");
+    if (lg != nullptr && lg[0] != '\0' && lg[0] != '0')
+      std::fprintf(stderr,
+                   "qmm own: grid %dx%d (clusters of %d) threads %d smem %d budget %d depth %d gp %d parts %d "
+                   "gq %d box %dx%d maxw %d owned %d\n",
+                   csize, p.ncl, csize, 32 * W, smem, budget, D, p.gp, p.kp, p.gq, p.nbox, p.bw, p.maxw, p.owned_max);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize, p.ncl, 1);
+  cfg.blockDim = dim3(32 * W, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D>, tmap, tmap_s, tmap_b, p);
+}
+
+template <int BITS, int GS, int NB>
+cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
+#define QMM_TRY_OWN(w, dd)                 \
+  if (d.WN == (w) && d.R == (dd))          \
+    return launch_own_impl<BITS, GS, NB, w, dd>(a, csize, d.WK, stream, plan_only);
+  QMM_OWN_TILES(QMM_TRY_OWN)
+#undef QMM_TRY_OWN
+  return cudaErrorNotSupported;
+}
+
+template <int BITS, int GS>
+cudaError_t launch_own_bg(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
+  if (a.M <= 8) return launch_own_tile<BITS, GS, 1>(a, d, csize, stream, plan_only);
+  return launch_own_tile<BITS, GS, 2>(a, d, csize, stream, plan_only);
+}
+
+}  // namespace qmm

@@ -12,3 +12,9 @@
   X(8, 16)               \
   X(4, 16)               \
   X(16, 16)
+
+//   own:  X(W consumer warps, ring stages per warp)
+#define QMM_OWN_TILES(X) \
+  X(8, 3)                \
+  X(16, 2)               \
+  X(4, 4)

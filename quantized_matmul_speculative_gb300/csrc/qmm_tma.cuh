@@ -50,6 +50,7 @@
 
 #include "qmm_device.cuh"
 #include "qmm_geometry.h"
+#include "qmm_group.cuh"
 
 namespace qmm {
 
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(32 * (W + 1), (W <= 8) ? 2 : 1)
 qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
   using C = TmaCfg<BITS, GS, NB, W, SMAX>;
+  using GM = GroupMath<BITS, GS, NB>;
   static_assert((2 * SMAX + 1) * 8 <= 512, "mbarriers must fit below the stages");
   const int S = p.stages;
   extern __shared__ __align__(128) unsigned char tma_smem[];
@@ -195,122 +197,27 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   griddep_wait();  // X may be the previous call's output; Y may still be read by it
   QMM_TRACE_POINT(1);
   const int cthreads = C::CONSUMER_THREADS;
-  // Stage this CTA's K-piece of X in unpack order: within each word's chunk
-  // of 32/b codes, 32-bit element i holds (x[i], x[i + 16/b]).  A task is one
-  // such chunk of one row (16 or 32 bytes); the tasks of a unit (row m,
-  // group j) sit in adjacent lanes, which add up their sums by shuffles
-  // (xsum[j * MP + m] = sum of x[m, k] over group j).  Loads are issued a
-  // batch at a time before any is used.  Rows m >= M are not staged: an MMA
-  // output column depends only on its own activation row, and the columns of
-  // rows >= M are never stored.
-  {
-    constexpr int CH = GS / C::VPW;  // tasks per unit (2..16, divides 32)
-    constexpr int TQ = C::VPW / 8;   // 16-byte loads per task
-    constexpr int BATCH = 4;
-    static_assert(32 % CH == 0, "a unit's tasks must share a warp");
-    const int ntask = p.M * p.gp * CH;
-    for (int base = 0; base < ntask; base += BATCH * cthreads) {
-      uint4 v[BATCH][TQ];
-#pragma unroll
-      for (int b = 0; b < BATCH; ++b) {
-        const int u = base + b * cthreads + tid;
-        const int unit = u / CH;
-        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * p.gp_magic) >> 32);
-        const int j = unit - m * p.gp;
-        const uint16_t* src =
-            p.X + static_cast<int64_t>(m) * p.K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * C::VPW;
-#pragma unroll
-        for (int q8 = 0; q8 < TQ; ++q8) v[b][q8] = (u < ntask) ? ld_nc_v4(src + 8 * q8) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int b = 0; b < BATCH; ++b) {
-        const int u = base + b * cthreads + tid;
-        const int unit = u / CH;
-        const int c = u - unit * CH;
-        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * p.gp_magic) >> 32);
-        const int j = unit - m * p.gp;
-        const uint32_t* e = reinterpret_cast<const uint32_t*>(v[b]);
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < C::VPW / 2; ++i) sum = add_bf16x2_f32(e[i], sum);
-        if (u < ntask) {
-          uint32_t out[C::HALF];
-#pragma unroll
-          for (int i = 0; i < C::HALF; ++i) {
-            const uint32_t a = e[i / 2];
-            const uint32_t bb = e[(i + C::HALF) / 2];
-            out[i] = (i % 2 == 0) ? prmt_lo(a, bb) : prmt_hi(a, bb);
-          }
-          uint2* d2 = reinterpret_cast<uint2*>(Xs + m * L.rsx + j * GS + c * C::VPW);
-#pragma unroll
-          for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
-        }
-#pragma unroll
-        for (int o = CH / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (u < ntask && c == 0) xsum[j * C::MP + m] = sum;
-      }
-    }
-  }
+  // This CTA's K-piece of X in unpack order, with its per-group sums.
+  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, cthreads);
   asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");  // consumers only
   QMM_TRACE_POINT(2);
 
-  const int g = lane >> 2;
-  const int t = lane & 3;
-  const int wofs = (C::TPW == 1) ? t * C::LW : t / C::TPW;
-  // This thread's activation row g at the first code of its first word; for
-  // words shared by TPW threads, the first MMA step this thread feeds.
-  const int tsub = (C::TPW == 1) ? 0 : (t % C::TPW) * (C::SPW / C::TPW);
-  const uint16_t* xrow = Xs + g * L.rsx + wofs * C::VPW + ((C::TPW == 1) ? 0 : 4 * tsub);
+  const typename GM::Lane ln = GM::lane_geometry(lane);
+  const int g = ln.g;
+  const int t = ln.t;
+  const int wofs = ln.wofs;
+  const uint16_t* xrow = GM::x_row(Xs, L.rsx, ln);
   const int gpb = p.box_words / C::GW;  // groups per TMA box
 
-  // Packed words of this thread's rows g and g + 8 for the group at wp.
-  auto load_words = [&](const uint32_t* wp, uint32_t (&wl)[C::LW], uint32_t (&wh)[C::LW]) {
-    ld_shared_words<C::LW>(wl, wp);
-    ld_shared_words<C::LW>(wh, wp + 8 * p.box_words);
-  };
-  // MMAs of group j (its packed words in wl, wh) into tmp (fresh per group).
-  auto group_mma_w = [&](const uint32_t (&wl)[C::LW], const uint32_t (&wh)[C::LW], int j, float (&tmp)[NB][4]) {
-    const uint16_t* xg = xrow + j * GS;
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tmp[nb][e] = 0.f;
-#pragma unroll
-    for (int st = 0; st < C::STEPS; ++st) {
-      const int lwi = (C::TPW == 1) ? st / C::SPW : 0;
-      const int sub = (C::TPW == 1) ? st % C::SPW : tsub + st;
-      uint32_t a[4];
-      a[0] = unpack_pair<BITS>(wl[lwi], 2 * sub);
-      a[1] = unpack_pair<BITS>(wh[lwi], 2 * sub);
-      a[2] = unpack_pair<BITS>(wl[lwi], 2 * sub + 1);
-      a[3] = unpack_pair<BITS>(wh[lwi], 2 * sub + 1);
-      const int ko = (C::TPW == 1) ? (lwi * C::VPW + 4 * sub) : 4 * st;
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const uint2 xb = *reinterpret_cast<const uint2*>(xg + nb * 8 * L.rsx + ko);
-        mma_bf16_16816(tmp[nb], a, xb.x, xb.y);
-      }
-    }
-  };
+  // MMAs of group j (packed words of this thread's rows at wp) into tmp (fresh per group).
   auto group_mma = [&](const uint32_t* wp, int j, float (&tmp)[NB][4]) {
     uint32_t wl[C::LW], wh[C::LW];
-    load_words(wp, wl, wh);
-    group_mma_w(wl, wh, j, tmp);
+    GM::load_words(wp, p.box_words, wl, wh);
+    GM::mma(wl, wh, xrow + j * GS, L.rsx, ln.tsub, tmp);
   };
-  // Fold group j's scale and bias (b' = b - 128 s) into acc.
+  // Fold group j's scale and bias into acc.
   auto group_fold = [&](const uint16_t* meta, int j, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
-    const float s_lo = __half2float(__ushort_as_half(meta[j]));
-    const float s_hi = __half2float(__ushort_as_half(meta[8 * p.mbw + j]));
-    const float b_lo = fmaf(-128.f, s_lo, __half2float(__ushort_as_half(meta[16 * p.mbw + j])));
-    const float b_hi = fmaf(-128.f, s_hi, __half2float(__ushort_as_half(meta[24 * p.mbw + j])));
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const float2 xs = *reinterpret_cast<const float2*>(xsum + j * C::MP + 8 * nb + 2 * t);
-      ffma2(acc[nb][0], acc[nb][1], b_lo, b_lo, xs.x, xs.y);
-      ffma2(acc[nb][0], acc[nb][1], s_lo, s_lo, tmp[nb][0], tmp[nb][1]);
-      ffma2(acc[nb][2], acc[nb][3], b_hi, b_hi, xs.x, xs.y);
-      ffma2(acc[nb][2], acc[nb][3], s_hi, s_hi, tmp[nb][2], tmp[nb][3]);
-    }
+    GM::fold(meta + j, p.mbw, xsum + j * C::MP, t, tmp, acc);
   };
 
   int s = 0, ph = 0;  // stage and phase parity of tile i
@@ -344,7 +251,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         // ahead of its stage.
         QMM_TRACE_POINT(40);
         mbar_wait(full_bar(s), ph, kStatusTimeoutFull);
-        QMM_TRACE_POINT(20 + i);
+        QMM_TRACE_POINT(20);
         if (ja < jb) {
           const unsigned char* stage = smem + L.stage_off + s * L.stage_bytes;
           // Stage layout of the packed words: [box][16 rows][box_words]; a group
@@ -419,7 +326,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
           __syncwarp();
           if (lane == 0) mbar_arrive(empty_bar(s));
         }
-        QMM_TRACE_POINT(8 + i);
+        QMM_TRACE_POINT(8);
         if (++s == S) {
           s = 0;
           ph ^= 1;
