@@ -71,6 +71,8 @@ const VariantDesc kVariants[] = {
     {"tma_own_w16_d2_1cta", kFamilyOwn, 2, 16, 1},
     {"tma_own_w8_d3_2cta", kFamilyOwn, 3, 8, 2},
     {"tma_own_w4_d4_2cta", kFamilyOwn, 4, 4, 2},
+    {"tma_own_w8_d3_half", kFamilyOwn, 3, 8, 2, 1},
+    {"tma_own_w4_d4_half", kFamilyOwn, 4, 4, 2, 1},
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces

@@ -24,7 +24,9 @@ struct VariantDesc {
   int family;
   int R;   // mma: m16 row tiles per warp; tma: ring stages; own: ring stages per warp
   int WN;  // mma: warps along N; tma, own: consumer warps
-  int WK;  // mma: warps along K (intra-CTA split-K); tma: CTAs per SM targeted
+  int WK;  // mma: warps along K (intra-CTA split-K); tma, own: CTAs per SM the shared memory is sized for
+  int wave;  // own: at most this many CTAs per SM launched (0: as many as fit); with wave < WK
+             // the next call's CTAs fit beside this call's and stream their weights early
 };
 
 const VariantDesc* variant_desc(int v);

@@ -19,7 +19,7 @@ namespace qmm {
 // slots and shared memory.  Returns cudaErrorNotSupported (and launches
 // nothing) when (W, D, csize, CTAs per SM) cannot run the shape.
 template <int BITS, int GS, int NB, int W, int D>
-cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, OwnParams* p, int* smem, int* budget) {
+cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, OwnParams* p, int* smem, int* budget) {
   constexpr int GW = GroupMath<BITS, GS, NB>::GW;
   constexpr int MP = 8 * NB;
   const int G = a.K / GS;
@@ -59,6 +59,11 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, OwnParams* p
   }
   int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), 32 * W, *budget, csize);
   if (ncl < 1) return cudaErrorNotSupported;
+  if (wave > 0 && wave < ctas_per_sm) {
+    // at most `wave` CTAs per SM: the rest of the SM is left to the next call's CTAs
+    const int cap = wave * device_sm_count() / csize;
+    if (cap >= 1 && ncl > cap) ncl = cap;
+  }
   if (ncl > p->tiles) ncl = p->tiles;
   p->ncl = ncl;
   const int nt_max = (p->tiles + ncl - 1) / ncl;
@@ -70,17 +75,14 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, OwnParams* p
   for (int kp = 1; kp <= p->gp; ++kp) {
     if (p->gp % kp != 0) continue;
     const int gq = p->gp / kp;
-    // weight boxes of whole groups, 16-byte multiples of <= 256 words, fewest fragment-load wavefronts
-    int bw = 0, best_wf = 1 << 30;
+    // weight boxes of whole groups, 16-byte multiples of <= 256 words: the
+    // widest (fewest copies per unit; measured to matter more than the
+    // shared-memory bank conflicts of the fragment loads)
+    int bw = 0;
     for (int d = 1; d <= gq; ++d) {
       if (gq % d != 0) continue;
       const int w = d * GW;
-      if (w > 256 || w % 4 != 0) continue;
-      const int wf = tma_box_wavefronts(w, GW);
-      if (wf < best_wf || (wf == best_wf && w > bw)) {
-        best_wf = wf;
-        bw = w;
-      }
+      if (w <= 256 && w % 4 == 0) bw = w;
     }
     if (bw == 0) continue;
     const int mbw = (7 + gq + 7) / 8 * 8;  // any start within 8 groups of the box start
@@ -112,10 +114,11 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, OwnParams* p
 }
 
 template <int BITS, int GS, int NB, int W, int D>
-cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaStream_t stream, bool plan_only) {
+cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int wave, cudaStream_t stream,
+                            bool plan_only) {
   OwnParams p;
   int smem = 0, budget = 0;
-  const cudaError_t pe = own_plan<BITS, GS, NB, W, D>(a, csize, ctas_per_sm, &p, &smem, &budget);
+  const cudaError_t pe = own_plan<BITS, GS, NB, W, D>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
   if (pe != cudaSuccess || plan_only) return pe;
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -172,7 +175,7 @@ template <int BITS, int GS, int NB>
 cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
 #define QMM_TRY_OWN(w, dd)                 \
   if (d.WN == (w) && d.R == (dd))          \
-    return launch_own_impl<BITS, GS, NB, w, dd>(a, csize, d.WK, stream, plan_only);
+    return launch_own_impl<BITS, GS, NB, w, dd>(a, csize, d.WK, d.wave, stream, plan_only);
   QMM_OWN_TILES(QMM_TRY_OWN)
 #undef QMM_TRY_OWN
   return cudaErrorNotSupported;
