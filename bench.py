@@ -179,6 +179,164 @@ def cpu_oracle_sample(p: synth.Problem, rows: int, ms):
     return nbytes, dt
 
 
+# ------------------------------------------------------------------ further reports
+def graph_us_per_call(torch, stream, capture, n_calls, warm=3, reps=5):
+    """Median us per call of a CUDA graph of n_calls calls (capture(i) issues
+    call i), timed with events on `stream` over `reps` replays."""
+    with torch.cuda.stream(stream):
+        capture(0)  # eager: sets kernel attributes outside the capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            capture(i)
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3 / n_calls)
+    del g
+    return float(np.median(times))
+
+
+def configs_report(torch, dev, stream, peak):
+    """us per call and weight+metadata GB/s of every workload shape at the
+    dispatcher's choice.  Calls rotate over weight copies whose total exceeds
+    4x L2; every call waits for the previous one on the stream (the kernels
+    wait for their predecessor before reading X)."""
+    from quantized_matmul_speculative_gb300 import binding
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = stream.cuda_stream
+    names = binding.variant_names()
+    out = []
+    plan = [(workloads.SINGLE_LAYER, None, None, (4,)),
+            (workloads.DENSE_27B_LAYER, None, None, workloads.DENSE_27B_LAYER.ms)]
+    plan += [(workloads.GROUP_BIT_SWEEP, b, g, (1, 4, 8, 16)) for b, g in workloads.GROUP_BIT_SWEEP.variants]
+    plan.append((workloads.VERIFY_STEP, None, None, (1, 4, 8)))
+    for w, bits, gs, ms in plan:
+        bits = bits or w.bits
+        gs = gs or w.group_size
+        for si, sh in enumerate(w.shapes):
+            p = synth.make_problem(workloads.shape_seed(w, si, 0, bits, gs), sh.N, sh.K, bits, gs)
+            cb = workloads.call_bytes(sh.N, sh.K, bits, gs)
+            ncopy = max(2, int(np.ceil(4 * l2 / cb)) + 1)
+            wq = torch.from_numpy(binding.pack(p.q, bits).view(np.int32))
+            sc = torch.from_numpy(p.scales.view(np.float16))
+            bi = torch.from_numpy(p.biases.view(np.float16))
+            copies = [(wq.to(dev), sc.to(dev), bi.to(dev)) for _ in range(ncopy)]
+            x = torch.from_numpy(p.x.view(np.int16)).to(dev).view(torch.bfloat16)
+            y = torch.empty((16, sh.N), dtype=torch.bfloat16, device=dev)
+            for M in ms:
+                def capture(i, M=M):
+                    wq_d, s_d, b_d = copies[i % ncopy]
+                    binding.small_m_ptr(x.data_ptr(), wq_d.data_ptr(), s_d.data_ptr(), b_d.data_ptr(), M, sh.N,
+                                        sh.K, bits, gs, y.data_ptr(), binding.OUT_BF16, -1, -1, handle)
+                us = graph_us_per_call(torch, stream, capture, 64)
+                v, sp = binding.select_variant(M, sh.N, sh.K, bits, gs)
+                gbs = cb / (us * 1e-6) / 1e9
+                out.append({"workload": w.name, "shape": f"{sh.name} {sh.N}x{sh.K}", "bits": bits, "group_size": gs,
+                            "M": M, "us_per_call": round(us, 3), "weight_gbs": round(gbs, 1),
+                            "frac_hbm": round(gbs / peak, 4), "variant": names[v], "splits": sp})
+            del copies
+            torch.cuda.empty_cache()
+    return out
+
+
+def verify_step_report(torch, dev, stream, peak, ms=tuple(range(1, 9)), steps=10):
+    """The whole verify step: 36 layers x (QKV, O, gate+up, down), 4-bit g64,
+    distinct weights per layer (3.9 GB), back to back on one stream.  Each
+    projection reads the first M*K elements of the previous projection's
+    output buffer as its activations (a real data dependency of the right
+    size; the layer math between projections is not part of this op), and the
+    next layer's QKV reads the down projection's output."""
+    from quantized_matmul_speculative_gb300 import binding
+
+    w = workloads.VERIFY_STEP
+    handle = stream.cuda_stream
+    bits, gs = w.bits, w.group_size
+    mats = []
+    for si, sh in enumerate(w.shapes):
+        p = synth.make_problem(workloads.shape_seed(w, si), sh.N, sh.K, bits, gs)
+        wq = torch.from_numpy(binding.pack(p.q, bits).view(np.int32)).to(dev)
+        sc = torch.from_numpy(p.scales.view(np.float16)).to(dev)
+        bi = torch.from_numpy(p.biases.view(np.float16)).to(dev)
+        mats.append((sh, wq, sc, bi))
+        if si == 0:
+            x0 = torch.from_numpy(p.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    # distinct memory per layer (same values): every call streams its own weights from HBM
+    layers = [[(sh, wq.clone(), sc.clone(), bi.clone()) for sh, wq, sc, bi in mats] for _ in range(w.layers)]
+    del mats
+    outs = [torch.empty((16 * sh.N,), dtype=torch.bfloat16, device=dev) for sh in w.shapes]
+    act = torch.empty((16 * w.shapes[0].K,), dtype=torch.bfloat16, device=dev)
+    act.copy_(x0.reshape(-1)[: act.numel()])
+    step_bytes = w.layers * sum(workloads.call_bytes(sh.N, sh.K, bits, gs) for sh in w.shapes)
+    res = []
+    for M in ms:
+        def one_step(M=M):
+            src = act
+            for lay in layers:
+                for j, (sh, wq, sc, bi) in enumerate(lay):
+                    binding.small_m_ptr(src.data_ptr(), wq.data_ptr(), sc.data_ptr(), bi.data_ptr(), M, sh.N, sh.K,
+                                        bits, gs, outs[j].data_ptr(), binding.OUT_BF16, -1, -1, handle)
+                    src = outs[j]
+            # the next step's first layer reads the last down projection's output
+        with torch.cuda.stream(stream):
+            one_step()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            one_step()
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                g.replay()
+            b.record(stream)
+            b.synchronize()
+        ms_step = a.elapsed_time(b) / steps
+        gbs = step_bytes / (ms_step * 1e-3) / 1e9
+        res.append({"M": M, "steps_per_s": round(1e3 / ms_step, 1), "ms_per_step": round(ms_step, 4),
+                    "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)})
+        del g
+    del layers
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "layers": w.layers, "calls_per_step": 4 * w.layers, "bytes_per_step": step_bytes,
+            "per_m": res, "chain": "each projection reads the first M*K elements of the previous output"}
+
+
+def dense_control(torch, dev, stream, ms=(1, 8, 16)):
+    """bf16 dense torch.matmul (cuBLAS) on the 5120x5120 layer, for scale only:
+    the dense bf16 weights are 4x the bytes of the 4-bit ones."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    N = K = 5120
+    ncopy = max(2, int(np.ceil(4 * l2 / (2 * N * K))) + 1)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    wd = torch.randn((N, K), generator=g).to(torch.bfloat16)
+    copies = [wd.to(dev) for _ in range(ncopy)]
+    x = torch.randn((16, K), generator=g).to(torch.bfloat16).to(dev)
+    y = torch.empty((16, N), dtype=torch.bfloat16, device=dev)
+    res = []
+    for M in ms:
+        def capture(i, M=M):
+            torch.matmul(x[:M], copies[i % ncopy].t(), out=y[:M])
+        us = graph_us_per_call(torch, stream, capture, 32)
+        res.append({"M": M, "us_per_call": round(us, 3), "weight_gbs": round(2 * N * K / (us * 1e-6) / 1e9, 1)})
+    del copies
+    torch.cuda.empty_cache()
+    return {"op": "torch.matmul bf16 dense, 5120x5120", "per_m": res,
+            "note": "library call (cuBLAS), for scale only; 2 bytes per weight"}
+
+
 def run_reference(args, world, rank):
     """The oracle arm: host cores, a bounded sample of the same workload per step.
 
@@ -350,6 +508,14 @@ def run_ours(args, world, rank, local):
                "sample": f"M=1..16 over the first {args.cpu_rows} of {N} rows, fp64 oracle, 1 thread, "
                          f"{dt:.1f} s"}
 
+    extra = {}
+    if not args.no_extra:
+        extra["configs"] = configs_report(torch, dev, stream, peak)
+        extra["verify_step"] = verify_step_report(torch, dev, stream, peak)
+        extra["controls"] = dense_control(torch, dev, stream)
+    kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
+                      "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
+
     clk = clocks.summary()
     if rank == 0:
         line = {
@@ -365,7 +531,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(value / world / peak, 4), "traffic": profiled_traffic(w.name),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                         else "fallback 6.8 TB/s", "kernel": "qmm_tma_kernel",
+                         else "fallback 6.8 TB/s", "kernel": ", ".join(kernels),
                          "achieved_def": "weight+metadata bytes per launch / mean launch time over the timed region"},
             "per_m": per_m,
             "cpu_baseline": cpu,
@@ -375,6 +541,7 @@ def run_ours(args, world, rank, local):
                             "every call"},
             "gpu_launches": steps_timed * calls_per_step,
             "clocks": clk,
+            **extra,
         }
         print(json.dumps(line), flush=True)
     return 0
@@ -390,6 +557,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=5120)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-config, verify-step and dense-control reports")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -2,6 +2,12 @@
 // dispatcher.
 #pragma once
 
+#ifdef __CUDACC__
+#define QMM_HD __host__ __device__
+#else
+#define QMM_HD
+#endif
+
 namespace qmm {
 
 // Shared-memory wavefronts of one warp's load of its weight fragment words
@@ -76,6 +82,36 @@ inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, i
   *nbox = best;
   *box_words = *pw / best;
   return true;
+}
+
+// First unit of warp w when U units are split into W contiguous ranges.
+QMM_HD inline int own_unit_begin(int w, int U, int W) {
+  return static_cast<int>((static_cast<long long>(w) * U) / W);
+}
+
+// Warps whose (non-empty) unit range meets tile i (units [i*kp, (i+1)*kp)),
+// and the position of warp w among them in *slot (-1 if w is not one).
+QMM_HD inline int own_contributors(int i, int kp, int U, int W, int w, int* slot) {
+  const int lo = i * kp, hi = (i + 1) * kp;
+  if (U >= W) {
+    // Every range is non-empty: the warp holding unit u is ((u + 1) W - 1) / U
+    // (the largest w with floor(w U / W) <= u), and the contributors are the
+    // warps from the one holding lo to the one holding hi - 1.
+    const int wl = static_cast<int>((static_cast<long long>(lo + 1) * W - 1) / U);
+    const int wh = static_cast<int>((static_cast<long long>(hi) * W - 1) / U);
+    *slot = (w >= wl && w <= wh) ? w - wl : -1;
+    return wh - wl + 1;
+  }
+  int n = 0;
+  *slot = -1;
+  for (int v = 0; v < W; ++v) {
+    const int a = own_unit_begin(v, U, W), b = own_unit_begin(v + 1, U, W);
+    if (a < b && a < hi && b > lo) {
+      if (v == w) *slot = n;
+      ++n;
+    }
+  }
+  return n;
 }
 
 // Shared-memory layout of one CTA of the TMA family (bytes); the kernel and

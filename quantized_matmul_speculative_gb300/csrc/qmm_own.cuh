@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "qmm_device.cuh"
+#include "qmm_geometry.h"
 #include "qmm_group.cuh"
 
 namespace qmm {
@@ -50,27 +51,6 @@ struct OwnParams {
   int owned_max;                // most tiles one CTA owns
   int out_f32;
 };
-
-// First unit of warp w when U units are split into W contiguous ranges.
-__host__ __device__ inline int own_unit_begin(int w, int U, int W) {
-  return static_cast<int>((static_cast<long long>(w) * U) / W);
-}
-
-// Warps whose (non-empty) unit range meets tile i (units [i*kp, (i+1)*kp)),
-// and the position of warp w among them in *slot (-1 if w is not one).
-__host__ __device__ inline int own_contributors(int i, int kp, int U, int W, int w, int* slot) {
-  int n = 0;
-  *slot = -1;
-  const int lo = i * kp, hi = (i + 1) * kp;
-  for (int v = 0; v < W; ++v) {
-    const int a = own_unit_begin(v, U, W), b = own_unit_begin(v + 1, U, W);
-    if (a < b && a < hi && b > lo) {
-      if (v == w) *slot = n;
-      ++n;
-    }
-  }
-  return n;
-}
 
 // Shared-memory layout of one CTA (bytes).  Only the M staged activation
 // rows are reserved: the MMA fragments of rows M..mp-1 read whatever lies
@@ -147,11 +127,16 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   cluster_arrive();
   griddep_launch_dependents();
 
-  // Copy unit qq of this warp's range into its stage qq mod D.
+  // Copy the unit at the issue cursor (tile ii, part ip: unit qq of this
+  // warp's range) into stage qq mod D, then advance the cursor.
+  int ii = ua / p.kp, ip = ua - (ua / p.kp) * p.kp;
   auto issue = [&](int qq) {
-    const int u = ua + qq;
-    const int i = u / p.kp;
-    const int part = u - i * p.kp;
+    const int i = ii;
+    const int part = ip;
+    if (++ip == p.kp) {
+      ip = 0;
+      ++ii;
+    }
     const int n0 = (t_begin + i) * 16;
     const int gs0 = g0 + part * p.gq;
     const int s = qq % D;
@@ -228,10 +213,14 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     for (int e = 0; e < 4; ++e) acc[nb][e] = 0.f;
   int cur = -1;
   bool waits_ok = true;
+  int ci = ua / p.kp, cp = ua - (ua / p.kp) * p.kp;  // compute cursor: tile and part of unit qq
   for (int qq = 0; qq < nu; ++qq) {
-    const int u = ua + qq;
-    const int i = u / p.kp;
-    const int part = u - i * p.kp;
+    const int i = ci;
+    const int part = cp;
+    if (++cp == p.kp) {
+      cp = 0;
+      ++ci;
+    }
     if (i != cur) {
       if (cur >= 0) {
         push(cur, acc);

@@ -40,11 +40,19 @@ def shapes(quick: bool):
     return [(N, K, b, g, tuple(sorted(ms))) for (N, K, b, g), ms in merged.items()]
 
 
-def candidates(nvar: int):
+def candidates(nvar: int, groups: int):
+    """(variant, splits): the TMA families try every cluster size up to 16
+    that divides the group count (non-powers of two balance tiles over
+    clusters better on some shapes); the mma family 1, 2, 4, 8."""
     names = binding.variant_names()
     for v in range(nvar):
-        for s in ((1, 2, 4, 8) if names[v].startswith("tma") else (1, 2, 4, 8)):
-            yield v, s
+        if names[v].startswith("tma"):
+            for s in range(1, 17):
+                if groups % s == 0 and (s <= 8 or s == 16 or s in (10, 12)):
+                    yield v, s
+        else:
+            for s in (1, 2, 4, 8):
+                yield v, s
 
 
 def time_config(torch, copies, x, y, M, N, K, bits, gs, v, s, stream, calls=48, reps=5):
@@ -105,7 +113,7 @@ def main():
         x = torch.from_numpy(p.x.view(np.int16)).to(dev).view(torch.bfloat16)
         y = torch.empty((16, N), dtype=torch.bfloat16, device=dev)
         for M in ms:
-            for v, s in candidates(len(names)):
+            for v, s in candidates(len(names), K // gs):
                 t0 = time.time()
                 try:
                     med, lo, hi = time_config(torch, copies, x, y, M, N, K, bits, gs, v, s, stream)

@@ -70,6 +70,28 @@ int main() {
            L.recv_off, L.total, L.rsx);
   }
   printf("{\"kind\":\"budget\",\"one\":%d,\"two\":%d}\n", tma_smem_budget(233472, 232448, 1), tma_smem_budget(233472, 232448, 2));
+  // warp-owned split: contributors of every tile against the definition
+  // (warps with a non-empty range [begin(w), begin(w+1)) meeting the tile's units)
+  int bad_contrib = 0, checked = 0;
+  for (int W : {4, 8, 12, 16}) for (int kp = 1; kp <= 9; ++kp) for (int nt = 1; nt <= 40; ++nt) {
+    const int U = nt * kp;
+    for (int i = 0; i < nt; ++i) {
+      int n_def = 0;
+      int slot_def[16];
+      for (int v = 0; v < W; ++v) {
+        const int a = own_unit_begin(v, U, W), b2 = own_unit_begin(v + 1, U, W);
+        slot_def[v] = -1;
+        if (a < b2 && a < (i + 1) * kp && b2 > i * kp) slot_def[v] = n_def++;
+      }
+      for (int v = -1; v < W; ++v) {
+        int sl;
+        const int n = own_contributors(i, kp, U, W, v, &sl);
+        ++checked;
+        if (n != n_def || (v >= 0 && sl != slot_def[v]) || (v < 0 && sl != -1)) ++bad_contrib;
+      }
+    }
+  }
+  printf("{\"kind\":\"contrib\",\"checked\":%d,\"bad\":%d}\n", checked, bad_contrib);
   return 0;
 }
 """
@@ -138,6 +160,13 @@ def test_layout_regions_ordered_and_aligned(records):
         # rows of X are 16-byte aligned modulo 8 bytes: the uint2 stores and
         # 8-byte fragment loads stay aligned, and rows fall on different banks
         assert (r["rsx"] * 2) % 16 == 8
+
+
+def test_warp_owned_contributors(records):
+    """The closed form of the warp-owned split's contributor set (used when
+    every warp has work) equals its definition, and so does the fallback."""
+    r = [r for r in records if r["kind"] == "contrib"][0]
+    assert r["checked"] > 10000 and r["bad"] == 0, r
 
 
 def test_budget(records):
