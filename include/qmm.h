@@ -97,6 +97,19 @@ qmm_status qmm_pack(const uint8_t* q, int64_t N, int64_t K, int bits, uint32_t* 
 /* Inverse of qmm_pack (host pointers).                                          */
 qmm_status qmm_unpack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint8_t* q);
 
+/* Conversion between the canonical layout above and the layout the kernels
+ * read ("native").  The kernels read the canonical layout directly (the
+ * k-permutation their tensor-core fragments need is applied to the
+ * activations while they are staged), so the native layout IS the canonical
+ * one: both calls are a stream-ordered device-to-device copy of
+ * N*K*bits/8 bytes on `stream`, and nothing when the two pointers are equal.
+ * Device pointers, caller-owned; the buffers must not partly overlap.
+ * QMM_ERR_UNSUPPORTED for bits not in {2,4,8}, QMM_ERR_SHAPE for a K that
+ * does not fill whole words, QMM_ERR_NULL for a null pointer with a non-empty
+ * matrix, QMM_ERR_CUDA if the copy cannot be queued.                            */
+qmm_status qmm_repack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint32_t* Wq_native, void* stream);
+qmm_status qmm_unrepack(const uint32_t* Wq_native, int64_t N, int64_t K, int bits, uint32_t* Wq, void* stream);
+
 /* Introspection of the dispatcher: the variant and split count qmm_small_m
  * would use, or -1 (and *splits untouched) if the shape is unsupported.         */
 int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* splits);

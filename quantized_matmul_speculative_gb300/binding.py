@@ -34,6 +34,8 @@ SIGNATURES = {
     "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
     "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
     "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
+    "qmm_repack": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp]),
+    "qmm_unrepack": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp]),
     "qmm_select_variant": (_i32, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_i32)]),
     "qmm_num_variants": (_i32, []),
     "qmm_variant_name": (ctypes.c_char_p, [_i32]),
@@ -96,6 +98,25 @@ def unpack(wq: np.ndarray, K: int, bits: int) -> np.ndarray:
     N = wq.shape[0]
     out = np.empty((N, K), dtype=np.uint8)
     _check(lib().qmm_unpack(wq.ctypes.data, N, K, bits, out.ctypes.data), "qmm_unpack")
+    return out
+
+
+def repack(wq, bits: int, out=None, inverse: bool = False, stream=None):
+    """Canonical -> native packed layout on the device (inverse: native ->
+    canonical).  ``wq``: CUDA int32/uint32 [N, K*bits/32]."""
+    import torch
+
+    if not wq.is_cuda or not wq.is_contiguous():
+        raise ValueError("wq must be a contiguous CUDA tensor")
+    N, words = wq.shape
+    K = words * 32 // bits
+    if out is None:
+        out = torch.empty_like(wq)
+    if stream is None:
+        stream = torch.cuda.current_stream(wq.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    fn = lib().qmm_unrepack if inverse else lib().qmm_repack
+    _check(fn(wq.data_ptr(), N, K, bits, out.data_ptr(), handle), "qmm_unrepack" if inverse else "qmm_repack")
     return out
 
 

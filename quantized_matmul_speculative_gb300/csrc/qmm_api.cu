@@ -463,4 +463,27 @@ qmm_status qmm_unpack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint8_
   return QMM_OK;
 }
 
+// The kernels read the canonical layout itself (the k-permutation the MMA
+// fragments need is applied to the activations in shared memory), so the
+// native layout is the canonical one and converting is a copy.
+static qmm_status layout_copy(const uint32_t* src, int64_t N, int64_t K, int bits, uint32_t* dst, void* stream) {
+  if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
+  if (N < 0 || K < 0 || (K * bits) % 32 != 0) return QMM_ERR_SHAPE;
+  const size_t bytes = static_cast<size_t>(N) * static_cast<size_t>(K) * static_cast<size_t>(bits) / 8;
+  if (bytes == 0) return QMM_OK;
+  if (src == nullptr || dst == nullptr) return QMM_ERR_NULL;
+  if (src == dst) return QMM_OK;
+  const cudaError_t e =
+      cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
+
+qmm_status qmm_repack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint32_t* Wq_native, void* stream) {
+  return layout_copy(Wq, N, K, bits, Wq_native, stream);
+}
+
+qmm_status qmm_unrepack(const uint32_t* Wq_native, int64_t N, int64_t K, int bits, uint32_t* Wq, void* stream) {
+  return layout_copy(Wq_native, N, K, bits, Wq, stream);
+}
+
 }  // extern "C"

@@ -87,3 +87,17 @@ def test_variant_registry(lib):
     assert 0 <= v < len(names) and 1 <= s <= 16
     assert binding.select_variant(17, 5120, 5120, 4, 64) == (None, None)
     assert lib.qmm_status_string(4) == b"misaligned pointer"
+
+
+def test_repack_validates_on_the_host(lib):
+    """qmm_repack / qmm_unrepack reject bad arguments before any CUDA call (the
+    pointers below are never dereferenced)."""
+    fake = 0x1000  # not a valid device pointer: must not be touched on the error paths
+    for fn in (lib.qmm_repack, lib.qmm_unrepack):
+        assert fn(fake, 4, 64, 3, fake + 256, None) == 3      # bits not in {2,4,8}
+        assert fn(fake, 4, 4, 4, fake + 256, None) == 2       # K*bits not a multiple of 32
+        assert fn(fake, -1, 64, 4, fake + 256, None) == 2     # negative N
+        assert fn(None, 4, 64, 4, fake, None) == 1            # null source, non-empty matrix
+        assert fn(fake, 4, 64, 4, None, None) == 1            # null destination
+        assert fn(None, 0, 64, 4, None, None) == 0            # empty: nothing to do
+        assert fn(fake, 4, 64, 4, fake, None) == 0            # in place: the layouts coincide

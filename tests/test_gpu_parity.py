@@ -242,3 +242,22 @@ def test_error_paths_launch_nothing(torch_cuda, monkeypatch):
     # the context is still healthy
     binding.small_m_ptr(*args, out_dtype=binding.OUT_F32)
     torch.cuda.synchronize()
+
+
+@pytest.mark.gpu
+def test_repack_round_trip_and_use(torch_cuda):
+    """qmm_repack / qmm_unrepack are bit-exact inverses, and a repacked matrix
+    gives the oracle's result through the normal entry point."""
+    import torch
+
+    p = synth.make_problem(91, 200, 1024, 4, 64)
+    dp = DeviceProblem(p)
+    native = binding.repack(dp.wq, 4)
+    back = binding.repack(native, 4, inverse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(native, dp.wq) and torch.equal(back, dp.wq)
+    ref = OracleRef(p)
+    y_ref, a_ref = ref.full(5)
+    y = binding.small_m(dp.x[:5].contiguous(), native, dp.s, dp.b, 4, 64, out_dtype=torch.float32)
+    assert_within(to_f64(y), y_ref, a_ref, "repacked weights")
+
