@@ -73,6 +73,8 @@ const VariantDesc kVariants[] = {
     {"tma_own_w4_d4_2cta", kFamilyOwn, 4, 4, 2},
     {"tma_own_w8_d3_half", kFamilyOwn, 3, 8, 2, 1},
     {"tma_own_w4_d4_half", kFamilyOwn, 4, 4, 2, 1},
+    {"tma_own_w8_d2_2cta", kFamilyOwn, 2, 8, 2},
+    {"tma_own_w8_d2_1cta", kFamilyOwn, 2, 8, 1},
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
@@ -380,6 +382,28 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
     int ts = 1;
     v = select_variant(a, &ts);
     if (s < 0) s = ts;
+    // The table's choice was measured on this shape; if it cannot be planned
+    // here (another device, or a resource limit that changed), take the
+    // rule-based choice rather than failing.
+    const VariantDesc& dt = kVariants[v];
+    bool ok = true;
+    if (dt.family == kFamilyTma) ok = s >= 1 && tma_supported(a, s, dt);
+    if (dt.family == kFamilyOwn) ok = s >= 1 && launch_own(a, dt, s, st, true) == cudaSuccess;
+    if (!ok) {
+      v = -1;
+      for (int dv : {kDefaultTma, kDefaultTma1}) {
+        const int c = rule_tma_cluster(a, kVariants[dv]);
+        if (c > 0) {
+          v = dv;
+          s = c;
+          break;
+        }
+      }
+      if (v < 0) {
+        v = 0;
+        s = rule_splits(kVariants[0], a.N, a.K, a.gs);
+      }
+    }
   }
   const VariantDesc& d = kVariants[v];
   if (s < 0 && d.family == kFamilyOwn) {

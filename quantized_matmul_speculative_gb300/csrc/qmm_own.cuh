@@ -75,8 +75,10 @@ struct OwnLayout {
   }
 };
 
+// With W <= 8 two CTAs must fit an SM (the "2cta" shared-memory budget and
+// the next call's CTAs under PDL), which caps registers at 128 per thread.
 template <int BITS, int GS, int NB, int W, int D>
-__global__ void __launch_bounds__(32 * W, 1)
+__global__ void __launch_bounds__(32 * W, (W <= 8) ? 2 : 1)
 qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const OwnParams p) {
   using GM = GroupMath<BITS, GS, NB>;
@@ -187,10 +189,13 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       }
     }
   };
+  // Tiles strictly inside this warp's range have no other contributor.
+  const int first_tile = (nu > 0) ? ua / p.kp : 0;
+  const int last_tile = (nu > 0) ? (ua + nu - 1) / p.kp : -1;
   // Hand this warp's partial of tile i to the tile's owner.
   auto push = [&](int i, const float (&acc)[NB][4]) {
-    int slot;
-    const int n = own_contributors(i, p.kp, U, W, warp, &slot);
+    int slot = 0;
+    const int n = (i > first_tile && i < last_tile) ? 1 : own_contributors(i, p.kp, U, W, warp, &slot);
     if (csize == 1 && n == 1) {
       write_y(i, acc);
       return;

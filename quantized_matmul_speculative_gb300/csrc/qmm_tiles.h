@@ -17,4 +17,5 @@
 #define QMM_OWN_TILES(X) \
   X(8, 3)                \
   X(16, 2)               \
-  X(4, 4)
+  X(4, 4)                \
+  X(8, 2)
