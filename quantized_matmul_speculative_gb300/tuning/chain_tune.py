@@ -30,17 +30,24 @@ from quantized_matmul_speculative_gb300 import binding, build, synth, workloads 
 from quantized_matmul_speculative_gb300.tuning.make_table import EXCLUDED_SUFFIXES  # noqa: E402
 
 
-def isolated_candidates(sweep_path: Path, top: int):
-    """(M, N, K) -> [(variant name, splits)] best first, from the isolated sweep."""
-    rows = {}
+def isolated_candidates(sweep_path: Path, top: int, top_excluded: int):
+    """(M, N, K) -> [(variant name, splits)] from the isolated sweep: the `top`
+    fastest the table may pick, then the `top_excluded` fastest of the
+    variants it never picks on its own (those are judged here, in the chain)."""
+    rows, extra = {}, {}
     for line in sweep_path.read_text().splitlines():
         if not line.strip():
             continue
         r = json.loads(line)
-        if "us" not in r or r["variant"].endswith(EXCLUDED_SUFFIXES):
+        if "us" not in r:
             continue
-        rows.setdefault((r["M"], r["N"], r["K"]), []).append((r["us"], r["variant"], r["splits"]))
-    return {k: [(v, s) for _, v, s in sorted(c)[:top]] for k, c in rows.items()}
+        dst = extra if r["variant"].endswith(EXCLUDED_SUFFIXES) else rows
+        dst.setdefault((r["M"], r["N"], r["K"]), []).append((r["us"], r["variant"], r["splits"]))
+    out = {}
+    for k, c in rows.items():
+        out[k] = [(v, s) for _, v, s in sorted(c)[:top]]
+        out[k] += [(v, s) for _, v, s in sorted(extra.get(k, []))[:top_excluded]]
+    return out
 
 
 def main():
@@ -48,6 +55,7 @@ def main():
     ap.add_argument("--sweep", required=True)
     ap.add_argument("--out", required=True)
     ap.add_argument("--top", type=int, default=4)
+    ap.add_argument("--top-excluded", type=int, default=2)
     ap.add_argument("--passes", type=int, default=2)
     ap.add_argument("--steps", type=int, default=8)
     args = ap.parse_args()
@@ -61,7 +69,7 @@ def main():
     names = binding.variant_names()
     w = workloads.VERIFY_STEP
     bits, gs = w.bits, w.group_size
-    cands = isolated_candidates(Path(args.sweep), args.top)
+    cands = isolated_candidates(Path(args.sweep), args.top, args.top_excluded)
 
     mats = []
     x0 = None
