@@ -103,7 +103,8 @@ def main():
     unit_r, unit_w = rm["dram__bytes_read.sum"][1], rm["dram__bytes_write.sum"][1]
     mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     per_launch = [r * mult.get(unit_r, 1) + w * mult.get(unit_w, 1) for r, w in zip(reads, writes)]
-    lines = [f"# ncu summary: qmm_tma_kernel on {a.workload}", ""]
+    family = next((f for f in ("qmm_own_kernel", "qmm_tma_kernel", "qmm_mma_kernel") if f in rm["kernel"]), rm["kernel"])
+    lines = [f"# ncu summary: {family} on {a.workload}", ""]
     if a.note:
         lines += [a.note, ""]
     lines += ["kernel_source_hash: " + kernel_hash(),
