@@ -64,7 +64,9 @@ class OracleLib:
         lib.oracle_qmm.argtypes = [vp, vp, vp, vp, i64, i64, i64, c_int, i64, vp, vp]
         lib.oracle_qmm_sampled.argtypes = [vp, vp, vp, vp, i64, i64, i64, c_int, i64, vp, vp, i64, vp, vp]
         lib.oracle_dequant.argtypes = [vp, vp, vp, i64, i64, c_int, i64, vp]
-        for name in ("oracle_pack", "oracle_unpack", "oracle_qmm", "oracle_qmm_sampled", "oracle_dequant"):
+        lib.oracle_qmm_residual.argtypes = [vp, vp, vp, vp, vp, c_int, i64, i64, i64, c_int, i64, vp, vp]
+        for name in ("oracle_pack", "oracle_unpack", "oracle_qmm", "oracle_qmm_sampled", "oracle_dequant",
+                     "oracle_qmm_residual"):
             getattr(lib, name).restype = c_int
         self.lib = lib
 
@@ -108,6 +110,28 @@ class OracleLib:
         rc = self.lib.oracle_qmm(_ptr(x), _ptr(wq), _ptr(s), _ptr(b), m, n, k, bits, group_size, _ptr(y), _ptr(a))
         if rc:
             raise OracleError(f"oracle_qmm rc={rc}")
+        return y, a
+
+    def qmm_residual(self, x_bits, wq, s_bits, b_bits, r, bits: int, group_size: int):
+        """Return (Y, A) of Y = R + X . W^T in fp64.  ``r``: [M, N] bf16 bit
+        patterns (uint16) or float32 values."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        wq = np.ascontiguousarray(wq, dtype=np.uint32)
+        s = np.ascontiguousarray(s_bits, dtype=np.uint16)
+        b = np.ascontiguousarray(b_bits, dtype=np.uint16)
+        r = np.ascontiguousarray(r)
+        if r.dtype not in (np.uint16, np.float32):
+            raise OracleError("r must be uint16 (bf16 bits) or float32")
+        m, k = x.shape
+        n = wq.shape[0]
+        if r.shape != (m, n):
+            raise OracleError("r must be [M, N]")
+        y = np.empty((m, n), dtype=np.float64)
+        a = np.empty((m, n), dtype=np.float64)
+        rc = self.lib.oracle_qmm_residual(_ptr(x), _ptr(wq), _ptr(s), _ptr(b), _ptr(r), int(r.dtype == np.float32),
+                                          m, n, k, bits, group_size, _ptr(y), _ptr(a))
+        if rc:
+            raise OracleError(f"oracle_qmm_residual rc={rc}")
         return y, a
 
     def qmm_sampled(self, x_bits, wq, s_bits, b_bits, bits: int, group_size: int, ms, ns):

@@ -29,6 +29,11 @@
 //    code k sits at bit offset b * (k mod (32/b)).
 //  * Unsigned codes 0 .. 2^b - 1; "affine" adds the bias, there is no other
 //    zero point.
+//  * Fused residual add (oracle_qmm_residual): Y = R + X · W^T, the sum that
+//    a MUL_MAT + ADD fusion writes from the matmul's store.
+//      - "metal : few-row MMA mat-mul and batched copies for speculative
+//        decoding" (llama.cpp PR #29869), Overview: the fusion-table entry
+//        MUL_MAT + ADD.
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
 // shapes, closed forms (all-zero codes, one-hot X, X = 1, saturated codes),
@@ -168,6 +173,23 @@ int oracle_qmm(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, const u
       Y[m * N + n] = y;
       if (A) A[m * N + n] = a;
     }
+  }
+  return 0;
+}
+
+// Y = R + X · dequant(W)^T.  R[M,N] is given as bf16 bit patterns (r_is_f32 = 0,
+// uint16) or as binary32 values (r_is_f32 = 1, float).  The product is the
+// sum over k in ascending order as in oracle_qmm, then r is added; A = |r| +
+// sum_k |x*w| (the tolerance scale of the rounded sum).
+int oracle_qmm_residual(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, const uint16_t* B, const void* R,
+                        int r_is_f32, int64_t M, int64_t N, int64_t K, int bits, int64_t g, double* Y, double* A) {
+  const int rc = oracle_qmm(X, Wq, S, B, M, N, K, bits, g, Y, A);
+  if (rc) return rc;
+  for (int64_t i = 0; i < M * N; ++i) {
+    const double r = r_is_f32 ? static_cast<double>(static_cast<const float*>(R)[i])
+                              : bf16_bits_to_double(static_cast<const uint16_t*>(R)[i]);
+    Y[i] = r + Y[i];
+    if (A) A[i] = std::fabs(r) + A[i];
   }
   return 0;
 }

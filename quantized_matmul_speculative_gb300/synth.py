@@ -12,7 +12,9 @@ Recipe (one numpy PCG64 stream per tensor, keyed by ``(seed, stream)``):
 * ``bias  = fp16(-(2^bits - 1)/2 * scale)``, i.e. ``-7.5 * scale`` at 4 bits
   and ``-1.5 * scale`` at 2 bits (the scale is taken after its fp16 rounding);
 * ``X = bf16(N(0,1))`` drawn for 16 rows; an M-row problem uses the first M
-  rows, so every M of a sweep sees the same leading rows.
+  rows, so every M of a sweep sees the same leading rows;
+* a residual ``R = N(0,1)`` per output element, stored as bf16 bit patterns
+  or as float32 (the output dtype it is added in).
 
 Rounding to fp16 is numpy's (round to nearest even); rounding binary32 to
 bf16 is round to nearest even on the bit pattern.
@@ -28,6 +30,7 @@ MAX_ROWS = 16
 STREAM_CODES = 0
 STREAM_SCALES = 1
 STREAM_X = 2
+STREAM_RESIDUAL = 3
 
 
 def rng_for(seed: int, stream: int) -> np.random.Generator:
@@ -87,6 +90,12 @@ def make_scales_biases(seed: int, N: int, groups: int, bits: int):
 def make_x(seed: int, K: int, rows: int = MAX_ROWS) -> np.ndarray:
     z = rng_for(seed, STREAM_X).standard_normal(size=(rows, K), dtype=np.float32)
     return f32_to_bf16_bits(z)
+
+
+def make_residual(seed: int, M: int, N: int, f32: bool = False) -> np.ndarray:
+    """R[M, N]: bf16 bit patterns (uint16), or float32 values if ``f32``."""
+    z = rng_for(seed, STREAM_RESIDUAL).standard_normal(size=(M, N), dtype=np.float32)
+    return z if f32 else f32_to_bf16_bits(z)
 
 
 def make_problem(seed: int, N: int, K: int, bits: int, group_size: int, rows: int = MAX_ROWS) -> Problem:

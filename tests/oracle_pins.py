@@ -217,6 +217,32 @@ def pin_invariants(lib):
     assert np.array_equal(yp, y[:, perm]), "row permutation"
 
 
+def pin_residual(lib):
+    """Y = R + X . W^T: exact rational sums for bf16 and fp32 residuals, X = 0
+    gives R exactly, R = 0 gives the plain product bit for bit."""
+    M, N, K, bits, g = 2, 5, 128, 4, 32
+    p = synth.make_problem(996, N, K, bits, g, rows=M)
+    wq = lib.pack(p.q, bits)
+    ye, ae = exact_product(p, M)
+    for f32 in (False, True):
+        r = synth.make_residual(996, M, N, f32=f32)
+        rf = [[Fraction(float(v)) for v in row] for row in (r if f32 else synth.bf16_bits_to_f32(r))]
+        y, a = lib.qmm_residual(p.x_rows(M), wq, p.scales, p.biases, r, bits, g)
+        for m in range(M):
+            for n in range(N):
+                ref, mag = rf[m][n] + ye[m][n], abs(rf[m][n]) + ae[m][n]
+                assert abs(Fraction(float(y[m, n])) - ref) <= Fraction(1, 10**12) * mag, f"residual y[{m},{n}]"
+                assert abs(Fraction(float(a[m, n])) - mag) <= Fraction(1, 10**12) * mag, f"residual a[{m},{n}]"
+        x0 = np.zeros_like(p.x_rows(M))
+        y0, _ = lib.qmm_residual(x0, wq, p.scales, p.biases, r, bits, g)
+        rr = r.astype(np.float64) if f32 else synth.bf16_bits_to_f32(r).astype(np.float64)
+        assert np.array_equal(y0, rr), "X = 0 must give R"
+    zero = np.zeros((M, N), dtype=np.float32)
+    yz, az = lib.qmm_residual(p.x_rows(M), wq, p.scales, p.biases, zero, bits, g)
+    yp, ap = lib.qmm(p.x_rows(M), wq, p.scales, p.biases, bits, g)
+    assert np.array_equal(yz, yp) and np.array_equal(az, ap), "R = 0 must give the plain product"
+
+
 def pin_sampled(lib):
     M, N, K, bits, g = 4, 11, 192, 2, 64
     p = synth.make_problem(995, N, K, bits, g, rows=M)
@@ -231,5 +257,5 @@ def pin_sampled(lib):
 # Pins that run fast enough for the mutation test (the exhaustive decoder pin
 # is run once against the real oracle only).
 FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
-             pin_invariants, pin_sampled)
+             pin_invariants, pin_residual, pin_sampled)
 ALL_PINS = (pin_decoders,) + FAST_PINS

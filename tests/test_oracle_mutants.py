@@ -18,6 +18,8 @@ MUTANTS = [
     ("abs_dropped", "a += std::fabs(p);\n      }\n      Y[m * N + n] = y;", "a += p;\n      }\n      Y[m * N + n] = y;"),
     ("half_bias", "expo - 25", "expo - 24"),
     ("bf16_frac", "128 + frac), expo - 134", "127 + frac), expo - 134"),
+    ("residual_sign", "Y[i] = r + Y[i];", "Y[i] = Y[i] - r;"),
+    ("residual_dropped_from_scale", "A[i] = std::fabs(r) + A[i];", "A[i] = A[i];"),
 ]
 
 
