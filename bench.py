@@ -314,6 +314,48 @@ def verify_step_report(torch, dev, stream, peak, ms=tuple(range(1, 9)), steps=10
             "per_m": res, "chain": "each projection reads the first M*K elements of the previous output"}
 
 
+def residual_report(torch, dev, stream, ms=(1, 8, 16)):
+    """The fused residual add on the 5120x5120 layer at the dispatcher's choice:
+    us per call without a residual, with a separate residual buffer, and in
+    place (R is Y), bf16.  Same chains as configs_report."""
+    from quantized_matmul_speculative_gb300 import binding
+
+    w = workloads.M_SWEEP
+    sh = w.shapes[0]
+    bits, gs = w.bits, w.group_size
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = stream.cuda_stream
+    p = synth.make_problem(workloads.shape_seed(w, 0), sh.N, sh.K, bits, gs)
+    cb = workloads.call_bytes(sh.N, sh.K, bits, gs)
+    ncopy = max(2, int(np.ceil(4 * l2 / cb)) + 1)
+    wq = torch.from_numpy(binding.pack(p.q, bits).view(np.int32))
+    sc = torch.from_numpy(p.scales.view(np.float16))
+    bi = torch.from_numpy(p.biases.view(np.float16))
+    copies = [(wq.to(dev), sc.to(dev), bi.to(dev)) for _ in range(ncopy)]
+    x = torch.from_numpy(p.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((16, sh.N), dtype=torch.bfloat16, device=dev)
+    r = torch.from_numpy(synth.make_residual(1, 16, sh.N).view(np.int16)).to(dev).view(torch.bfloat16)
+    res = []
+    for M in ms:
+        row = {"M": M}
+        for mode in ("plain", "residual", "in_place"):
+            def capture(i, M=M, mode=mode):
+                wq_d, s_d, b_d = copies[i % ncopy]
+                args = (x.data_ptr(), wq_d.data_ptr(), s_d.data_ptr(), b_d.data_ptr())
+                if mode == "plain":
+                    binding.small_m_ptr(*args, M, sh.N, sh.K, bits, gs, y.data_ptr(), binding.OUT_BF16, -1, -1,
+                                        handle)
+                else:
+                    rp = r.data_ptr() if mode == "residual" else y.data_ptr()
+                    binding.small_m_residual_ptr(*args, rp, M, sh.N, sh.K, bits, gs, y.data_ptr(), binding.OUT_BF16,
+                                                 -1, -1, handle)
+            row[f"us_{mode}"] = round(graph_us_per_call(torch, stream, capture, 64), 3)
+        res.append(row)
+    del copies
+    torch.cuda.empty_cache()
+    return {"op": "fused residual add Y = R + X W^T, 5120x5120 4-bit g64, bf16", "per_m": res}
+
+
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):
     """bf16 dense torch.matmul (cuBLAS) on the 5120x5120 layer, for scale only:
     the dense bf16 weights are 4x the bytes of the 4-bit ones."""
@@ -513,6 +555,7 @@ def run_ours(args, world, rank, local):
         extra["configs"] = configs_report(torch, dev, stream, peak)
         extra["verify_step"] = verify_step_report(torch, dev, stream, peak)
         extra["controls"] = dense_control(torch, dev, stream)
+        extra["residual"] = residual_report(torch, dev, stream)
     kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
                       "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
 

@@ -55,7 +55,8 @@ typedef enum {
   QMM_OK = 0,
   QMM_ERR_NULL = 1,        /* a required pointer is null                          */
   QMM_ERR_SHAPE = 2,       /* M outside 0..16, N or K negative, K not a multiple   */
-                           /* of group_size, or a size that overflows              */
+                           /* of group_size, a size that overflows, or a residual  */
+                           /* that partly overlaps Y                               */
   QMM_ERR_UNSUPPORTED = 3, /* bits not in {2,4}, group_size not in {32,64,128},    */
                            /* unknown variant, bad split count or output dtype     */
   QMM_ERR_ALIGN = 4,       /* X or Wq not 16-byte aligned, scales/biases/Y not     */
@@ -84,6 +85,19 @@ qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, co
 qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
                           int M, int N, int K, int bits, int group_size, void* Y,
                           int out_dtype, int variant, int splits, void* stream);
+
+/* Fused residual add: Y = R + X . dequant(W)^T.  R has Y's dtype and layout
+ * ([M, N], bf16 or fp32 per out_dtype) and is added to the fp32 result in the
+ * kernel's store, before the single rounding to Y's dtype; R may be Y itself
+ * (an in-place update of a residual stream) but must not otherwise overlap it.
+ * Other arguments, errors and dispatch as qmm_small_m_ex; R == NULL with a
+ * non-empty output returns QMM_ERR_NULL.  K == 0 gives Y = R.
+ * Source: "metal : few-row MMA mat-mul and batched copies for speculative
+ * decoding" (llama.cpp PR #29869), Overview: a fusion-table entry for
+ * MUL_MAT + ADD writes the residual sum from the MMA store.                    */
+qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                                const void* R, int M, int N, int K, int bits, int group_size, void* Y,
+                                int out_dtype, int variant, int splits, void* stream);
 
 /* Number of uint32 words of a packed [N, K] matrix: N * K * bits / 32
  * (0 if bits is unsupported or K*bits is not a multiple of 32).                 */

@@ -31,6 +31,8 @@ _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
 SIGNATURES = {
     "qmm_small_m": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "qmm_small_m_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
+    "qmm_small_m_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32,
+                                    _vp]),
     "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
     "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
     "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
@@ -146,13 +148,24 @@ def small_m_ptr(x_ptr: int, wq_ptr: int, s_ptr: int, b_ptr: int, M: int, N: int,
     _check(rc, "qmm_small_m_ex")
 
 
+def small_m_residual_ptr(x_ptr: int, wq_ptr: int, s_ptr: int, b_ptr: int, r_ptr: int, M: int, N: int, K: int,
+                         bits: int, group_size: int, y_ptr: int, out_dtype: int = OUT_BF16, variant: int = -1,
+                         splits: int = -1, stream: int = 0) -> None:
+    """Raw-pointer call of qmm_small_m_residual: Y = R + X . dequant(W)^T."""
+    rc = lib().qmm_small_m_residual(x_ptr, wq_ptr, s_ptr, b_ptr, r_ptr, M, N, K, bits, group_size, y_ptr,
+                                    out_dtype, variant, splits, stream)
+    _check(rc, "qmm_small_m_residual")
+
+
 def small_m(x, wq, scales, biases, bits: int, group_size: int, out=None, out_dtype=None,
-            variant: int = -1, splits: int = -1, stream=None):
-    """Y = X . dequant(Wq, scales, biases)^T on the GPU.
+            variant: int = -1, splits: int = -1, stream=None, residual=None):
+    """Y = X . dequant(Wq, scales, biases)^T on the GPU (+ ``residual``).
 
     ``x``: bf16 [M, K]; ``wq``: int32/uint32 [N, K*bits/32]; ``scales``,
     ``biases``: fp16 [N, K/group_size]; all CUDA tensors, contiguous.  Returns
-    ``out`` (bf16 or fp32 [M, N]), allocated by torch if not given.
+    ``out`` (bf16 or fp32 [M, N]), allocated by torch if not given.  With
+    ``residual`` (a contiguous [M, N] tensor of the output dtype, which may be
+    ``out`` itself) the kernels store residual + product.
     """
     import torch
 
@@ -180,6 +193,14 @@ def small_m(x, wq, scales, biases, bits: int, group_size: int, out=None, out_dty
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    small_m_ptr(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), M, N, K, bits, group_size,
-                out.data_ptr(), OUT_F32 if out_dtype == torch.float32 else OUT_BF16, variant, splits, handle)
+    od = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    if residual is None:
+        small_m_ptr(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), M, N, K, bits, group_size,
+                    out.data_ptr(), od, variant, splits, handle)
+        return out
+    if (not residual.is_cuda or not residual.is_contiguous() or tuple(residual.shape) != (M, N)
+            or residual.dtype != out_dtype):
+        raise ValueError("residual must be a contiguous CUDA [M, N] tensor of the output dtype")
+    small_m_residual_ptr(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), residual.data_ptr(),
+                         M, N, K, bits, group_size, out.data_ptr(), od, variant, splits, handle)
     return out

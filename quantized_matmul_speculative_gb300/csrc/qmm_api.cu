@@ -336,9 +336,14 @@ unsigned int qmm_device_status(int clear) {
   return v;
 }
 
-qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N,
-                          int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,
-                          void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One call of either entry point; R is the residual (null: none).
+qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const void* biases, const void* R, int M,
+                    int N, int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,
+                    void* stream) {
   if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
   if (bits != 2 && bits != 4) return QMM_ERR_UNSUPPORTED;
   if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
@@ -350,9 +355,18 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
   const size_t esize = out_dtype == QMM_OUT_F32 ? 4 : 2;
   if (Y == nullptr) return QMM_ERR_NULL;
   if (!aligned(Y, esize)) return QMM_ERR_ALIGN;
+  const size_t ybytes = static_cast<size_t>(M) * static_cast<size_t>(N) * esize;
+  if (R != nullptr) {
+    if (!aligned(R, esize)) return QMM_ERR_ALIGN;
+    const uintptr_t r0 = reinterpret_cast<uintptr_t>(R), y0 = reinterpret_cast<uintptr_t>(Y);
+    if (r0 != y0 && r0 < y0 + ybytes && y0 < r0 + ybytes) return QMM_ERR_SHAPE;  // partial overlap
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (K == 0) {
-    const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * static_cast<size_t>(N) * esize, st);
+    // the empty sum: Y = 0, or Y = R
+    const cudaError_t e = (R == nullptr) ? cudaMemsetAsync(Y, 0, ybytes, st)
+                          : (R == Y)     ? cudaSuccess
+                                         : cudaMemcpyAsync(Y, R, ybytes, cudaMemcpyDeviceToDevice, st);
     return e == cudaSuccess ? QMM_OK : fail_cuda(e);
   }
   if (X == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
@@ -364,6 +378,7 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
   a.S = static_cast<const uint16_t*>(scales);
   a.B = static_cast<const uint16_t*>(biases);
   a.Y = Y;
+  a.R = R;
   a.M = M;
   a.N = N;
   a.K = K;
@@ -439,6 +454,23 @@ qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales,
                         : (d.family == kFamilyOwn) ? launch_own(a, d, s, st, false)
                                                    : cudaErrorInvalidValue;
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N,
+                          int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,
+                          void* stream) {
+  return run_call(X, Wq, scales, biases, nullptr, M, N, K, bits, group_size, Y, out_dtype, variant, splits, stream);
+}
+
+qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                                const void* R, int M, int N, int K, int bits, int group_size, void* Y, int out_dtype,
+                                int variant, int splits, void* stream) {
+  if (M > 0 && N > 0 && R == nullptr) return QMM_ERR_NULL;
+  return run_call(X, Wq, scales, biases, R, M, N, K, bits, group_size, Y, out_dtype, variant, splits, stream);
 }
 
 qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N, int K,

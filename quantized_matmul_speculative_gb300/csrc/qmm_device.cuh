@@ -237,6 +237,20 @@ __device__ __forceinline__ void ffma2(float& a0, float& a1, float b0, float b1, 
       : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// The epilogue store of one output element: Y[off] = v, or with a residual R
+// (Y's dtype and layout) Y[off] = R[off] + v, added in fp32 and rounded once
+// to Y's dtype.  The same thread reads R[off] before it writes Y[off], so R may
+// be Y itself (an in-place residual update).
+__device__ __forceinline__ void store_y(void* Y, const void* R, int64_t off, float v, int out_f32) {
+  if (out_f32) {
+    if (R != nullptr) v += static_cast<const float*>(R)[off];
+    static_cast<float*>(Y)[off] = v;
+  } else {
+    if (R != nullptr) v += __bfloat162float(static_cast<const __nv_bfloat16*>(R)[off]);
+    static_cast<__nv_bfloat16*>(Y)[off] = __float2bfloat16_rn(v);
+  }
+}
+
 // Split cluster barrier: arrive (release) now, wait (acquire) later.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

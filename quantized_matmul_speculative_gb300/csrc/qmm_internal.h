@@ -13,6 +13,7 @@ struct CallArgs {
   const uint16_t* S;   // fp16 [N, K/gs]
   const uint16_t* B;   // fp16 [N, K/gs]
   void* Y;             // bf16 or fp32 [M, N]
+  const void* R;       // residual, Y's dtype [M, N], added in the store; may be Y; null: none
   int M, N, K, bits, gs, out_f32;
 };
 

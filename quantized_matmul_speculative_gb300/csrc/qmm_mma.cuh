@@ -56,6 +56,7 @@ struct MmaParams {
   const uint16_t* __restrict__ S;
   const uint16_t* __restrict__ B;
   void* __restrict__ Y;
+  const void* R;  // residual added to Y (Y's dtype, [M, N]), may be Y itself; null: none
   int M, N, K;
   int G;        // groups per row (K / GS)
   int gpc;      // groups per CTA K-range
@@ -308,8 +309,7 @@ qmm_mma_kernel(const MmaParams p) {
       const int n = n0 + (e - m * C::NT);
       if (n < p.N) {
         const int64_t o = static_cast<int64_t>(m) * p.N + n;
-        if (p.out_f32) static_cast<float*>(p.Y)[o] = v;
-        else static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(v);
+        store_y(p.Y, p.R, o, v, p.out_f32);
       }
     }
     return;
@@ -332,8 +332,7 @@ qmm_mma_kernel(const MmaParams p) {
     const int n = n0 + (e - m * C::NT);
     if (n < p.N) {
       const int64_t o = static_cast<int64_t>(m) * p.N + n;
-      if (p.out_f32) static_cast<float*>(p.Y)[o] = v;
-      else static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(v);
+      store_y(p.Y, p.R, o, v, p.out_f32);
     }
   }
   cluster_sync_all();  // keep this CTA's shared memory alive until all peers have read it

@@ -21,6 +21,7 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   p.S = a.S;
   p.B = a.B;
   p.Y = a.Y;
+  p.R = a.R;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;

@@ -38,6 +38,7 @@ namespace qmm {
 struct OwnParams {
   const uint16_t* __restrict__ X;
   void* __restrict__ Y;
+  const void* R;  // residual added to Y (Y's dtype, [M, N]), may be Y itself; null: none
   int M, N, K;
   int gp;                       // groups per CTA K-piece (G / C)
   unsigned long long gp_magic;  // ceil(2^32 / gp), for u / gp = (u * gp_magic) >> 32
@@ -183,8 +184,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         const int n = (e < 2) ? n_lo : n_hi;
         if (m < p.M && n < p.N) {
           const int64_t off = static_cast<int64_t>(m) * p.N + n;
-          if (p.out_f32) static_cast<float*>(p.Y)[off] = v[nb][e];
-          else static_cast<__nv_bfloat16*>(p.Y)[off] = __float2bfloat16_rn(v[nb][e]);
+          store_y(p.Y, p.R, off, v[nb][e], p.out_f32);
         }
       }
     }

@@ -27,6 +27,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
   p->X = a.X;
   p->Y = a.Y;
+  p->R = a.R;
   p->M = a.M;
   p->N = a.N;
   p->K = a.K;

@@ -59,6 +59,7 @@ struct TmaParams {
   const uint16_t* __restrict__ S;
   const uint16_t* __restrict__ B;
   void* __restrict__ Y;
+  const void* R;  // residual added to Y (Y's dtype, [M, N]), may be Y itself; null: none
   int M, N, K;
   int G;          // groups per row
   int gp;         // groups per K-piece (G / C), even
@@ -391,8 +392,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         const int n = (t_begin + i) * 16 + (r & 15);
         if (n < p.N) {
           const int64_t off = static_cast<int64_t>(m) * p.N + n;
-          if (p.out_f32) static_cast<float*>(p.Y)[off] = v;
-          else static_cast<__nv_bfloat16*>(p.Y)[off] = __float2bfloat16_rn(v);
+          store_y(p.Y, p.R, off, v, p.out_f32);
         }
       }
       QMM_TRACE_POINT(6);
@@ -412,8 +412,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         const int n = (t_begin + i) * 16 + (e & 15);
         if (n < p.N) {
           const int64_t o = static_cast<int64_t>(m) * p.N + n;
-          if (p.out_f32) static_cast<float*>(p.Y)[o] = v;
-          else static_cast<__nv_bfloat16*>(p.Y)[o] = __float2bfloat16_rn(v);
+          store_y(p.Y, p.R, o, v, p.out_f32);
         }
       }
     }

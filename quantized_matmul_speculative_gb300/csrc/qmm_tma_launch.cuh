@@ -70,6 +70,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.S = a.S;
   p.B = a.B;
   p.Y = a.Y;
+  p.R = a.R;
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;

@@ -79,6 +79,28 @@ def test_validation_before_launch(lib):
     assert rc(M=0) == 0 and rc(N=0) == 0  # nothing to compute
 
 
+def test_residual_validation_before_launch(lib):
+    """qmm_small_m_residual rejects a missing, misaligned or partly overlapping
+    residual before any CUDA call (the pointers are never dereferenced)."""
+    call = lib.qmm_small_m_residual
+    p, r, y = 0x10000, 0x200000, 0x400000
+    # (X, Wq, S, B, R, M, N, K, bits, gs, Y, out, variant, splits, stream)
+    base = [p, p, p, p, r, 4, 64, 256, 4, 64, y, 0, -1, -1, None]
+
+    def rc(**kw):
+        a = list(base)
+        pos = {"R": 4, "M": 5, "N": 6, "Y": 10, "out": 11}
+        for k, v in kw.items():
+            a[pos[k]] = v
+        return call(*a)
+
+    assert rc(R=None) == 1
+    assert rc(R=r + 1) == 4 and rc(R=r + 2, out=1) == 4      # bf16 needs 2-byte, fp32 4-byte alignment
+    assert rc(R=y + 2) == 2 and rc(R=y - 2) == 2              # partly overlaps Y
+    assert rc(R=None, M=0) == 0 and rc(R=None, N=0) == 0      # nothing to compute
+    assert rc(M=17) == 2
+
+
 def test_variant_registry(lib):
     names = binding.variant_names()
     assert len(names) == lib.qmm_num_variants() >= 1
