@@ -29,6 +29,11 @@
 //    code k sits at bit offset b * (k mod (32/b)).
 //  * Unsigned codes 0 .. 2^b - 1; "affine" adds the bias, there is no other
 //    zero point.
+//  * Code widths b = 2, 4 and 8.  The 8-bit affine mode is the same
+//    definition with four codes per word:
+//      - "MLX quantized_matmul small-M verify kernels", facts "qmv_wide
+//        speedup" (int8 at M=8) and "mlx-dspark skinny_qmm" (widths 6-16 at
+//        8-bit).
 //  * Fused residual add (oracle_qmm_residual): Y = R + X · W^T, the sum that
 //    a MUL_MAT + ADD fusion writes from the matmul's store.
 //      - "metal : few-row MMA mat-mul and batched copies for speculative
@@ -36,9 +41,10 @@
 //        MUL_MAT + ADD.
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
-// shapes, closed forms (all-zero codes, one-hot X, X = 1, saturated codes),
-// the scale=1/bias=0 special case against numpy's integer matmul, linearity,
-// row-permutation and batch invariance, and the two documented pack words.
+// shapes (2-, 4- and 8-bit), closed forms (all-zero codes, one-hot X, X = 1,
+// saturated codes), the scale=1/bias=0 special case against numpy's integer
+// matmul, linearity, row-permutation and batch invariance, the documented
+// pack words, and the residual form.
 
 #include <cmath>
 #include <cstdint>

@@ -65,6 +65,9 @@ TINY_CASES = [
     (3, 4, 64, 2, 32),
     (2, 3, 128, 2, 64),
     (2, 2, 256, 2, 128),
+    (2, 3, 64, 8, 32),
+    (3, 2, 128, 8, 64),
+    (1, 2, 256, 8, 128),
 ]
 
 
@@ -146,7 +149,7 @@ def pin_brute_force(lib):
 
 
 def pin_closed_forms(lib):
-    for bits, g in ((4, 64), (4, 32), (2, 64), (4, 128)):
+    for bits, g in ((4, 64), (4, 32), (2, 64), (4, 128), (8, 64), (8, 32)):
         M, N, K = 3, 6, 4 * g
         G = K // g
         p = synth.make_problem(950 + bits * 10 + g, N, K, bits, g, rows=M)
@@ -180,7 +183,7 @@ def pin_closed_forms(lib):
 
 def pin_integer_special_case(lib):
     # scale 1, bias 0: y = X @ Q^T, an integer-matrix times bf16 product
-    for bits, g in ((4, 64), (2, 32)):
+    for bits, g in ((4, 64), (2, 32), (8, 64)):
         M, N, K = 4, 7, 256
         p = synth.make_problem(970 + bits, N, K, bits, g, rows=M)
         ones = np.full(p.scales.shape, FP16_ONE, dtype=np.uint16)
