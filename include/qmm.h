@@ -22,9 +22,10 @@
  *   X       bf16 [M, K]                         device
  *   Wq      uint32 [N, K*bits/32]               device
  *           code k of row n sits in word k/(32/bits) of that row at bit
- *           offset bits*(k mod (32/bits)); codes are unsigned 0..2^bits-1.
- *           (The pages print no bit layout; this is the layout qmm_pack
- *           writes.)
+ *           offset bits*(k mod (32/bits)); codes are unsigned 0..2^bits-1,
+ *           bits = 2, 4 or 8.  (The pages print no bit layout; this is the
+ *           layout qmm_pack writes.  8-bit affine: same page, facts
+ *           "qmv_wide speedup" (int8 at M=8) and "mlx-dspark skinny_qmm".)
  *   scales  fp16 [N, K/group_size]              device
  *   biases  fp16 [N, K/group_size]              device
  *           w[n,k] = scales[n, k/g] * q[n,k] + biases[n, k/g]
@@ -57,7 +58,7 @@ typedef enum {
   QMM_ERR_SHAPE = 2,       /* M outside 0..16, N or K negative, K not a multiple   */
                            /* of group_size, a size that overflows, or a residual  */
                            /* that partly overlaps Y                               */
-  QMM_ERR_UNSUPPORTED = 3, /* bits not in {2,4}, group_size not in {32,64,128},    */
+  QMM_ERR_UNSUPPORTED = 3, /* bits not in {2,4,8}, group_size not in {32,64,128},  */
                            /* unknown variant, bad split count or output dtype     */
   QMM_ERR_ALIGN = 4,       /* X or Wq not 16-byte aligned, scales/biases/Y not     */
                            /* aligned to their element size                        */

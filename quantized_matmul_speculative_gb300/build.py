@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               f"-I{INCLUDE}", f"-I{CSRC}"]
 
-MMA_INSTANCES = [(4, 32), (4, 64), (4, 128), (2, 32), (2, 64), (2, 128)]
+MMA_INSTANCES = [(4, 32), (4, 64), (4, 128), (2, 32), (2, 64), (2, 128), (8, 32), (8, 64), (8, 128)]
 
 
 def nvcc() -> str:

@@ -30,6 +30,9 @@ extern template cudaError_t launch_mma_bg<4, 128>(const CallArgs&, const Variant
 extern template cudaError_t launch_mma_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<8, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<8, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_bg<8, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template <int BITS, int GS>
 cudaError_t launch_tma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_tma_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
@@ -38,6 +41,9 @@ extern template cudaError_t launch_tma_bg<4, 128>(const CallArgs&, const Variant
 extern template cudaError_t launch_tma_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_tma_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_tma_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<8, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<8, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_tma_bg<8, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template <int BITS, int GS>
 cudaError_t launch_own_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 extern template cudaError_t launch_own_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
@@ -46,6 +52,9 @@ extern template cudaError_t launch_own_bg<4, 128>(const CallArgs&, const Variant
 extern template cudaError_t launch_own_bg<2, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 extern template cudaError_t launch_own_bg<2, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 extern template cudaError_t launch_own_bg<2, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<8, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<8, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_bg<8, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 template <int BITS, int GS>
 unsigned int read_device_status(int clear);
 extern template unsigned int read_device_status<4, 32>(int);
@@ -54,6 +63,9 @@ extern template unsigned int read_device_status<4, 128>(int);
 extern template unsigned int read_device_status<2, 32>(int);
 extern template unsigned int read_device_status<2, 64>(int);
 extern template unsigned int read_device_status<2, 128>(int);
+extern template unsigned int read_device_status<8, 32>(int);
+extern template unsigned int read_device_status<8, 64>(int);
+extern template unsigned int read_device_status<8, 128>(int);
 
 namespace {
 
@@ -225,7 +237,8 @@ bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
     }
   }
   const int mp = a.M <= 8 ? 8 : 16;
-  const TmaLayout L(pw, gp, a.gs, mp, 2, 1, d.WN, mbw);  // two stages, one tile, every warp a slot  // two stages, one tile
+  // two stages, one tile, every warp a slot; 8-bit codes stage 2g activations per group
+  const TmaLayout L(pw, gp, a.bits == 8 ? 2 * a.gs : a.gs, mp, 2, 1, d.WN, mbw);
   return L.total <= tma_smem_budget(sm_bytes, optin, d.WK);
 }
 
@@ -237,6 +250,9 @@ cudaError_t launch_own(const CallArgs& a, const VariantDesc& d, int splits, cuda
     case 2032: return launch_own_bg<2, 32>(a, d, splits, stream, plan_only);
     case 2064: return launch_own_bg<2, 64>(a, d, splits, stream, plan_only);
     case 2128: return launch_own_bg<2, 128>(a, d, splits, stream, plan_only);
+    case 8032: return launch_own_bg<8, 32>(a, d, splits, stream, plan_only);
+    case 8064: return launch_own_bg<8, 64>(a, d, splits, stream, plan_only);
+    case 8128: return launch_own_bg<8, 128>(a, d, splits, stream, plan_only);
     default: return cudaErrorNotSupported;
   }
 }
@@ -249,6 +265,9 @@ cudaError_t launch_tma(const CallArgs& a, const VariantDesc& d, int splits, cuda
     case 2032: return launch_tma_bg<2, 32>(a, d, splits, stream);
     case 2064: return launch_tma_bg<2, 64>(a, d, splits, stream);
     case 2128: return launch_tma_bg<2, 128>(a, d, splits, stream);
+    case 8032: return launch_tma_bg<8, 32>(a, d, splits, stream);
+    case 8064: return launch_tma_bg<8, 64>(a, d, splits, stream);
+    case 8128: return launch_tma_bg<8, 128>(a, d, splits, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -275,6 +294,9 @@ cudaError_t launch_mma(const CallArgs& a, const VariantDesc& d, int splits, cuda
     case 2032: return launch_mma_bg<2, 32>(a, d, splits, stream);
     case 2064: return launch_mma_bg<2, 64>(a, d, splits, stream);
     case 2128: return launch_mma_bg<2, 128>(a, d, splits, stream);
+    case 8032: return launch_mma_bg<8, 32>(a, d, splits, stream);
+    case 8064: return launch_mma_bg<8, 64>(a, d, splits, stream);
+    case 8128: return launch_mma_bg<8, 128>(a, d, splits, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -311,7 +333,7 @@ size_t qmm_packed_words(int64_t N, int64_t K, int bits) {
 
 int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* splits) {
   if (M < 1 || M > 16 || N < 1 || K < 1) return -1;
-  if ((bits != 2 && bits != 4) || (group_size != 32 && group_size != 64 && group_size != 128)) return -1;
+  if ((bits != 2 && bits != 4 && bits != 8) || (group_size != 32 && group_size != 64 && group_size != 128)) return -1;
   if (K % group_size != 0) return -1;
   CallArgs a = {};
   a.M = M;
@@ -333,6 +355,9 @@ unsigned int qmm_device_status(int clear) {
   v |= read_device_status<2, 32>(clear);
   v |= read_device_status<2, 64>(clear);
   v |= read_device_status<2, 128>(clear);
+  v |= read_device_status<8, 32>(clear);
+  v |= read_device_status<8, 64>(clear);
+  v |= read_device_status<8, 128>(clear);
   return v;
 }
 
@@ -345,7 +370,7 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
                     int N, int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,
                     void* stream) {
   if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
-  if (bits != 2 && bits != 4) return QMM_ERR_UNSUPPORTED;
+  if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
   if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
   if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
   if (variant < -1 || variant >= kNumVariants) return QMM_ERR_UNSUPPORTED;

@@ -37,6 +37,13 @@ __device__ __forceinline__ void ld_stream<4>(uint32_t (&d)[4], const uint32_t* p
   asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "l"(p));
 }
+template <>
+__device__ __forceinline__ void ld_stream<8>(uint32_t (&d)[8], const uint32_t* p) {
+  asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]) : "l"(p));
+  asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(d[4]), "=r"(d[5]), "=r"(d[6]), "=r"(d[7]) : "l"(p + 4));
+}
 
 // Read-only 16-byte load of activations (cached: every CTA of a row tile reads them).
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
@@ -44,6 +51,21 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   asm("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
+}
+
+// Read-only 8-byte load of activations.
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+  uint2 v;
+  asm("ld.global.nc.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+// Both bf16 halves of v times 16, exactly (a power-of-two scaling; finite for
+// |x| < 2^124): one bf16x2 FMA, v * 16 + (-0).
+__device__ __forceinline__ uint32_t bf16x2_times16(uint32_t v) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x41804180u), "r"(0x80008000u));
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -218,7 +240,13 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // address is aligned to the vector size by construction).
 template <int N>
 __device__ __forceinline__ void ld_shared_words(uint32_t (&d)[N], const uint32_t* p) {
-  if constexpr (N == 4) {
+  static_assert(N == 1 || N == 2 || N == 4 || N == 8, "1, 2, 4 or 8 words");
+  if constexpr (N == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint4 w = *reinterpret_cast<const uint4*>(p + 4);
+    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    d[4] = w.x; d[5] = w.y; d[6] = w.z; d[7] = w.w;
+  } else if constexpr (N == 4) {
     const uint4 v = *reinterpret_cast<const uint4*>(p);
     d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
   } else if constexpr (N == 2) {

@@ -8,6 +8,16 @@
 // s * P + (b - 128 s) * sum_k x_k.  That is the group's contribution
 // s * sum x q + b * sum x of the affine dequantization ("MLX quantized_matmul
 // small-M verify kernels", facts "Fix family 1" and "Group-size mechanism").
+//
+// 8-bit codes (E8) run on the same 4-bit machinery.  A word of four 8-bit
+// codes is read as eight 4-bit "virtual" codes: byte c of the word gives the
+// virtual codes lo(q) and hi(q), at virtual positions 2c and 2c + 1.  The
+// activations are staged for the virtual positions as x and 16 x (16 x is
+// exact in bf16), so the MMA sums x (128 + lo) + 16 x (128 + hi) =
+// x (q + 2176) exactly per product, and the fold removes 2176 s sum x instead
+// of 128 s sum x.  With E8 the template's (BITS, GS) are the virtual ones (4,
+// 2g) and the K handed to stage_x is the virtual 2K; the word layout, the
+// group count and the scale/bias layout are those of the 8-bit matrix.
 #pragma once
 
 #include <cstdint>
@@ -17,8 +27,10 @@
 
 namespace qmm {
 
-template <int BITS, int GS, int NB>
+template <int BITS, int GS, int NB, bool E8 = false>
 struct GroupMath {
+  static_assert(!E8 || BITS == 4, "8-bit codes run as virtual 4-bit codes");
+  static constexpr float OFFSET = E8 ? 2176.f : 128.f;  // sum of the unpack offsets per code
   static constexpr int VPW = 32 / BITS;               // codes per 32-bit word
   static constexpr int HALF = VPW / 2;                // code pairs per word
   static constexpr int GW = GS / VPW;                 // words per row and group
@@ -39,6 +51,10 @@ struct GroupMath {
   // thread of [0, nthreads) must call this (warp shuffles).
   __device__ static void stage_x(const uint16_t* X, int K, int M, int g0, int gp, unsigned long long gp_magic,
                                  uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
+    if constexpr (E8) {
+      stage_x_e8(X, K / 2, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads);
+      return;
+    }
     constexpr int CH = GS / VPW;  // tasks per unit (2..16, divides 32)
     constexpr int TQ = VPW / 8;   // 16-byte loads per task
     constexpr int BATCH = 4;
@@ -79,6 +95,51 @@ struct GroupMath {
           uint2* d2 = reinterpret_cast<uint2*>(Xs + m * rsx + j * GS + c * VPW);
 #pragma unroll
           for (int i = 0; i < HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
+        }
+#pragma unroll
+        for (int o = CH / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (u < ntask && c == 0) xsum[j * MP + m] = sum;
+      }
+    }
+  }
+
+  // stage_x for 8-bit codes: a task is one packed word, i.e. 4 activations
+  // x0..x3 of one row (8 bytes, real row length Kr), staged as the 8 virtual
+  // values (x0, 16x0, x1, 16x1, x2, 16x2, x3, 16x3) in unpack order:
+  // (x0, x2), (16x0, 16x2), (x1, x3), (16x1, 16x3).  xsum holds sums of the
+  // real activations.
+  __device__ static void stage_x_e8(const uint16_t* X, int Kr, int M, int g0, int gp, unsigned long long gp_magic,
+                                    uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
+    constexpr int CH = GS / VPW;  // words per row and group (8..32, divides 32)
+    constexpr int GSR = GS / 2;   // real codes per group
+    constexpr int BATCH = 4;
+    static_assert(32 % CH == 0, "a unit's tasks must share a warp");
+    const int ntask = M * gp * CH;
+    for (int base = 0; base < ntask; base += BATCH * nthreads) {
+      uint2 v[BATCH];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * nthreads + tid;
+        const int unit = u / CH;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
+        const int j = unit - m * gp;
+        const uint16_t* src =
+            X + static_cast<int64_t>(m) * Kr + static_cast<int64_t>(g0 + j) * GSR + (u - unit * CH) * 4;
+        v[b] = (u < ntask) ? ld_nc_v2(src) : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * nthreads + tid;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
+        const int j = unit - m * gp;
+        float sum = add_bf16x2_f32(v[b].y, add_bf16x2_f32(v[b].x, 0.f));
+        if (u < ntask) {
+          const uint32_t h0 = bf16x2_times16(v[b].x), h1 = bf16x2_times16(v[b].y);
+          uint2* d2 = reinterpret_cast<uint2*>(Xs + m * rsx + j * GS + c * VPW);
+          d2[0] = make_uint2(prmt_lo(v[b].x, v[b].y), prmt_lo(h0, h1));
+          d2[1] = make_uint2(prmt_hi(v[b].x, v[b].y), prmt_hi(h0, h1));
         }
 #pragma unroll
         for (int o = CH / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
@@ -141,15 +202,15 @@ struct GroupMath {
     }
   }
 
-  // acc += s * P + (b - 128 s) * sum x for one group.  meta_j -> fp16 scale of
+  // acc += s * P + (b - OFFSET s) * sum x for one group.  meta_j -> fp16 scale of
   // (row g, this group); row g + 8 at + 8 * mbw, the biases at + 16 * mbw and
   // + 24 * mbw.  xs_j -> the group's activation sums (MP floats).
   __device__ static void fold(const uint16_t* meta_j, int mbw, const float* xs_j, int t, const float (&tmp)[NB][4],
                               float (&acc)[NB][4]) {
     const float s_lo = __half2float(__ushort_as_half(meta_j[0]));
     const float s_hi = __half2float(__ushort_as_half(meta_j[8 * mbw]));
-    const float b_lo = fmaf(-128.f, s_lo, __half2float(__ushort_as_half(meta_j[16 * mbw])));
-    const float b_hi = fmaf(-128.f, s_hi, __half2float(__ushort_as_half(meta_j[24 * mbw])));
+    const float b_lo = fmaf(-OFFSET, s_lo, __half2float(__ushort_as_half(meta_j[16 * mbw])));
+    const float b_hi = fmaf(-OFFSET, s_hi, __half2float(__ushort_as_half(meta_j[24 * mbw])));
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const float2 xs = *reinterpret_cast<const float2*>(xs_j + 8 * nb + 2 * t);

@@ -17,6 +17,17 @@ struct CallArgs {
   int M, N, K, bits, gs, out_f32;
 };
 
+// 8-bit codes run on the 4-bit kernels as "virtual" 4-bit codes (each byte
+// read as its low and high nibble): the same words, groups and scales, with
+// twice as many codes per row and per group.
+inline CallArgs as_virtual_nibbles(const CallArgs& a) {
+  CallArgs v = a;
+  v.K = 2 * a.K;
+  v.gs = 2 * a.gs;
+  v.bits = 4;
+  return v;
+}
+
 enum Family { kFamilyMma = 0, kFamilySimt = 1, kFamilyTma = 2, kFamilyOwn = 3 };
 
 // One kernel variant: a family and its CTA tiling.

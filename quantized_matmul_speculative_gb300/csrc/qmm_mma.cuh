@@ -103,7 +103,7 @@ struct MmaSmem {
   }
 };
 
-template <int BITS, int GS, int NB, int R, int WN, int WK>
+template <int BITS, int GS, int NB, int R, int WN, int WK, bool E8>
 __global__ void __launch_bounds__(32 * WN * WK, (32 * WN * WK >= 256) ? 2 : 4)
 qmm_mma_kernel(const MmaParams p) {
   using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
@@ -162,32 +162,48 @@ qmm_mma_kernel(const MmaParams p) {
       const int64_t k0 = static_cast<int64_t>(c0 + jl) * GS;
       uint16_t* dst = Xs + m * L.rsx + jl * GS;
       float s = 0.f;
+      if constexpr (E8) {
+        // 8-bit codes as virtual nibbles: word wc holds real codes 4wc..4wc+3
+        // of the group; stage (x0, x2), (16x0, 16x2), (x1, x3), (16x1, 16x3)
+        // and sum the real activations (see qmm_group.cuh).
 #pragma unroll
-      for (int wc = 0; wc < C::GW; ++wc) {
-        uint4 v[C::VPW / 8];
-#pragma unroll
-        for (int q = 0; q < C::VPW / 8; ++q) {
-          if (m < p.M) v[q] = ld_nc_v4(p.X + static_cast<int64_t>(m) * p.K + k0 + wc * C::VPW + 8 * q);
-          else v[q] = make_uint4(0, 0, 0, 0);
+        for (int wc = 0; wc < C::GW; ++wc) {
+          uint2 v = make_uint2(0, 0);
+          if (m < p.M) v = ld_nc_v2(p.X + static_cast<int64_t>(m) * (p.K / 2) + k0 / 2 + 4 * wc);
+          const uint32_t h0 = bf16x2_times16(v.x), h1 = bf16x2_times16(v.y);
+          s += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y);
+          uint2* d2 = reinterpret_cast<uint2*>(dst + wc * C::VPW);
+          d2[0] = make_uint2(prmt_lo(v.x, v.y), prmt_lo(h0, h1));
+          d2[1] = make_uint2(prmt_hi(v.x, v.y), prmt_hi(h0, h1));
         }
-        const uint32_t* e = reinterpret_cast<const uint32_t*>(v);  // VPW/2 words of bf16 pairs
-        uint32_t out[C::HALF];
+      } else {
 #pragma unroll
-        for (int i = 0; i < C::HALF; ++i) {
-          // out[i] = (x[i], x[i + HALF]); x[j] lives in e[j/2], half j%2.
-          const uint32_t a = e[i / 2];
-          const uint32_t b = e[(i + C::HALF) / 2];
-          out[i] = (i % 2 == 0) ? prmt_lo(a, b) : prmt_hi(a, b);
+        for (int wc = 0; wc < C::GW; ++wc) {
+          uint4 v[C::VPW / 8];
+#pragma unroll
+          for (int q = 0; q < C::VPW / 8; ++q) {
+            if (m < p.M) v[q] = ld_nc_v4(p.X + static_cast<int64_t>(m) * p.K + k0 + wc * C::VPW + 8 * q);
+            else v[q] = make_uint4(0, 0, 0, 0);
+          }
+          const uint32_t* e = reinterpret_cast<const uint32_t*>(v);  // VPW/2 words of bf16 pairs
+          uint32_t out[C::HALF];
+#pragma unroll
+          for (int i = 0; i < C::HALF; ++i) {
+            // out[i] = (x[i], x[i + HALF]); x[j] lives in e[j/2], half j%2.
+            const uint32_t a = e[i / 2];
+            const uint32_t b = e[(i + C::HALF) / 2];
+            out[i] = (i % 2 == 0) ? prmt_lo(a, b) : prmt_hi(a, b);
+          }
+#pragma unroll
+          for (int j = 0; j < C::VPW / 2; ++j) s += bf16_lo(e[j]) + bf16_hi(e[j]);
+          uint2* d2 = reinterpret_cast<uint2*>(dst + wc * C::VPW);
+#pragma unroll
+          for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
         }
-#pragma unroll
-        for (int j = 0; j < C::VPW / 2; ++j) s += bf16_lo(e[j]) + bf16_hi(e[j]);
-        uint2* d2 = reinterpret_cast<uint2*>(dst + wc * C::VPW);
-#pragma unroll
-        for (int i = 0; i < C::HALF / 2; ++i) d2[i] = make_uint2(out[2 * i], out[2 * i + 1]);
       }
       xsum[m * p.chunk + jl] = s;
     }
-    // ---- stage (scale, bias - 128 scale) per row and group ----
+    // ---- stage (scale, bias - offset * scale) per row and group; offset 128, or 2176 for 8-bit ----
     for (int u = tid; u < C::NT * nch; u += C::THREADS) {
       const int rl = u / nch;
       const int jl = u - rl * nch;
@@ -197,7 +213,7 @@ qmm_mma_kernel(const MmaParams p) {
         const int64_t idx = static_cast<int64_t>(n) * p.G + c0 + jl;
         const float sc = __half2float(__ushort_as_half(p.S[idx]));
         const float bi = __half2float(__ushort_as_half(p.B[idx]));
-        sb = make_float2(sc, fmaf(-128.f, sc, bi));
+        sb = make_float2(sc, fmaf(E8 ? -2176.f : -128.f, sc, bi));
       }
       meta[rl * p.chunk + jl] = sb;
     }

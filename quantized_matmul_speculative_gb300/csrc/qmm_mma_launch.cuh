@@ -12,7 +12,7 @@ namespace qmm {
 // Shared memory one CTA may use; keeps two 256-thread CTAs resident per SM.
 constexpr int kMmaSmemBudget = 100 * 1024;
 
-template <int BITS, int GS, int NB, int R, int WN, int WK>
+template <int BITS, int GS, int NB, int R, int WN, int WK, bool E8>
 cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) {
   using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
   MmaParams p;
@@ -36,7 +36,7 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   if (p.chunk < 1) p.chunk = 1;
   const int smem = MmaSmem<C>(p.chunk).total;
 
-  auto kern = qmm_mma_kernel<BITS, GS, NB, R, WN, WK>;
+  auto kern = qmm_mma_kernel<BITS, GS, NB, R, WN, WK, E8>;
   static std::mutex mu;
   static int smem_set = 0;
   static bool nonportable_set = false;
@@ -72,11 +72,11 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int BITS, int GS, int NB>
+template <int BITS, int GS, int NB, bool E8>
 cudaError_t launch_mma_tile(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
 #define QMM_TRY_TILE(r, wn, wk)                                                     \
   if (d.R == (r) && d.WN == (wn) && d.WK == (wk))                                   \
-    return launch_mma_impl<BITS, GS, NB, r, wn, wk>(a, splits, stream);
+    return launch_mma_impl<BITS, GS, NB, r, wn, wk, E8>(a, splits, stream);
   QMM_MMA_TILES(QMM_TRY_TILE)
 #undef QMM_TRY_TILE
   return cudaErrorInvalidValue;
@@ -85,8 +85,14 @@ cudaError_t launch_mma_tile(const CallArgs& a, const VariantDesc& d, int splits,
 // Entry for one (bits, group size): picks the activation-tile count from M.
 template <int BITS, int GS>
 cudaError_t launch_mma_bg(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
-  if (a.M <= 8) return launch_mma_tile<BITS, GS, 1>(a, d, splits, stream);
-  return launch_mma_tile<BITS, GS, 2>(a, d, splits, stream);
+  if constexpr (BITS == 8) {
+    const CallArgs v = as_virtual_nibbles(a);
+    if (v.M <= 8) return launch_mma_tile<4, 2 * GS, 1, true>(v, d, splits, stream);
+    return launch_mma_tile<4, 2 * GS, 2, true>(v, d, splits, stream);
+  } else {
+    if (a.M <= 8) return launch_mma_tile<BITS, GS, 1, false>(a, d, splits, stream);
+    return launch_mma_tile<BITS, GS, 2, false>(a, d, splits, stream);
+  }
 }
 
 }  // namespace qmm

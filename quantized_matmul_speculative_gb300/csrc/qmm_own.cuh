@@ -78,11 +78,11 @@ struct OwnLayout {
 
 // With W <= 8 two CTAs must fit an SM (the "2cta" shared-memory budget and
 // the next call's CTAs under PDL), which caps registers at 128 per thread.
-template <int BITS, int GS, int NB, int W, int D>
+template <int BITS, int GS, int NB, int W, int D, bool E8>
 __global__ void __launch_bounds__(32 * W, (W <= 8) ? 2 : 1)
 qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const OwnParams p) {
-  using GM = GroupMath<BITS, GS, NB>;
+  using GM = GroupMath<BITS, GS, NB, E8>;
   constexpr int MP = GM::MP;
   constexpr int GW = GM::GW;
   extern __shared__ __align__(128) unsigned char own_smem[];

@@ -18,7 +18,7 @@ namespace qmm {
 // Plan one call: K-piece, parts per tile, box widths, clusters, receive
 // slots and shared memory.  Returns cudaErrorNotSupported (and launches
 // nothing) when (W, D, csize, CTAs per SM) cannot run the shape.
-template <int BITS, int GS, int NB, int W, int D>
+template <int BITS, int GS, int NB, int W, int D, bool E8>
 cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, OwnParams* p, int* smem, int* budget) {
   constexpr int GW = GroupMath<BITS, GS, NB>::GW;
   constexpr int MP = 8 * NB;
@@ -36,7 +36,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   p->gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p->gp) - 1) / static_cast<unsigned long long>(p->gp);
   p->tiles = (a.N + 15) / 16;
 
-  auto kern = qmm_own_kernel<BITS, GS, NB, W, D>;
+  auto kern = qmm_own_kernel<BITS, GS, NB, W, D, E8>;
   int sm_bytes = 0, optin = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
@@ -114,12 +114,12 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   return found ? cudaSuccess : cudaErrorNotSupported;
 }
 
-template <int BITS, int GS, int NB, int W, int D>
+template <int BITS, int GS, int NB, int W, int D, bool E8>
 cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int wave, cudaStream_t stream,
                             bool plan_only) {
   OwnParams p;
   int smem = 0, budget = 0;
-  const cudaError_t pe = own_plan<BITS, GS, NB, W, D>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
+  const cudaError_t pe = own_plan<BITS, GS, NB, W, D, E8>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
   if (pe != cudaSuccess || plan_only) return pe;
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -169,14 +169,14 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D>, tmap, tmap_s, tmap_b, p);
+  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D, E8>, tmap, tmap_s, tmap_b, p);
 }
 
-template <int BITS, int GS, int NB>
+template <int BITS, int GS, int NB, bool E8>
 cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
 #define QMM_TRY_OWN(w, dd)                 \
   if (d.WN == (w) && d.R == (dd))          \
-    return launch_own_impl<BITS, GS, NB, w, dd>(a, csize, d.WK, d.wave, stream, plan_only);
+    return launch_own_impl<BITS, GS, NB, w, dd, E8>(a, csize, d.WK, d.wave, stream, plan_only);
   QMM_OWN_TILES(QMM_TRY_OWN)
 #undef QMM_TRY_OWN
   return cudaErrorNotSupported;
@@ -184,8 +184,14 @@ cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, 
 
 template <int BITS, int GS>
 cudaError_t launch_own_bg(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
-  if (a.M <= 8) return launch_own_tile<BITS, GS, 1>(a, d, csize, stream, plan_only);
-  return launch_own_tile<BITS, GS, 2>(a, d, csize, stream, plan_only);
+  if constexpr (BITS == 8) {
+    const CallArgs v = as_virtual_nibbles(a);
+    if (v.M <= 8) return launch_own_tile<4, 2 * GS, 1, true>(v, d, csize, stream, plan_only);
+    return launch_own_tile<4, 2 * GS, 2, true>(v, d, csize, stream, plan_only);
+  } else {
+    if (a.M <= 8) return launch_own_tile<BITS, GS, 1, false>(a, d, csize, stream, plan_only);
+    return launch_own_tile<BITS, GS, 2, false>(a, d, csize, stream, plan_only);
+  }
 }
 
 }  // namespace qmm

@@ -62,7 +62,7 @@ inline int max_active_clusters(const void* kern, int threads, int smem, int csiz
   return n;
 }
 
-template <int BITS, int GS, int NB, int W, int S>
+template <int BITS, int GS, int NB, int W, int S, bool E8>
 cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaStream_t stream) {
   using Cfg = TmaCfg<BITS, GS, NB, W, S>;
   TmaParams p;
@@ -83,7 +83,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
-  auto kern = qmm_tma_kernel<BITS, GS, NB, W, S>;
+  auto kern = qmm_tma_kernel<BITS, GS, NB, W, S, E8>;
   // Shared memory: what remains of the SM's budget for ctas_per_sm CTAs goes to
   // the partial tiles of one reduction round.
   int sm_bytes = 0, optin = 0, dev = 0;
@@ -223,11 +223,11 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   return cudaLaunchKernelEx(&cfg, kern, tmap, tmap_s, tmap_b, p);
 }
 
-template <int BITS, int GS, int NB>
+template <int BITS, int GS, int NB, bool E8>
 cudaError_t launch_tma_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream) {
 #define QMM_TRY_TMA(w, s)                                                   \
   if (d.WN == (w) && d.R == (s))                                            \
-    return launch_tma_impl<BITS, GS, NB, w, s>(a, csize, d.WK, stream);
+    return launch_tma_impl<BITS, GS, NB, w, s, E8>(a, csize, d.WK, stream);
   QMM_TMA_TILES(QMM_TRY_TMA)
 #undef QMM_TRY_TMA
   return cudaErrorInvalidValue;
@@ -235,8 +235,14 @@ cudaError_t launch_tma_tile(const CallArgs& a, const VariantDesc& d, int csize, 
 
 template <int BITS, int GS>
 cudaError_t launch_tma_bg(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream) {
-  if (a.M <= 8) return launch_tma_tile<BITS, GS, 1>(a, d, csize, stream);
-  return launch_tma_tile<BITS, GS, 2>(a, d, csize, stream);
+  if constexpr (BITS == 8) {
+    const CallArgs v = as_virtual_nibbles(a);
+    if (v.M <= 8) return launch_tma_tile<4, 2 * GS, 1, true>(v, d, csize, stream);
+    return launch_tma_tile<4, 2 * GS, 2, true>(v, d, csize, stream);
+  } else {
+    if (a.M <= 8) return launch_tma_tile<BITS, GS, 1, false>(a, d, csize, stream);
+    return launch_tma_tile<BITS, GS, 2, false>(a, d, csize, stream);
+  }
 }
 
 }  // namespace qmm

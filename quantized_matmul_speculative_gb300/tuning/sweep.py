@@ -7,6 +7,7 @@ several replays is kept.  Variants are interleaved per shape so that clock
 drift affects all of them alike.  Output: one JSON object per line.
 
     python -m quantized_matmul_speculative_gb300.tuning.sweep --out sweep.jsonl [--quick]
+        [--only-n N ...] [--only-bits B]
 """
 from __future__ import annotations
 
@@ -90,6 +91,7 @@ def main():
     ap.add_argument("--quick", action="store_true")
     ap.add_argument("--only-n", type=int, default=None, help="sweep only shapes with this N (repeatable)",
                     action="append")
+    ap.add_argument("--only-bits", type=int, default=None, help="sweep only shapes of this code width")
     args = ap.parse_args()
     import torch
 
@@ -102,6 +104,8 @@ def main():
     out = open(args.out, "w")
     for N, K, bits, gs, ms in shapes(args.quick):
         if args.only_n and N not in args.only_n:
+            continue
+        if args.only_bits and bits != args.only_bits:
             continue
         p = synth.make_problem(1, N, K, bits, gs)
         call_b = workloads.call_bytes(N, K, bits, gs)

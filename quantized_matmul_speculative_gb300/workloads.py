@@ -91,7 +91,15 @@ VERIFY_STEP = Workload(
     note="36 layers x 4 projections of a 4096-hidden dense stack, back to back on one stream",
 )
 
-ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP)
+INT8_AFFINE = Workload(
+    name="int8_affine_8b_g64",
+    shapes=(Shape("square", 5120, 5120), Shape("gate_up", 15360, 3840)),
+    bits=8, group_size=64, ms=tuple(range(1, 17)), seed_base=6000,
+    note="8-bit affine g64: the 5120x5120 layer and a 15360x3840 gate/up projection (the shape of the "
+         "pages' int8 qmv_wide measurement; its 60 groups per row take the mma family)",
+)
+
+ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP, INT8_AFFINE)
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -71,7 +71,7 @@ def test_validation_before_launch(lib):
         return call(*a)
 
     assert rc(M=17) == 2 and rc(M=-1) == 2 and rc(N=-3) == 2
-    assert rc(bits=3) == 3 and rc(bits=8) == 3 and rc(gs=48) == 3 and rc(gs=256) == 3
+    assert rc(bits=3) == 3 and rc(bits=16) == 3 and rc(gs=48) == 3 and rc(gs=256) == 3
     assert rc(K=96) == 2
     assert rc(out=2) == 3 and rc(variant=lib.qmm_num_variants()) == 3 and rc(splits=0) == 3 and rc(splits=17) == 3
     assert rc(X=None) == 1 and rc(Wq=None) == 1 and rc(Y=None) == 1

@@ -13,7 +13,7 @@ from quantized_matmul_speculative_gb300 import binding, synth, workloads
 
 pytestmark = pytest.mark.gpu
 
-BITS_GS = [(4, 32), (4, 64), (4, 128), (2, 32), (2, 64), (2, 128)]
+BITS_GS = [(4, 32), (4, 64), (4, 128), (2, 32), (2, 64), (2, 128), (8, 32), (8, 64), (8, 128)]
 
 
 @pytest.fixture(scope="module")
@@ -70,7 +70,7 @@ def test_small_shapes_all_m(torch_cuda, bits, gs):
 
 
 @pytest.mark.parametrize("N", [1, 7, 15, 17, 129])
-@pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (4, 128)])
+@pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (4, 128), (8, 64)])
 def test_ragged_n_and_one_group(torch_cuda, N, bits, gs):
     torch = torch_cuda
     for K in (gs, 2 * gs, 8 * gs):
@@ -153,6 +153,21 @@ def test_verify_step_shapes_sampled(torch_cuda, shape_index):
         ms, ns = sample_positions(M, sh.N, 96, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
         assert_within(y[ms, ns], y_ref, a_ref, f"{sh.name} M={M}")
+
+
+@pytest.mark.parametrize("shape_index", range(2))
+def test_int8_affine_sampled(torch_cuda, shape_index):
+    """8-bit affine g64, M = 1..16 through the dispatcher: 5120x5120 and the
+    15360x3840 gate/up shape (60 groups per row: the mma family)."""
+    w = workloads.INT8_AFFINE
+    sh = w.shapes[shape_index]
+    p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    for M in w.ms:
+        y = to_f64(dp.run(M))
+        ms, ns = sample_positions(M, sh.N, 128, seed=M)
+        y_ref, a_ref = ref.sampled(M, ms, ns)
+        assert_within(y[ms, ns], y_ref, a_ref, f"int8 {sh.name} M={M}")
 
 
 # ------------------------------------------------------------- properties
