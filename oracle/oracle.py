@@ -65,8 +65,9 @@ class OracleLib:
         lib.oracle_qmm_sampled.argtypes = [vp, vp, vp, vp, i64, i64, i64, c_int, i64, vp, vp, i64, vp, vp]
         lib.oracle_dequant.argtypes = [vp, vp, vp, i64, i64, c_int, i64, vp]
         lib.oracle_qmm_residual.argtypes = [vp, vp, vp, vp, vp, c_int, i64, i64, i64, c_int, i64, vp, vp]
+        lib.oracle_gather_qmm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, i64, vp, vp]
         for name in ("oracle_pack", "oracle_unpack", "oracle_qmm", "oracle_qmm_sampled", "oracle_dequant",
-                     "oracle_qmm_residual"):
+                     "oracle_qmm_residual", "oracle_gather_qmm"):
             getattr(lib, name).restype = c_int
         self.lib = lib
 
@@ -132,6 +133,26 @@ class OracleLib:
                                           m, n, k, bits, group_size, _ptr(y), _ptr(a))
         if rc:
             raise OracleError(f"oracle_qmm_residual rc={rc}")
+        return y, a
+
+    def gather_qmm(self, x_bits, wq, s_bits, b_bits, lhs, rhs, bits: int, group_size: int):
+        """Return (Y, A) [P, N] of Y[i] = X[lhs[i]] . W[rhs[i]]^T in fp64.
+        ``wq``: [E, N, K*bits/32]; ``s_bits``, ``b_bits``: [E, N, K/g]."""
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        wq = np.ascontiguousarray(wq, dtype=np.uint32)
+        s = np.ascontiguousarray(s_bits, dtype=np.uint16)
+        b = np.ascontiguousarray(b_bits, dtype=np.uint16)
+        lhs = np.ascontiguousarray(lhs, dtype=np.int32)
+        rhs = np.ascontiguousarray(rhs, dtype=np.int32)
+        t, k = x.shape
+        e, n = wq.shape[0], wq.shape[1]
+        p = len(lhs)
+        y = np.empty((p, n), dtype=np.float64)
+        a = np.empty((p, n), dtype=np.float64)
+        rc = self.lib.oracle_gather_qmm(_ptr(x), _ptr(wq), _ptr(s), _ptr(b), _ptr(lhs), _ptr(rhs), p, t, e, n, k,
+                                        bits, group_size, _ptr(y), _ptr(a))
+        if rc:
+            raise OracleError(f"oracle_gather_qmm rc={rc}")
         return y, a
 
     def qmm_sampled(self, x_bits, wq, s_bits, b_bits, bits: int, group_size: int, ms, ns):

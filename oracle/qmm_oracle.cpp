@@ -39,6 +39,12 @@
 //      - "metal : few-row MMA mat-mul and batched copies for speculative
 //        decoding" (llama.cpp PR #29869), Overview: the fusion-table entry
 //        MUL_MAT + ADD.
+//  * Gathered product (oracle_gather_qmm), the MoE form of the op at verify
+//    widths: entry i of a list pairs activation row lhs[i] with expert matrix
+//    rhs[i] of a stack W[E][N][K]: Y[i, n] = sum_k x[lhs[i], k] * w[rhs[i], n, k].
+//      - "MLX quantized_matmul small-M verify kernels", the open question on
+//        "dense and MoE (gather_qmm) verify" and the "expert-union cost per
+//        verify row".
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
 // shapes (2-, 4- and 8-bit), closed forms (all-zero codes, one-hot X, X = 1,
@@ -196,6 +202,38 @@ int oracle_qmm_residual(const uint16_t* X, const uint32_t* Wq, const uint16_t* S
                               : bf16_bits_to_double(static_cast<const uint16_t*>(R)[i]);
     Y[i] = r + Y[i];
     if (A) A[i] = std::fabs(r) + A[i];
+  }
+  return 0;
+}
+
+// Gathered product.  W is a stack of E matrices: Wq [E][N][K*bits/32], S, B
+// [E][N][K/g].  lhs[i] in 0..T-1 selects the activation row, rhs[i] in 0..E-1
+// the matrix.  Y[P,N], A[P,N] as in oracle_qmm.  Returns 2 for an index out
+// of range.
+int oracle_gather_qmm(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, const uint16_t* B,
+                      const int32_t* lhs, const int32_t* rhs, int64_t P, int64_t T, int64_t E, int64_t N,
+                      int64_t K, int bits, int64_t g, double* Y, double* A) {
+  const int rc = check_shape(T, N, K, bits, g);
+  if (rc) return rc;
+  if (P < 0 || E < 0) return 2;
+  const int64_t words_per_matrix = N * (K * bits / 32);
+  const int64_t groups_per_matrix = N * (K / g);
+  for (int64_t i = 0; i < P; ++i) {
+    const int64_t t = lhs[i], e = rhs[i];
+    if (t < 0 || t >= T || e < 0 || e >= E) return 2;
+    const uint32_t* We = Wq + e * words_per_matrix;
+    const uint16_t* Se = S + e * groups_per_matrix;
+    const uint16_t* Be = B + e * groups_per_matrix;
+    for (int64_t n = 0; n < N; ++n) {
+      double y = 0.0, a = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = bf16_bits_to_double(X[t * K + k]) * weight_at(We, Se, Be, K, bits, g, n, k);
+        y += p;
+        a += std::fabs(p);
+      }
+      Y[i * N + n] = y;
+      if (A) A[i * N + n] = a;
+    }
   }
   return 0;
 }

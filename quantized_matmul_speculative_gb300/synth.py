@@ -14,7 +14,12 @@ Recipe (one numpy PCG64 stream per tensor, keyed by ``(seed, stream)``):
 * ``X = bf16(N(0,1))`` drawn for 16 rows; an M-row problem uses the first M
   rows, so every M of a sweep sees the same leading rows;
 * a residual ``R = N(0,1)`` per output element, stored as bf16 bit patterns
-  or as float32 (the output dtype it is added in).
+  or as float32 (the output dtype it is added in);
+* mixture-of-experts stacks: E matrices drawn as above (codes, scales and
+  biases of the whole stack from one stream each), and a routing in which
+  each of T tokens picks k distinct experts with probabilities
+  ``softmax(1.5 * z)``, ``z ~ N(0,1)`` per expert (a few popular experts, so
+  the tokens of a verify step share some of theirs).
 
 Rounding to fp16 is numpy's (round to nearest even); rounding binary32 to
 bf16 is round to nearest even on the bit pattern.
@@ -31,6 +36,7 @@ STREAM_CODES = 0
 STREAM_SCALES = 1
 STREAM_X = 2
 STREAM_RESIDUAL = 3
+STREAM_ROUTING = 4
 
 
 def rng_for(seed: int, stream: int) -> np.random.Generator:
@@ -96,6 +102,51 @@ def make_residual(seed: int, M: int, N: int, f32: bool = False) -> np.ndarray:
     """R[M, N]: bf16 bit patterns (uint16), or float32 values if ``f32``."""
     z = rng_for(seed, STREAM_RESIDUAL).standard_normal(size=(M, N), dtype=np.float32)
     return z if f32 else f32_to_bf16_bits(z)
+
+
+@dataclass
+class MoeProblem:
+    """A stack of E expert matrices and a routing of T tokens to k experts each.
+
+    ``q``: uint8 [E, N, K]; ``scales``/``biases``: fp16 bits [E, N, K/g];
+    ``x``: bf16 bits [16, K]; ``experts``: int32 [T, k] (distinct per token).
+    The gathered list is entry i = t * k + j: lhs[i] = t, rhs[i] = experts[t, j].
+    """
+
+    E: int
+    N: int
+    K: int
+    bits: int
+    group_size: int
+    q: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    x: np.ndarray
+    experts: np.ndarray
+    seed: int
+
+    def lists(self):
+        T, k = self.experts.shape
+        lhs = np.repeat(np.arange(T, dtype=np.int32), k)
+        return lhs, np.ascontiguousarray(self.experts.reshape(-1), dtype=np.int32)
+
+
+def make_routing(seed: int, T: int, k: int, E: int) -> np.ndarray:
+    rng = rng_for(seed, STREAM_ROUTING)
+    z = rng.standard_normal(size=E)
+    p = np.exp(1.5 * (z - z.max()))
+    p /= p.sum()
+    return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+
+
+def make_moe(seed: int, E: int, N: int, K: int, bits: int, group_size: int, T: int, k: int) -> MoeProblem:
+    if K % group_size:
+        raise ValueError("K must be a multiple of group_size")
+    q = make_codes(seed, E * N, K, bits).reshape(E, N, K)
+    scales, biases = make_scales_biases(seed, E * N, K // group_size, bits)
+    return MoeProblem(E=E, N=N, K=K, bits=bits, group_size=group_size, q=q,
+                      scales=scales.reshape(E, N, -1), biases=biases.reshape(E, N, -1), x=make_x(seed, K),
+                      experts=make_routing(seed, T, k, E), seed=seed)
 
 
 def make_problem(seed: int, N: int, K: int, bits: int, group_size: int, rows: int = MAX_ROWS) -> Problem:

@@ -246,6 +246,43 @@ def pin_residual(lib):
     assert np.array_equal(yz, yp) and np.array_equal(az, ap), "R = 0 must give the plain product"
 
 
+def pin_gather(lib):
+    """Y[i] = X[lhs[i]] . W[rhs[i]]^T: exact rational sums on a tiny stack with a
+    repeated entry; relabelling the experts leaves Y unchanged; an index out of
+    range is an error."""
+    E, N, K, bits, g, T = 3, 4, 64, 4, 32, 3
+    mp = synth.make_moe(997, E, N, K, bits, g, T, 2)
+    wq = np.stack([lib.pack(mp.q[e], bits) for e in range(E)])
+    lhs = np.array([0, 2, 1, 2, 0, 1], dtype=np.int32)
+    rhs = np.array([2, 0, 1, 2, 1, 2], dtype=np.int32)
+    y, a = lib.gather_qmm(mp.x[:T], wq, mp.scales, mp.biases, lhs, rhs, bits, g)
+    s = [[[frac_half(v) for v in row] for row in mp.scales[e]] for e in range(E)]
+    b = [[[frac_half(v) for v in row] for row in mp.biases[e]] for e in range(E)]
+    x = [[frac_bf16(v) for v in row] for row in mp.x[:T]]
+    for i in range(len(lhs)):
+        t, e = int(lhs[i]), int(rhs[i])
+        for n in range(N):
+            acc, mag = Fraction(0), Fraction(0)
+            for k in range(K):
+                term = x[t][k] * (s[e][n][k // g] * int(mp.q[e, n, k]) + b[e][n][k // g])
+                acc += term
+                mag += abs(term)
+            assert abs(Fraction(float(y[i, n])) - acc) <= Fraction(1, 10**12) * mag, f"gather y[{i},{n}]"
+            assert abs(Fraction(float(a[i, n])) - mag) <= Fraction(1, 10**12) * mag, f"gather a[{i},{n}]"
+    perm = np.array([2, 0, 1])  # new expert j is old expert perm[j]
+    inv = np.argsort(perm).astype(np.int32)
+    y2, _ = lib.gather_qmm(mp.x[:T], wq[perm], mp.scales[perm], mp.biases[perm], lhs, inv[rhs], bits, g)
+    assert np.array_equal(y2, y), "relabelled experts"
+    bad = rhs.copy()
+    bad[3] = E
+    try:
+        lib.gather_qmm(mp.x[:T], wq, mp.scales, mp.biases, lhs, bad, bits, g)
+    except Exception:
+        pass
+    else:
+        raise AssertionError("an expert index out of range must be an error")
+
+
 def pin_sampled(lib):
     M, N, K, bits, g = 4, 11, 192, 2, 64
     p = synth.make_problem(995, N, K, bits, g, rows=M)
@@ -260,5 +297,5 @@ def pin_sampled(lib):
 # Pins that run fast enough for the mutation test (the exhaustive decoder pin
 # is run once against the real oracle only).
 FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
-             pin_invariants, pin_residual, pin_sampled)
+             pin_invariants, pin_residual, pin_gather, pin_sampled)
 ALL_PINS = (pin_decoders,) + FAST_PINS

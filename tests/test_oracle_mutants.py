@@ -20,6 +20,10 @@ MUTANTS = [
     ("bf16_frac", "128 + frac), expo - 134", "127 + frac), expo - 134"),
     ("residual_sign", "Y[i] = r + Y[i];", "Y[i] = Y[i] - r;"),
     ("residual_dropped_from_scale", "A[i] = std::fabs(r) + A[i];", "A[i] = A[i];"),
+    ("gather_rhs_ignored", "const int64_t t = lhs[i], e = rhs[i];", "const int64_t t = lhs[i], e = 0;"),
+    ("gather_lhs_ignored", "const int64_t t = lhs[i], e = rhs[i];", "const int64_t t = i % T, e = rhs[i];"),
+    ("gather_expert_stride", "const int64_t words_per_matrix = N * (K * bits / 32);",
+     "const int64_t words_per_matrix = K * bits / 32;"),
 ]
 
 
