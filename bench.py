@@ -357,6 +357,48 @@ def residual_report(torch, dev, stream, ms=(1, 8, 16)):
     return {"op": "fused residual add Y = R + X W^T, 5120x5120 4-bit g64, bf16", "per_m": res}
 
 
+def moe_report(torch, dev, stream, peak):
+    """The gathered (MoE) form on a 128-expert top-8 gate+up stack at T = 1, 2,
+    4, 8 verify tokens: us per call, and GB/s over the bytes of the experts in
+    the routing's union (each streamed once per call).  Calls rotate over
+    copies of the whole stack so that every call reads cold HBM."""
+    from quantized_matmul_speculative_gb300 import binding
+
+    w = workloads.MOE_GATE_UP
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = stream.cuda_stream
+    mp = synth.make_moe(w.seed, w.E, w.N, w.K, w.bits, w.group_size, max(w.ts), w.k)
+    wq = torch.from_numpy(binding.pack(mp.q.reshape(w.E * w.N, w.K), w.bits).view(np.int32)).to(dev)
+    sc = torch.from_numpy(mp.scales.view(np.float16)).to(dev)
+    bi = torch.from_numpy(mp.biases.view(np.float16)).to(dev)
+    smallest = workloads.moe_union_bytes(w, mp.experts[:min(w.ts)])
+    ncopy = max(2, int(np.ceil(4 * l2 / smallest)) + 1)
+    copies = [(wq, sc, bi)] + [(wq.clone(), sc.clone(), bi.clone()) for _ in range(ncopy - 1)]
+    x = torch.from_numpy(mp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((max(w.ts) * w.k, w.N), dtype=torch.bfloat16, device=dev)
+    res = []
+    for T in w.ts:
+        experts = mp.experts[:T]
+        lhs = torch.from_numpy(np.repeat(np.arange(T, dtype=np.int32), w.k)).to(dev)
+        rhs = torch.from_numpy(np.ascontiguousarray(experts.reshape(-1))).to(dev)
+        ub = workloads.moe_union_bytes(w, experts)
+
+        def capture(i, T=T, lhs=lhs, rhs=rhs):
+            wq_d, s_d, b_d = copies[i % ncopy]
+            binding.gather_small_m_ptr(x.data_ptr(), wq_d.data_ptr(), s_d.data_ptr(), b_d.data_ptr(), lhs.data_ptr(),
+                                       rhs.data_ptr(), T * w.k, T, w.E, w.N, w.K, w.bits, w.group_size, y.data_ptr(),
+                                       binding.OUT_BF16, -1, -1, handle)
+        us = graph_us_per_call(torch, stream, capture, 32)
+        gbs = ub / (us * 1e-6) / 1e9
+        res.append({"T": T, "entries": T * w.k, "experts_in_union": int(len(np.unique(experts))),
+                    "union_bytes": ub, "us_per_call": round(us, 3), "union_gbs": round(gbs, 1),
+                    "frac_hbm": round(gbs / peak, 4)})
+    del copies, wq, sc, bi
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "per_t": res,
+            "note": "gathered form on the mma family; bytes = distinct experts of the routing x expert bytes"}
+
+
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):
     """bf16 dense torch.matmul (cuBLAS) on the 5120x5120 layer, for scale only:
     the dense bf16 weights are 4x the bytes of the 4-bit ones."""
@@ -557,6 +599,7 @@ def run_ours(args, world, rank, local):
         extra["verify_step"] = verify_step_report(torch, dev, stream, peak)
         extra["controls"] = dense_control(torch, dev, stream)
         extra["residual"] = residual_report(torch, dev, stream)
+        extra["moe"] = moe_report(torch, dev, stream, peak)
     kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
                       "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
 

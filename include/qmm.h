@@ -100,6 +100,27 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
                                 const void* R, int M, int N, int K, int bits, int group_size, void* Y,
                                 int out_dtype, int variant, int splits, void* stream);
 
+/* Gathered form for mixture-of-experts layers at verify widths:
+ *     Y[i, :] = X[lhs[i], :] . dequant(W[rhs[i]])^T,   i = 0 .. P-1
+ * X bf16 [T, K]; Wq [E][N][K*bits/32], scales and biases fp16 [E][N][K/g]: a
+ * stack of E matrices back to back, each in the layout above; lhs, rhs int32
+ * [P] device arrays, 0 <= lhs[i] < T, 0 <= rhs[i] < E; Y [P, N].  Each expert
+ * in the union of rhs is streamed once per call for all the entries that name
+ * it.  Entries per expert: at most 8 if T <= 8 or P <= 8, else at most 16
+ * (true when the k experts of each token are distinct).  P <= 256.
+ * Source: "MLX quantized_matmul small-M verify kernels", the open question on
+ * "dense and MoE (gather_qmm) verify" and the "expert-union cost per verify
+ * row".
+ * Runs on the "mma" variants (variant = -1: the first; a TMA variant returns
+ * QMM_ERR_UNSUPPORTED); splits as in qmm_small_m_ex.  The index lists are read
+ * on the device: an index out of range, or too many entries for one expert,
+ * leaves the affected rows of Y unwritten and sets bit 3 of
+ * qmm_device_status().  K == 0 fills Y with zeros; P == 0 or N == 0 launches
+ * nothing.                                                                     */
+qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                              const int32_t* lhs, const int32_t* rhs, int P, int T, int E, int N, int K, int bits,
+                              int group_size, void* Y, int out_dtype, int variant, int splits, void* stream);
+
 /* Number of uint32 words of a packed [N, K] matrix: N * K * bits / 32
  * (0 if bits is unsupported or K*bits is not a multiple of 32).                 */
 size_t qmm_packed_words(int64_t N, int64_t K, int bits);
@@ -136,7 +157,8 @@ int qmm_last_cuda_error(void);                 /* cudaError_t of the last failur
 
 /* Device status word of the kernels, OR-ed over all kernel units: bit 0 = a
  * consumer gave up waiting for a weight tile, bit 1 = the producer gave up
- * waiting for a free stage, bit 2 = copies still in flight at exit gave up.
+ * waiting for a free stage, bit 2 = copies still in flight at exit gave up,
+ * bit 3 = a gathered call had an invalid index list (see qmm_gather_small_m).
  * Every wait is bounded (about 2 s), so a fault shows up here instead of as a
  * hang.  Synchronizes with the device; clears the word when `clear` != 0.
  * 0xFFFFFFFF if the word could not be read.                                    */

@@ -33,6 +33,8 @@ SIGNATURES = {
     "qmm_small_m_ex": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "qmm_small_m_residual": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32,
                                     _vp]),
+    "qmm_gather_small_m": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
+                                  _i32, _i32, _i32, _vp]),
     "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
     "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
     "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
@@ -155,6 +157,50 @@ def small_m_residual_ptr(x_ptr: int, wq_ptr: int, s_ptr: int, b_ptr: int, r_ptr:
     rc = lib().qmm_small_m_residual(x_ptr, wq_ptr, s_ptr, b_ptr, r_ptr, M, N, K, bits, group_size, y_ptr,
                                     out_dtype, variant, splits, stream)
     _check(rc, "qmm_small_m_residual")
+
+
+def gather_small_m_ptr(x_ptr: int, wq_ptr: int, s_ptr: int, b_ptr: int, lhs_ptr: int, rhs_ptr: int, P: int, T: int,
+                       E: int, N: int, K: int, bits: int, group_size: int, y_ptr: int, out_dtype: int = OUT_BF16,
+                       variant: int = -1, splits: int = -1, stream: int = 0) -> None:
+    """Raw-pointer call of qmm_gather_small_m: Y[i] = X[lhs[i]] . W[rhs[i]]^T."""
+    rc = lib().qmm_gather_small_m(x_ptr, wq_ptr, s_ptr, b_ptr, lhs_ptr, rhs_ptr, P, T, E, N, K, bits, group_size,
+                                  y_ptr, out_dtype, variant, splits, stream)
+    _check(rc, "qmm_gather_small_m")
+
+
+def gather_small_m(x, wq, scales, biases, lhs, rhs, bits: int, group_size: int, out=None, out_dtype=None,
+                   variant: int = -1, splits: int = -1, stream=None):
+    """Y[i] = X[lhs[i]] . dequant(W[rhs[i]])^T over an expert stack.
+
+    ``x``: bf16 [T, K]; ``wq``: int32 [E, N, K*bits/32]; ``scales``, ``biases``:
+    fp16 [E, N, K/group_size]; ``lhs``, ``rhs``: int32 [P]; all contiguous CUDA
+    tensors.  Returns ``out`` [P, N] (bf16 or fp32).
+    """
+    import torch
+
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    for name, t in (("x", x), ("wq", wq), ("scales", scales), ("biases", biases), ("lhs", lhs), ("rhs", rhs)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if lhs.dtype != torch.int32 or rhs.dtype != torch.int32 or lhs.shape != rhs.shape or lhs.dim() != 1:
+        raise TypeError("lhs and rhs must be int32 vectors of one length")
+    T, K = x.shape
+    E, N = wq.shape[0], wq.shape[1]
+    if wq.shape[2] * 32 != K * bits or tuple(scales.shape) != (E, N, K // group_size):
+        raise ValueError("wq / scales shapes do not match K, bits and group_size")
+    P = lhs.shape[0]
+    if out is None:
+        out = torch.empty((P, N), dtype=out_dtype, device=x.device)
+    elif tuple(out.shape) != (P, N) or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [P, N] tensor of out_dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    gather_small_m_ptr(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), biases.data_ptr(), lhs.data_ptr(),
+                       rhs.data_ptr(), P, T, E, N, K, bits, group_size, out.data_ptr(),
+                       OUT_F32 if out_dtype == torch.float32 else OUT_BF16, variant, splits, handle)
+    return out
 
 
 def small_m(x, wq, scales, biases, bits: int, group_size: int, out=None, out_dtype=None,

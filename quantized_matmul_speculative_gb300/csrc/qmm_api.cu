@@ -498,6 +498,75 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
   return run_call(X, Wq, scales, biases, R, M, N, K, bits, group_size, Y, out_dtype, variant, splits, stream);
 }
 
+qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
+                              const int32_t* lhs, const int32_t* rhs, int P, int T, int E, int N, int K, int bits,
+                              int group_size, void* Y, int out_dtype, int variant, int splits, void* stream) {
+  constexpr int kMaxGatherEntries = 256;  // one entry per thread of the index scan
+  if (P < 0 || P > kMaxGatherEntries || T < 0 || E < 0 || N < 0 || K < 0) return QMM_ERR_SHAPE;
+  if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
+  if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
+  if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
+  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family != kFamilyMma))
+    return QMM_ERR_UNSUPPORTED;
+  if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
+  if (K % group_size != 0) return QMM_ERR_SHAPE;
+  if (P == 0 || N == 0) return QMM_OK;
+  const size_t esize = out_dtype == QMM_OUT_F32 ? 4 : 2;
+  if (Y == nullptr) return QMM_ERR_NULL;
+  if (!aligned(Y, esize)) return QMM_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(P) * static_cast<size_t>(N) * esize, st);
+    return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+  }
+  if (T < 1 || E < 1) return QMM_ERR_SHAPE;
+  if (X == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr || lhs == nullptr || rhs == nullptr)
+    return QMM_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(Wq, 16) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(lhs, 4) ||
+      !aligned(rhs, 4))
+    return QMM_ERR_ALIGN;
+
+  CallArgs a;
+  a.X = static_cast<const uint16_t*>(X);
+  a.Wq = Wq;
+  a.S = static_cast<const uint16_t*>(scales);
+  a.B = static_cast<const uint16_t*>(biases);
+  a.Y = Y;
+  a.R = nullptr;
+  a.M = (T <= 8 || P <= 8) ? 8 : 16;  // entries one expert may take: the activation tile
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.gs = group_size;
+  a.out_f32 = out_dtype == QMM_OUT_F32;
+  a.lhs = lhs;
+  a.rhs = rhs;
+  a.P = P;
+  a.T = T;
+  a.E = E;
+  const int fv = forced_variant();
+  if (variant < 0 && fv >= 0 && kVariants[fv].family == kFamilyMma) variant = fv;
+  const VariantDesc& d = kVariants[variant < 0 ? 0 : variant];
+  int s = splits;
+  if (s < 0) {
+    // about two CTAs per SM over the tiles of every possible expert of the union
+    const int slots = E < P ? E : P;
+    const int rows = variant_rows_per_cta(d);
+    const int64_t ctas = static_cast<int64_t>((N + rows - 1) / rows) * slots;
+    const int64_t target = 2 * static_cast<int64_t>(device_sm_count());
+    s = static_cast<int>((target + ctas - 1) / ctas);
+    int cap = (K / group_size) / d.WK;
+    if (cap > 8) cap = 8;
+    if (s > cap) s = cap;
+    if (s < 1) s = 1;
+  }
+  if (env_flag("QMM_LOG"))
+    std::fprintf(stderr, "qmm gather: P=%d T=%d E=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", P, T, E, N, K, bits,
+                 group_size, d.name, s);
+  const cudaError_t e = launch_mma(a, d, s, st);
+  return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
+
 qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N, int K,
                        int bits, int group_size, void* Y, void* stream) {
   return qmm_small_m_ex(X, Wq, scales, biases, M, N, K, bits, group_size, Y, QMM_OUT_BF16, -1, -1, stream);

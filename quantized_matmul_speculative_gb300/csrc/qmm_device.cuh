@@ -157,6 +157,8 @@ static __device__ unsigned int g_qmm_status = 0;
 constexpr unsigned int kStatusTimeoutFull = 1u;   // a consumer gave up waiting for a tile
 constexpr unsigned int kStatusTimeoutEmpty = 2u;  // the producer gave up waiting for a free stage
 constexpr unsigned int kStatusTimeoutDrain = 4u;  // copies still in flight at exit gave up
+constexpr unsigned int kStatusBadGather = 8u;     // a gathered call had an index out of range, or more
+                                                  // entries for one expert than its activation tile holds
 // Time after which a wait is abandoned (ns).  Far above any legitimate wait.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

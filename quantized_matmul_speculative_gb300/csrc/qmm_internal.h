@@ -15,6 +15,13 @@ struct CallArgs {
   void* Y;             // bf16 or fp32 [M, N]
   const void* R;       // residual, Y's dtype [M, N], added in the store; may be Y; null: none
   int M, N, K, bits, gs, out_f32;
+  // Gathered form (null rhs: a plain call): entry i of P multiplies activation
+  // row lhs[i] of X [T, K] by matrix rhs[i] of the stack Wq/S/B [E][N][...]
+  // into row i of Y [P, N]; M is then the largest row count one expert can
+  // take (8 or 16).
+  const int32_t* lhs = nullptr;
+  const int32_t* rhs = nullptr;
+  int P = 0, T = 0, E = 0;
 };
 
 // 8-bit codes run on the 4-bit kernels as "virtual" 4-bit codes (each byte

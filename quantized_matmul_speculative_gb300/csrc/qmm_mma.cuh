@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include "qmm_device.cuh"
+#include "qmm_gather.cuh"
 #include "qmm_internal.h"
 
 namespace qmm {
@@ -62,6 +63,14 @@ struct MmaParams {
   int gpc;      // groups per CTA K-range
   int chunk;    // groups staged in shared memory at a time
   int out_f32;
+  // Gathered form (rhs null: a plain call): entry i pairs X row lhs[i] with
+  // matrix rhs[i] of the stack; CTA x = slot * tiles + row tile (qmm_gather.cuh).
+  const int32_t* lhs;
+  const int32_t* rhs;
+  int P, T, E;
+  int tiles;           // CTA row tiles per matrix
+  int64_t w_stride;    // packed words per matrix of the stack
+  int64_t m_stride;    // scales (and biases) per matrix of the stack
 };
 
 template <int BITS, int GS, int NB, int R, int WN, int WK>
@@ -123,7 +132,29 @@ qmm_mma_kernel(const MmaParams p) {
   const int g = lane >> 2;
   const int t = lane & 3;
 
-  const int n0 = blockIdx.x * C::NT;
+  // Gathered form: this CTA's expert, its entries' activation rows and output
+  // rows; a CTA whose slot is past the union exits (so does its whole
+  // cluster, which shares blockIdx.x).
+  __shared__ int g_row[C::MP], g_out[C::MP];
+  int M = p.M;
+  int tile = blockIdx.x;
+  const uint32_t* Wq = p.Wq;
+  const uint16_t* Sg = p.S;
+  const uint16_t* Bg = p.B;
+  const bool gathered = p.rhs != nullptr;
+  if (gathered) {
+    tile = blockIdx.x % p.tiles;
+    int e = 0;
+    if (!gather_setup<C::THREADS>(p.lhs, p.rhs, p.P, p.T, p.E, blockIdx.x / p.tiles, C::MP, g_row, g_out, &e, &M))
+      return;
+    Wq += e * p.w_stride;
+    Sg += e * p.m_stride;
+    Bg += e * p.m_stride;
+  }
+  auto xrow = [&](int m) { return static_cast<int64_t>(gathered ? g_row[m] : m); };
+  auto yrow = [&](int m) { return static_cast<int64_t>(gathered ? g_out[m] : m); };
+
+  const int n0 = tile * C::NT;
   const int split = blockIdx.y;
   const int cta_g0 = split * p.gpc;
   int cta_g1 = cta_g0 + p.gpc;
@@ -140,7 +171,7 @@ qmm_mma_kernel(const MmaParams p) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int n = n0 + wn * 16 * R + 16 * r + 8 * h + g;
-      wrow[r][h] = (n < p.N) ? p.Wq + static_cast<int64_t>(n) * row_words + wofs : nullptr;
+      wrow[r][h] = (n < p.N) ? Wq + static_cast<int64_t>(n) * row_words + wofs : nullptr;
     }
 
   float acc[R][NB][4];
@@ -169,7 +200,7 @@ qmm_mma_kernel(const MmaParams p) {
 #pragma unroll
         for (int wc = 0; wc < C::GW; ++wc) {
           uint2 v = make_uint2(0, 0);
-          if (m < p.M) v = ld_nc_v2(p.X + static_cast<int64_t>(m) * (p.K / 2) + k0 / 2 + 4 * wc);
+          if (m < M) v = ld_nc_v2(p.X + xrow(m) * (p.K / 2) + k0 / 2 + 4 * wc);
           const uint32_t h0 = bf16x2_times16(v.x), h1 = bf16x2_times16(v.y);
           s += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y);
           uint2* d2 = reinterpret_cast<uint2*>(dst + wc * C::VPW);
@@ -182,7 +213,7 @@ qmm_mma_kernel(const MmaParams p) {
           uint4 v[C::VPW / 8];
 #pragma unroll
           for (int q = 0; q < C::VPW / 8; ++q) {
-            if (m < p.M) v[q] = ld_nc_v4(p.X + static_cast<int64_t>(m) * p.K + k0 + wc * C::VPW + 8 * q);
+            if (m < M) v[q] = ld_nc_v4(p.X + xrow(m) * p.K + k0 + wc * C::VPW + 8 * q);
             else v[q] = make_uint4(0, 0, 0, 0);
           }
           const uint32_t* e = reinterpret_cast<const uint32_t*>(v);  // VPW/2 words of bf16 pairs
@@ -211,8 +242,8 @@ qmm_mma_kernel(const MmaParams p) {
       float2 sb = make_float2(0.f, 0.f);
       if (n < p.N) {
         const int64_t idx = static_cast<int64_t>(n) * p.G + c0 + jl;
-        const float sc = __half2float(__ushort_as_half(p.S[idx]));
-        const float bi = __half2float(__ushort_as_half(p.B[idx]));
+        const float sc = __half2float(__ushort_as_half(Sg[idx]));
+        const float bi = __half2float(__ushort_as_half(Bg[idx]));
         sb = make_float2(sc, fmaf(E8 ? -2176.f : -128.f, sc, bi));
       }
       meta[rl * p.chunk + jl] = sb;
@@ -314,7 +345,7 @@ qmm_mma_kernel(const MmaParams p) {
     }
   __syncthreads();
 
-  const int E = p.M * C::NT;  // only rows m < M are reduced and written
+  const int E = M * C::NT;  // only rows m < M are reduced and written
   const int splits = gridDim.y;
   if (splits == 1) {
     for (int e = tid; e < E; e += C::THREADS) {
@@ -324,7 +355,7 @@ qmm_mma_kernel(const MmaParams p) {
       const int m = e / C::NT;
       const int n = n0 + (e - m * C::NT);
       if (n < p.N) {
-        const int64_t o = static_cast<int64_t>(m) * p.N + n;
+        const int64_t o = yrow(m) * p.N + n;
         store_y(p.Y, p.R, o, v, p.out_f32);
       }
     }
@@ -347,7 +378,7 @@ qmm_mma_kernel(const MmaParams p) {
     const int m = e / C::NT;
     const int n = n0 + (e - m * C::NT);
     if (n < p.N) {
-      const int64_t o = static_cast<int64_t>(m) * p.N + n;
+      const int64_t o = yrow(m) * p.N + n;
       store_y(p.Y, p.R, o, v, p.out_f32);
     }
   }

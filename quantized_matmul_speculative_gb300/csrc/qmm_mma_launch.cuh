@@ -28,6 +28,17 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   p.out_f32 = a.out_f32;
   p.G = a.K / GS;
   p.gpc = (p.G + splits - 1) / splits;
+  p.lhs = a.lhs;
+  p.rhs = a.rhs;
+  p.P = a.P;
+  p.T = a.T;
+  p.E = a.E;
+  p.tiles = (a.N + C::NT - 1) / C::NT;
+  p.w_stride = static_cast<int64_t>(a.N) * (a.K / C::VPW);
+  p.m_stride = static_cast<int64_t>(a.N) * p.G;
+  // gathered form: one group of row tiles per possible expert of the union
+  const int slots = (a.rhs != nullptr) ? (a.E < a.P ? a.E : a.P) : 1;
+  if (a.rhs != nullptr && (a.P > C::THREADS || slots < 1)) return cudaErrorInvalidValue;
   // Largest chunk that fits the budget, then even chunks across the K-range.
   int cmax = p.gpc;
   while (cmax > 1 && MmaSmem<C>(cmax).total > kMmaSmemBudget) --cmax;
@@ -55,7 +66,7 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   }
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.N + C::NT - 1) / C::NT, splits, 1);
+  cfg.gridDim = dim3(p.tiles * slots, splits, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

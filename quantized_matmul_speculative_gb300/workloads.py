@@ -100,6 +100,36 @@ INT8_AFFINE = Workload(
 )
 
 ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP, INT8_AFFINE)
+
+
+@dataclass(frozen=True)
+class MoeWorkload:
+    """A stack of E expert matrices [N, K] and T tokens routed to k experts each."""
+
+    name: str
+    E: int
+    N: int
+    K: int
+    k: int
+    bits: int
+    group_size: int
+    ts: tuple
+    seed: int
+    note: str = ""
+
+
+MOE_GATE_UP = MoeWorkload(
+    name="moe_gate_up_128x1536x2048_top8_4b_g64",
+    E=128, N=1536, K=2048, k=8, bits=4, group_size=64, ts=(1, 2, 4, 8), seed=7000,
+    note="gate+up projections of a 128-expert, top-8 MoE layer (2048 hidden, 768 expert width), T verify tokens",
+)
+
+
+def moe_union_bytes(w: MoeWorkload, experts) -> int:
+    """Weight + metadata bytes of the distinct experts a routing names."""
+    import numpy as np
+
+    return len(np.unique(np.asarray(experts))) * call_bytes(w.N, w.K, w.bits, w.group_size)
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -101,6 +101,31 @@ def test_residual_validation_before_launch(lib):
     assert rc(M=17) == 2
 
 
+def test_gather_validation_before_launch(lib):
+    """qmm_gather_small_m rejects bad sizes, widths, variants, null and
+    misaligned pointers before any CUDA call."""
+    call = lib.qmm_gather_small_m
+    p = 0x10000
+    # (X, Wq, S, B, lhs, rhs, P, T, E, N, K, bits, gs, Y, out, variant, splits, stream)
+    base = [p, p, p, p, p, p, 8, 4, 16, 64, 256, 4, 64, p, 0, -1, -1, None]
+    pos = {"X": 0, "lhs": 4, "rhs": 5, "P": 6, "T": 7, "E": 8, "N": 9, "K": 10, "bits": 11, "gs": 12, "Y": 13,
+           "out": 14, "variant": 15, "splits": 16}
+
+    def rc(**kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[pos[k]] = v
+        return call(*a)
+
+    assert rc(P=257) == 2 and rc(P=-1) == 2 and rc(T=0) == 2 and rc(E=0) == 2 and rc(K=96) == 2
+    assert rc(bits=3) == 3 and rc(gs=16) == 3 and rc(out=2) == 3 and rc(splits=0) == 3
+    tma = next(i for i, n in enumerate(binding.variant_names()) if n.startswith("tma"))
+    assert rc(variant=tma) == 3
+    assert rc(lhs=None) == 1 and rc(rhs=None) == 1 and rc(Y=None) == 1
+    assert rc(lhs=p + 2) == 4 and rc(X=p + 8) == 4
+    assert rc(P=0) == 0 and rc(N=0) == 0
+
+
 def test_variant_registry(lib):
     names = binding.variant_names()
     assert len(names) == lib.qmm_num_variants() >= 1

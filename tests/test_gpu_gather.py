@@ -1,0 +1,134 @@
+"""GPU parity of the gathered (mixture-of-experts) form,
+Y[i] = X[lhs[i]] . dequant(W[rhs[i]])^T over an expert stack
+(qmm_gather_small_m), against the oracle's gathered product, with the
+library's bound |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from qmm_harness import assert_within, to_f64
+from quantized_matmul_speculative_gb300 import binding, synth, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_matmul_speculative_gb300 import build
+
+    build.build()
+    binding.lib()
+    return torch
+
+
+@pytest.fixture(autouse=True)
+def no_device_faults(torch_cuda):
+    binding.device_status(clear=True)
+    yield
+    torch_cuda.cuda.synchronize()
+    assert binding.device_status(clear=True) == 0
+
+
+class DeviceStack:
+    """A synth.MoeProblem on the GPU (product packing)."""
+
+    def __init__(self, torch, mp: synth.MoeProblem):
+        self.mp = mp
+        E, N, K = mp.E, mp.N, mp.K
+        wq = binding.pack(mp.q.reshape(E * N, K), mp.bits).reshape(E, N, -1)
+        self.wq = torch.from_numpy(wq.view(np.int32)).cuda()
+        self.s = torch.from_numpy(mp.scales.view(np.float16)).cuda()
+        self.b = torch.from_numpy(mp.biases.view(np.float16)).cuda()
+        self.x = torch.from_numpy(mp.x.view(np.int16)).cuda().view(torch.bfloat16)
+
+    def run(self, torch, T, lhs, rhs, **kw):
+        return binding.gather_small_m(self.x[:T].contiguous(), self.wq, self.s, self.b,
+                                      torch.from_numpy(lhs).cuda(), torch.from_numpy(rhs).cuda(), self.mp.bits,
+                                      self.mp.group_size, **kw)
+
+
+def oracle_ref(mp: synth.MoeProblem, T, lhs, rhs):
+    ol = oracle.load()
+    E, N, K = mp.E, mp.N, mp.K
+    wq = ol.pack(mp.q.reshape(E * N, K), mp.bits).reshape(E, N, -1)
+    return ol.gather_qmm(mp.x[:T], wq, mp.scales, mp.biases, lhs, rhs, mp.bits, mp.group_size)
+
+
+def mma_variants():
+    return [i for i, n in enumerate(binding.variant_names()) if n.startswith("mma")]
+
+
+@pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (8, 32), (4, 128)])
+def test_gather_small_stacks(torch_cuda, bits, gs):
+    """Ragged N, T = 1..16 tokens routed to k = 1..4 distinct experts, every
+    mma variant, split 1 and 2, bf16 and fp32."""
+    torch = torch_cuda
+    E, N, K = 6, 200, 4 * gs
+    for T, k in ((1, 1), (3, 2), (8, 4), (16, 2), (5, 4)):
+        mp = synth.make_moe(8100 + T * 10 + k + bits * 100 + gs, E, N, K, bits, gs, T, k)
+        ds = DeviceStack(torch, mp)
+        lhs, rhs = mp.lists()
+        y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
+        for v in mma_variants():
+            for s in (1, 2):
+                for dt in (torch.float32, torch.bfloat16):
+                    y = ds.run(torch, T, lhs, rhs, out_dtype=dt, variant=v, splits=s)
+                    assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
+
+
+def test_gather_arbitrary_lists_and_determinism(torch_cuda):
+    """A hand-made list with repeated entries, unsorted experts and an expert
+    used by one entry only; repeats are bit-identical."""
+    torch = torch_cuda
+    mp = synth.make_moe(8200, 5, 136, 512, 4, 64, 4, 1)
+    ds = DeviceStack(torch, mp)
+    lhs = np.array([3, 0, 0, 2, 1, 3, 0, 2], dtype=np.int32)
+    rhs = np.array([4, 1, 4, 1, 0, 1, 1, 4], dtype=np.int32)
+    y_ref, a_ref = oracle_ref(mp, 4, lhs, rhs)
+    first = ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32)
+    assert_within(to_f64(first), y_ref, a_ref, "hand-made list")
+    for _ in range(3):
+        assert torch.equal(first, ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32))
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_gather_moe_workload_full(torch_cuda, T):
+    """The 128-expert top-8 gate+up stack at verify widths: every output."""
+    torch = torch_cuda
+    w = workloads.MOE_GATE_UP
+    mp = synth.make_moe(w.seed, w.E, w.N, w.K, w.bits, w.group_size, T, w.k)
+    ds = DeviceStack(torch, mp)
+    lhs, rhs = mp.lists()
+    y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
+    y = ds.run(torch, T, lhs, rhs)
+    assert_within(to_f64(y), y_ref, a_ref, f"moe T={T}")
+
+
+def test_gather_invalid_lists_flagged(torch_cuda):
+    """An expert index out of range, and a ninth entry for one expert with
+    T <= 8: the affected rows stay unwritten, the others are right, and the
+    device status word reports bit 3."""
+    torch = torch_cuda
+    mp = synth.make_moe(8300, 4, 64, 256, 4, 64, 4, 1)
+    ds = DeviceStack(torch, mp)
+    lhs = np.array([0, 1, 2, 3], dtype=np.int32)
+    rhs = np.array([0, 9, 2, 1], dtype=np.int32)
+    out = torch.full((4, 64), 5.0, dtype=torch.float32, device="cuda")
+    ds.run(torch, 4, lhs, rhs, out=out)
+    torch.cuda.synchronize()
+    assert binding.device_status(clear=True) & 8
+    assert bool((out[1] == 5.0).all())
+    ok = np.array([0, 2, 3])
+    y_ref, a_ref = oracle_ref(mp, 4, lhs[ok], rhs[ok])
+    assert_within(to_f64(out)[ok], y_ref, a_ref, "valid rows of a list with a bad index")
+
+    lhs9 = np.array([0, 1, 2, 3, 0, 1, 2, 3, 0], dtype=np.int32)
+    rhs9 = np.zeros(9, dtype=np.int32)
+    out9 = torch.full((9, 64), 5.0, dtype=torch.float32, device="cuda")
+    ds.run(torch, 4, lhs9, rhs9, out=out9)
+    torch.cuda.synchronize()
+    assert binding.device_status(clear=True) & 8
+    assert bool((out9 == 5.0).all())
