@@ -383,20 +383,23 @@ def moe_report(torch, dev, stream, peak):
         rhs = torch.from_numpy(np.ascontiguousarray(experts.reshape(-1))).to(dev)
         ub = workloads.moe_union_bytes(w, experts)
 
-        def capture(i, T=T, lhs=lhs, rhs=rhs):
+        def capture(i, T=T, lhs=lhs, rhs=rhs, v=-1):
             wq_d, s_d, b_d = copies[i % ncopy]
             binding.gather_small_m_ptr(x.data_ptr(), wq_d.data_ptr(), s_d.data_ptr(), b_d.data_ptr(), lhs.data_ptr(),
                                        rhs.data_ptr(), T * w.k, T, w.E, w.N, w.K, w.bits, w.group_size, y.data_ptr(),
-                                       binding.OUT_BF16, -1, -1, handle)
+                                       binding.OUT_BF16, v, -1, handle)
         us = graph_us_per_call(torch, stream, capture, 32)
+        tma = binding.variant_names().index("tma_w8_2cta")
+        us_tma = graph_us_per_call(torch, stream, lambda i, T=T, lhs=lhs, rhs=rhs: capture(i, T, lhs, rhs, tma), 32)
         gbs = ub / (us * 1e-6) / 1e9
         res.append({"T": T, "entries": T * w.k, "experts_in_union": int(len(np.unique(experts))),
                     "union_bytes": ub, "us_per_call": round(us, 3), "union_gbs": round(gbs, 1),
-                    "frac_hbm": round(gbs / peak, 4)})
+                    "frac_hbm": round(gbs / peak, 4), "us_per_call_tma_w8_2cta": round(us_tma, 3)})
     del copies, wq, sc, bi
     torch.cuda.empty_cache()
     return {"workload": w.name, "per_t": res,
-            "note": "gathered form on the mma family; bytes = distinct experts of the routing x expert bytes"}
+            "note": "gathered form at the library's choice (mma family), and forced onto tma_w8_2cta; "
+                    "bytes = distinct experts of the routing x expert bytes"}
 
 
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):

@@ -106,14 +106,20 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
  * stack of E matrices back to back, each in the layout above; lhs, rhs int32
  * [P] device arrays, 0 <= lhs[i] < T, 0 <= rhs[i] < E; Y [P, N].  Each expert
  * in the union of rhs is streamed once per call for all the entries that name
- * it.  Entries per expert: at most 8 if T <= 8 or P <= 8, else at most 16
- * (true when the k experts of each token are distinct).  P <= 256.
+ * it.  P <= 256.  On the mma variants, entries per expert: at most 8 if
+ * T <= 8 or P <= 8, else at most 16 (true when the k experts of each token
+ * are distinct and T <= 16).
  * Source: "MLX quantized_matmul small-M verify kernels", the open question on
  * "dense and MoE (gather_qmm) verify" and the "expert-union cost per verify
  * row".
- * Runs on the "mma" variants (variant = -1: the first; a TMA variant returns
- * QMM_ERR_UNSUPPORTED); splits as in qmm_small_m_ex.  The index lists are read
- * on the device: an index out of range, or too many entries for one expert,
+ * variant = -1 runs the "mma" variants, which take each expert's own entries.
+ * A forced "tma" variant (T <= 16, a shape the tma variants take, P at most
+ * its thread count) computes all T rows against each expert of the union and
+ * writes the rows the entries name (then any number of entries per expert is
+ * fine); otherwise it returns QMM_ERR_UNSUPPORTED, as does a "tma_own"
+ * variant.  splits as in qmm_small_m_ex.  The index
+ * lists are read on the device, after the wait for the preceding kernel: an
+ * index out of range, or (mma variants) too many entries for one expert,
  * leaves the affected rows of Y unwritten and sets bit 3 of
  * qmm_device_status().  K == 0 fills Y with zeros; P == 0 or N == 0 launches
  * nothing.                                                                     */

@@ -169,7 +169,8 @@ int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
 // candidate (8, 4, 2, 1) with the best tile balance over the clusters that fit
 // two CTAs per SM, larger clusters first on ties.
 int rule_tma_cluster(const CallArgs& a, const VariantDesc& d) {
-  const int tiles = (a.N + 15) / 16;
+  // (the gathered form: the tiles of the largest possible union)
+  const int tiles = ((a.N + 15) / 16) * (a.rhs != nullptr ? (a.E < a.P ? a.E : a.P) : 1);
   const int sms = device_sm_count();
   int best = -1;
   double best_cost = 1e30;
@@ -501,12 +502,11 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
 qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
                               const int32_t* lhs, const int32_t* rhs, int P, int T, int E, int N, int K, int bits,
                               int group_size, void* Y, int out_dtype, int variant, int splits, void* stream) {
-  constexpr int kMaxGatherEntries = 256;  // one entry per thread of the index scan
   if (P < 0 || P > kMaxGatherEntries || T < 0 || E < 0 || N < 0 || K < 0) return QMM_ERR_SHAPE;
   if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
   if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
   if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
-  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family != kFamilyMma))
+  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family == kFamilyOwn))
     return QMM_ERR_UNSUPPORTED;
   if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
   if (K % group_size != 0) return QMM_ERR_SHAPE;
@@ -533,7 +533,7 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   a.B = static_cast<const uint16_t*>(biases);
   a.Y = Y;
   a.R = nullptr;
-  a.M = (T <= 8 || P <= 8) ? 8 : 16;  // entries one expert may take: the activation tile
+  a.M = 0;
   a.N = N;
   a.K = K;
   a.bits = bits;
@@ -545,7 +545,32 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   a.T = T;
   a.E = E;
   const int fv = forced_variant();
-  if (variant < 0 && fv >= 0 && kVariants[fv].family == kFamilyMma) variant = fv;
+  if (variant < 0 && fv >= 0 && kVariants[fv].family != kFamilyOwn) variant = fv;
+
+  // A tma variant (forced) computes every token row against each expert of
+  // the union (T <= 16 rows staged once) under the TMA shape rules; the mma
+  // family (the default: measured faster on the 128-expert top-8 stack, where
+  // the tma kernel needs many reduction rounds) takes each expert's own
+  // entries (at most 8 or 16 of them).
+  const bool tma_forced = variant >= 0 && kVariants[variant].family == kFamilyTma;
+  if (T <= 16 && tma_forced) {
+    CallArgs at = a;
+    at.M = T;
+    const VariantDesc& dd = kVariants[variant];
+    if (P > 32 * (dd.WN + 1)) return QMM_ERR_UNSUPPORTED;
+    const int c = splits > 0 ? (tma_supported(at, splits, dd) ? splits : -1) : rule_tma_cluster(at, dd);
+    if (c < 1) return QMM_ERR_UNSUPPORTED;
+    if (env_flag("QMM_LOG"))
+      std::fprintf(stderr, "qmm gather: P=%d T=%d E=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", P, T, E, N, K,
+                   bits, group_size, dd.name, c);
+    const cudaError_t e = launch_tma(at, dd, c, st);
+    if (e == cudaSuccess) return QMM_OK;
+    if (e == cudaErrorInvalidValue) return QMM_ERR_UNSUPPORTED;
+    return fail_cuda(e);
+  } else if (tma_forced) {
+    return QMM_ERR_UNSUPPORTED;
+  }
+  a.M = (T <= 8 || P <= 8) ? 8 : 16;  // entries one expert may take: the activation tile
   const VariantDesc& d = kVariants[variant < 0 ? 0 : variant];
   int s = splits;
   if (s < 0) {

@@ -24,6 +24,10 @@ struct CallArgs {
   int P = 0, T = 0, E = 0;
 };
 
+// Most entries of a gathered call: the kernels scan the index lists with one
+// entry per thread.
+constexpr int kMaxGatherEntries = 256;
+
 // 8-bit codes run on the 4-bit kernels as "virtual" 4-bit codes (each byte
 // read as its low and high nibble): the same words, groups and scales, with
 // twice as many codes per row and per group.

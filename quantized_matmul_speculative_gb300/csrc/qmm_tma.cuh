@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include "qmm_device.cuh"
+#include "qmm_gather.cuh"
 #include "qmm_geometry.h"
 #include "qmm_group.cuh"
 
@@ -79,6 +80,16 @@ struct TmaParams {
   int recv_tiles; // tiles one CTA owns in the push reduction
   int mbw;        // scale/bias TMA box width in halves
   int out_f32;
+  // Gathered form (rhs null: a plain call).  The tensor maps span the whole
+  // stack (E*N rows); tile tau is row tile tau % tpe of the expert in union
+  // slot tau / tpe; every token row (M = T) is computed against it and the
+  // entries naming (token, expert) receive the result.  `tiles` is then the
+  // largest union's tile count; the kernel splits the actual union's tiles.
+  const int32_t* lhs;
+  const int32_t* rhs;
+  int P, E;
+  int tpe;        // 16-row tiles per matrix of the stack
+  int gather_off; // byte offset of the gathered lists' shared scratch
 };
 
 template <int BITS, int GS, int NB, int W, int SMAX>
@@ -96,7 +107,7 @@ struct TmaCfg {
   static constexpr int CONSUMER_THREADS = 32 * W;
 };
 
-template <int BITS, int GS, int NB, int W, int SMAX, bool E8>
+template <int BITS, int GS, int NB, int W, int SMAX, bool E8, bool GATHER>
 __global__ void __launch_bounds__(32 * (W + 1), (W <= 8) ? 2 : 1)
 qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
@@ -121,10 +132,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int csize = static_cast<int>(gridDim.x);  // CTAs per cluster (cluster spans x)
   const int rank = static_cast<int>(blockIdx.x);
   const int q = static_cast<int>(blockIdx.y);
-  const int t_begin = static_cast<int>((static_cast<int64_t>(p.tiles) * q) / p.ncl);
-  const int t_end = static_cast<int>((static_cast<int64_t>(p.tiles) * (q + 1)) / p.ncl);
-  const int nt = t_end - t_begin;
-  const int nrounds = (nt + p.rt - 1) / p.rt;
+  // this cluster's tiles (computed before the barrier below, which hides the
+  // 64-bit divisions; a gathered call recomputes them for its actual union)
+  int t_begin = static_cast<int>((static_cast<int64_t>(p.tiles) * q) / p.ncl);
+  int t_end = static_cast<int>((static_cast<int64_t>(p.tiles) * (q + 1)) / p.ncl);
   const int g0 = rank * p.gp;  // first group of this CTA's K-piece
 
   QMM_TRACE_POINT(0);
@@ -137,6 +148,39 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     fence_mbar_init();
   }
   __syncthreads();
+  // Gathered form: the index lists may be the previous call's output, so they
+  // are read after the dependency wait (the weights of a gathered call cannot
+  // stream before it: which experts to read is not known yet).
+  constexpr bool gathered = GATHER;
+  GatherLists gl;
+  if constexpr (GATHER) {
+    griddep_wait();
+    gl = gather_lists<C::THREADS>(p.lhs, p.rhs, p.P, p.M, p.E, reinterpret_cast<int*>(smem + p.gather_off));
+    const int tiles = gl.u * p.tpe;
+    t_begin = static_cast<int>((static_cast<int64_t>(tiles) * q) / p.ncl);
+    t_end = static_cast<int>((static_cast<int64_t>(tiles) * (q + 1)) / p.ncl);
+  }
+  // first weight row (of the tensor maps) of tile tau, and its first output row within its matrix
+  auto tile_row = [&](int tau) {
+    if constexpr (GATHER) return gl.expert[tau / p.tpe] * p.N + (tau % p.tpe) * 16;
+    else return tau * 16;
+  };
+  auto tile_n0 = [&](int tau) {
+    if constexpr (GATHER) return (tau % p.tpe) * 16;
+    else return tau * 16;
+  };
+  // Y[m, n] of tile tau: the plain store, or one store per entry naming (token m, the tile's expert)
+  auto store_tile = [&](int tau, int m, int n, float v) {
+    if constexpr (!GATHER) {
+      store_y(p.Y, p.R, static_cast<int64_t>(m) * p.N + n, v, p.out_f32);
+    } else {
+      const int sl = tau / p.tpe;
+      for (int j = gl.start[sl]; j < gl.start[sl + 1]; ++j)
+        if (gl.token[j] == m) store_y(p.Y, nullptr, static_cast<int64_t>(gl.entry[j]) * p.N + n, v, p.out_f32);
+    }
+  };
+  const int nt = t_end - t_begin;
+  const int nrounds = (nt + p.rt - 1) / p.rt;
   // Push reduction: tell the cluster this CTA's barriers exist (the matching
   // wait comes right before the first remote store).
   if (p.push) cluster_arrive();
@@ -163,7 +207,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       const int s = i % S;
       if (lane == 0) {
         if (i >= S) mbar_wait(empty_bar(s), ((i / S) - 1) & 1, kStatusTimeoutEmpty);
-        const int n0 = (t_begin + i) * 16;
+        const int n0 = tile_row(t_begin + i);
         const uint32_t dst = smem_addr(smem + L.stage_off + s * L.stage_bytes);
         mbar_arrive_expect_tx(full_bar(s), tx_bytes);
         for (int b = 0; b < p.nbox; ++b)
@@ -389,11 +433,8 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         for (int r2 = 0; r2 < csize; ++r2) v += recv[(o * csize + r2) * C::MP * 16 + r];
         const int i = i_lo + o * csize + rank;
         const int m = r >> 4;
-        const int n = (t_begin + i) * 16 + (r & 15);
-        if (n < p.N) {
-          const int64_t off = static_cast<int64_t>(m) * p.N + n;
-          store_y(p.Y, p.R, off, v, p.out_f32);
-        }
+        const int n = tile_n0(t_begin + i) + (r & 15);
+        if (n < p.N) store_tile(t_begin + i, m, n, v);
       }
       QMM_TRACE_POINT(6);
       return;  // one round only
@@ -409,11 +450,8 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         float v = 0.f;
         for (int r2 = 0; r2 < csize; ++r2) v += ld_dsmem_f32(src, static_cast<uint32_t>(r2));
         const int m = e >> 4;
-        const int n = (t_begin + i) * 16 + (e & 15);
-        if (n < p.N) {
-          const int64_t o = static_cast<int64_t>(m) * p.N + n;
-          store_y(p.Y, p.R, o, v, p.out_f32);
-        }
+        const int n = tile_n0(t_begin + i) + (e & 15);
+        if (n < p.N) store_tile(t_begin + i, m, n, v);
       }
     }
     QMM_TRACE_POINT(5);

@@ -62,7 +62,7 @@ inline int max_active_clusters(const void* kern, int threads, int smem, int csiz
   return n;
 }
 
-template <int BITS, int GS, int NB, int W, int S, bool E8>
+template <int BITS, int GS, int NB, int W, int S, bool E8, bool GATHER>
 cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaStream_t stream) {
   using Cfg = TmaCfg<BITS, GS, NB, W, S>;
   TmaParams p;
@@ -80,26 +80,42 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p.gp) - 1) / static_cast<unsigned long long>(p.gp);
   if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorInvalidValue;
   p.tiles = (a.N + 15) / 16;
+  // Gathered form: tiles of the largest possible union; the stack's rows in the tensor maps
+  p.lhs = a.lhs;
+  p.rhs = a.rhs;
+  p.P = a.P;
+  p.E = a.E;
+  p.tpe = p.tiles;
+  p.gather_off = 0;
+  constexpr bool gathered = GATHER;
+  int64_t map_rows = a.N;
+  if (gathered) {
+    if (a.P > Cfg::THREADS || a.P > kMaxGatherEntries || a.E < 1) return cudaErrorInvalidValue;
+    p.tiles = (a.E < a.P ? a.E : a.P) * p.tpe;
+    map_rows = static_cast<int64_t>(a.E) * a.N;
+  }
+  const int gather_bytes = gathered ? kGatherSmemInts * 4 : 0;
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
-  auto kern = qmm_tma_kernel<BITS, GS, NB, W, S, E8>;
+  auto kern = qmm_tma_kernel<BITS, GS, NB, W, S, E8, GATHER>;
   // Shared memory: what remains of the SM's budget for ctas_per_sm CTAs goes to
   // the partial tiles of one reduction round.
   int sm_bytes = 0, optin = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const int budget = tma_smem_budget(sm_bytes, optin, ctas_per_sm);
+  const int budget_all = tma_smem_budget(sm_bytes, optin, ctas_per_sm);
+  const int budget = budget_all - gather_bytes;  // what the stages and partials may use
   static std::mutex mu;
   static int smem_set = 0;
   static bool nonportable = false;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (budget > smem_set) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    if (budget_all > smem_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, budget_all);
       if (e != cudaSuccess) return e;
-      smem_set = budget;
+      smem_set = budget_all;
     }
     if (csize > 8 && !nonportable) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -108,7 +124,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
     }
   }
   // Clusters: as many as fit at the budget's shared-memory size, no more than tiles.
-  int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget, csize);
+  int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget_all, csize);
   if (ncl < 1) return cudaErrorInvalidConfiguration;
   if (ncl > p.tiles) ncl = p.tiles;
   p.ncl = ncl;
@@ -172,11 +188,15 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
       p.recv_tiles = recv_tiles;
     }
   }
-  const int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
+  int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
+  if (gathered) {
+    p.gather_off = (smem + 15) & ~15;
+    smem = p.gather_off + gather_bytes;
+  }
 
   CUtensorMap tmap, tmap_s, tmap_b;
   {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(map_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.box_words), 16u};
     const cuuint32_t estride[2] = {1u, 1u};
@@ -186,7 +206,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
       return cudaErrorInvalidValue;
   }
   for (int arr = 0; arr < 2; ++arr) {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.G), static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(p.G), static_cast<cuuint64_t>(map_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(p.G) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
     const cuuint32_t estride[2] = {1u, 1u};
@@ -227,7 +247,8 @@ template <int BITS, int GS, int NB, bool E8>
 cudaError_t launch_tma_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream) {
 #define QMM_TRY_TMA(w, s)                                                   \
   if (d.WN == (w) && d.R == (s))                                            \
-    return launch_tma_impl<BITS, GS, NB, w, s, E8>(a, csize, d.WK, stream);
+    return (a.rhs != nullptr) ? launch_tma_impl<BITS, GS, NB, w, s, E8, true>(a, csize, d.WK, stream)  \
+                              : launch_tma_impl<BITS, GS, NB, w, s, E8, false>(a, csize, d.WK, stream);
   QMM_TMA_TILES(QMM_TRY_TMA)
 #undef QMM_TRY_TMA
   return cudaErrorInvalidValue;

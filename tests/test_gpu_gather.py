@@ -57,41 +57,59 @@ def oracle_ref(mp: synth.MoeProblem, T, lhs, rhs):
     return ol.gather_qmm(mp.x[:T], wq, mp.scales, mp.biases, lhs, rhs, mp.bits, mp.group_size)
 
 
-def mma_variants():
-    return [i for i, n in enumerate(binding.variant_names()) if n.startswith("mma")]
+def gather_variants():
+    """The mma variants and the tma variants (not the warp-owned ones)."""
+    return [i for i, n in enumerate(binding.variant_names()) if n.startswith("mma") or
+            (n.startswith("tma") and not n.startswith("tma_own"))]
 
 
+@pytest.mark.parametrize("groups", [4, 8], ids=["G4_mma_only", "G8_tma_too"])
 @pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (8, 32), (4, 128)])
-def test_gather_small_stacks(torch_cuda, bits, gs):
+def test_gather_small_stacks(torch_cuda, bits, gs, groups):
     """Ragged N, T = 1..16 tokens routed to k = 1..4 distinct experts, every
-    mma variant, split 1 and 2, bf16 and fp32."""
+    mma and tma variant, split 1 and 2, bf16 and fp32.  With 4 groups per row
+    only the mma variants take the shape."""
     torch = torch_cuda
-    E, N, K = 6, 200, 4 * gs
+    E, N, K = 6, 200, groups * gs
+    ran_tma = False
     for T, k in ((1, 1), (3, 2), (8, 4), (16, 2), (5, 4)):
-        mp = synth.make_moe(8100 + T * 10 + k + bits * 100 + gs, E, N, K, bits, gs, T, k)
+        mp = synth.make_moe(8100 + T * 10 + k + bits * 100 + gs + groups, E, N, K, bits, gs, T, k)
         ds = DeviceStack(torch, mp)
         lhs, rhs = mp.lists()
         y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
-        for v in mma_variants():
+        y = ds.run(torch, T, lhs, rhs, out_dtype=torch.float32)  # the library's choice (mma)
+        assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} default")
+        for v in gather_variants():
             for s in (1, 2):
                 for dt in (torch.float32, torch.bfloat16):
-                    y = ds.run(torch, T, lhs, rhs, out_dtype=dt, variant=v, splits=s)
+                    try:
+                        y = ds.run(torch, T, lhs, rhs, out_dtype=dt, variant=v, splits=s)
+                    except binding.QmmError as e:
+                        assert e.status == 3 and binding.variant_names()[v].startswith("tma")
+                        continue
+                    ran_tma |= binding.variant_names()[v].startswith("tma")
                     assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
+    assert ran_tma == (groups == 8)
 
 
-def test_gather_arbitrary_lists_and_determinism(torch_cuda):
-    """A hand-made list with repeated entries, unsorted experts and an expert
-    used by one entry only; repeats are bit-identical."""
+@pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])
+def test_gather_arbitrary_lists_and_determinism(torch_cuda, K):
+    """A hand-made list with a repeated (token, expert) entry, unsorted experts
+    and an expert used by one entry only, on the default (mma) path and (8
+    groups per row) a forced tma variant; repeats are bit-identical."""
     torch = torch_cuda
-    mp = synth.make_moe(8200, 5, 136, 512, 4, 64, 4, 1)
+    mp = synth.make_moe(8200, 5, 136, K, 4, 64, 4, 1)
     ds = DeviceStack(torch, mp)
     lhs = np.array([3, 0, 0, 2, 1, 3, 0, 2], dtype=np.int32)
     rhs = np.array([4, 1, 4, 1, 0, 1, 1, 4], dtype=np.int32)
     y_ref, a_ref = oracle_ref(mp, 4, lhs, rhs)
-    first = ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32)
-    assert_within(to_f64(first), y_ref, a_ref, "hand-made list")
-    for _ in range(3):
-        assert torch.equal(first, ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32))
+    tma = binding.variant_names().index("tma_w8_2cta")
+    for v in ([-1, tma] if K == 512 else [-1]):
+        first = ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32, variant=v)
+        assert_within(to_f64(first), y_ref, a_ref, f"hand-made list v{v}")
+        assert torch.equal(first[1], first[6]), "a repeated entry gets the same row"
+        for _ in range(3):
+            assert torch.equal(first, ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32, variant=v))
 
 
 @pytest.mark.parametrize("T", [1, 4, 8])
@@ -107,24 +125,34 @@ def test_gather_moe_workload_full(torch_cuda, T):
     assert_within(to_f64(y), y_ref, a_ref, f"moe T={T}")
 
 
-def test_gather_invalid_lists_flagged(torch_cuda):
-    """An expert index out of range, and a ninth entry for one expert with
-    T <= 8: the affected rows stay unwritten, the others are right, and the
-    device status word reports bit 3."""
+@pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])
+def test_gather_invalid_index_flagged(torch_cuda, K):
+    """An expert index out of range: its row stays unwritten, the others are
+    right, and the device status word reports bit 3."""
     torch = torch_cuda
-    mp = synth.make_moe(8300, 4, 64, 256, 4, 64, 4, 1)
+    mp = synth.make_moe(8300, 4, 64, K, 4, 64, 4, 1)
     ds = DeviceStack(torch, mp)
     lhs = np.array([0, 1, 2, 3], dtype=np.int32)
     rhs = np.array([0, 9, 2, 1], dtype=np.int32)
-    out = torch.full((4, 64), 5.0, dtype=torch.float32, device="cuda")
-    ds.run(torch, 4, lhs, rhs, out=out)
-    torch.cuda.synchronize()
-    assert binding.device_status(clear=True) & 8
-    assert bool((out[1] == 5.0).all())
     ok = np.array([0, 2, 3])
     y_ref, a_ref = oracle_ref(mp, 4, lhs[ok], rhs[ok])
-    assert_within(to_f64(out)[ok], y_ref, a_ref, "valid rows of a list with a bad index")
+    tma = binding.variant_names().index("tma_w8_2cta")
+    for v in ([-1, tma] if K == 512 else [-1]):
+        out = torch.full((4, 64), 5.0, dtype=torch.float32, device="cuda")
+        ds.run(torch, 4, lhs, rhs, out=out, variant=v)
+        torch.cuda.synchronize()
+        assert binding.device_status(clear=True) & 8
+        assert bool((out[1] == 5.0).all())
+        assert_within(to_f64(out)[ok], y_ref, a_ref, f"valid rows of a list with a bad index v{v}")
 
+
+def test_gather_too_many_entries_for_one_expert_flagged(torch_cuda):
+    """On the mma variants, a ninth entry for one expert with T <= 8 is flagged
+    and that expert's rows stay unwritten; a forced tma variant (8 groups per
+    row) takes the same list."""
+    torch = torch_cuda
+    mp = synth.make_moe(8301, 4, 64, 256, 4, 64, 4, 1)
+    ds = DeviceStack(torch, mp)
     lhs9 = np.array([0, 1, 2, 3, 0, 1, 2, 3, 0], dtype=np.int32)
     rhs9 = np.zeros(9, dtype=np.int32)
     out9 = torch.full((9, 64), 5.0, dtype=torch.float32, device="cuda")
@@ -132,3 +160,8 @@ def test_gather_invalid_lists_flagged(torch_cuda):
     torch.cuda.synchronize()
     assert binding.device_status(clear=True) & 8
     assert bool((out9 == 5.0).all())
+    mp8 = synth.make_moe(8302, 4, 64, 512, 4, 64, 4, 1)
+    ds8 = DeviceStack(torch, mp8)
+    y = ds8.run(torch, 4, lhs9, rhs9, out_dtype=torch.float32, variant=binding.variant_names().index("tma_w8_2cta"))
+    y_ref, a_ref = oracle_ref(mp8, 4, lhs9, rhs9)
+    assert_within(to_f64(y), y_ref, a_ref, "nine entries for one expert on the tma path")
