@@ -142,6 +142,36 @@ qmm_mma_kernel(const MmaParams p) {
   const uint16_t* Sg = p.S;
   const uint16_t* Bg = p.B;
   const bool gathered = p.rhs != nullptr;
+  // Programmatic dependent launch: the next kernel may start now.  Until the
+  // previous one has finished, only the weights (which it cannot have
+  // written) are touched: a plain call pulls its CTA's weight rows and
+  // scales/biases into L2.  X, the index lists and Y come after the wait.
+  griddep_launch_dependents();
+  if (!gathered) {
+    const int g_lo = blockIdx.y * p.gpc;
+    const int g_hi = (g_lo + p.gpc < p.G) ? g_lo + p.gpc : p.G;
+    const int64_t rw = static_cast<int64_t>(p.K) / C::VPW;
+    const int bytes = (g_hi - g_lo) * C::GW * 4;    // of one row's K-range
+    const int lines = (bytes + 127) / 128 + 1;       // 128-byte lines it can touch
+    for (int u = tid; u < C::NT * lines; u += C::THREADS) {
+      const int r = u / lines;
+      const int n = tile * C::NT + r;
+      if (n >= p.N || bytes <= 0) continue;
+      // every address stays inside the row's range [lo, lo + bytes)
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(Wq + n * rw + static_cast<int64_t>(g_lo) * C::GW);
+      uintptr_t a = (lo & ~static_cast<uintptr_t>(127)) + 128 * static_cast<uintptr_t>(u - r * lines);
+      if (a < lo) a = lo;
+      if (a < lo + bytes) prefetch_l2(reinterpret_cast<const void*>(a));
+    }
+    for (int r = tid; r < C::NT; r += C::THREADS) {
+      const int n = tile * C::NT + r;
+      if (n < p.N && g_lo < g_hi) {
+        prefetch_l2(Sg + static_cast<int64_t>(n) * p.G + g_lo);
+        prefetch_l2(Bg + static_cast<int64_t>(n) * p.G + g_lo);
+      }
+    }
+  }
+  griddep_wait();
   if (gathered) {
     tile = blockIdx.x % p.tiles;
     int e = 0;
