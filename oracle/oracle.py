@@ -66,8 +66,10 @@ class OracleLib:
         lib.oracle_dequant.argtypes = [vp, vp, vp, i64, i64, c_int, i64, vp]
         lib.oracle_qmm_residual.argtypes = [vp, vp, vp, vp, vp, c_int, i64, i64, i64, c_int, i64, vp, vp]
         lib.oracle_gather_qmm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, i64, vp, vp]
+        lib.oracle_ggml_dequant.argtypes = [c_int, vp, i64, i64, vp]
+        lib.oracle_ggml_qmm.argtypes = [c_int, vp, vp, i64, i64, i64, vp, vp]
         for name in ("oracle_pack", "oracle_unpack", "oracle_qmm", "oracle_qmm_sampled", "oracle_dequant",
-                     "oracle_qmm_residual", "oracle_gather_qmm"):
+                     "oracle_qmm_residual", "oracle_gather_qmm", "oracle_ggml_dequant", "oracle_ggml_qmm"):
             getattr(lib, name).restype = c_int
         self.lib = lib
 
@@ -153,6 +155,35 @@ class OracleLib:
                                         bits, group_size, _ptr(y), _ptr(a))
         if rc:
             raise OracleError(f"oracle_gather_qmm rc={rc}")
+        return y, a
+
+    GGML_TYPES = {"q4_0": (0, 18), "q4_1": (1, 20), "q8_0": (2, 34)}
+
+    def ggml_dequant(self, kind: str, blocks, n: int, k: int) -> np.ndarray:
+        """fp64 W[N, K] from ggml blocks (uint8, N * K/32 blocks, row-major)."""
+        t, nbytes = self.GGML_TYPES[kind]
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        if blocks.size != n * (k // 32) * nbytes:
+            raise OracleError("block buffer size does not match N, K")
+        w = np.empty((n, k), dtype=np.float64)
+        rc = self.lib.oracle_ggml_dequant(t, _ptr(blocks), n, k, _ptr(w))
+        if rc:
+            raise OracleError(f"oracle_ggml_dequant rc={rc}")
+        return w
+
+    def ggml_qmm(self, kind: str, x_bits, blocks, n: int):
+        """(Y, A) of X . W^T for W [N, K] in ggml blocks."""
+        t, nbytes = self.GGML_TYPES[kind]
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        m, k = x.shape
+        if blocks.size != n * (k // 32) * nbytes:
+            raise OracleError("block buffer size does not match N, K")
+        y = np.empty((m, n), dtype=np.float64)
+        a = np.empty((m, n), dtype=np.float64)
+        rc = self.lib.oracle_ggml_qmm(t, _ptr(x), _ptr(blocks), m, n, k, _ptr(y), _ptr(a))
+        if rc:
+            raise OracleError(f"oracle_ggml_qmm rc={rc}")
         return y, a
 
     def qmm_sampled(self, x_bits, wq, s_bits, b_bits, bits: int, group_size: int, ms, ns):

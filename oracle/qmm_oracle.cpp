@@ -45,6 +45,17 @@
 //      - "MLX quantized_matmul small-M verify kernels", the open question on
 //        "dense and MoE (gather_qmm) verify" and the "expert-union cost per
 //        verify row".
+//  * ggml block formats Q4_0, Q4_1 and Q8_0 (oracle_ggml_dequant, _qmm): blocks
+//    of 32 weights along K, each row of W a run of K/32 blocks.  The pages name
+//    the formats without their byte layout ("metal : few-row MMA mat-mul ...",
+//    Overview: Q4_0, Q8_0 and Q4_1 kernels); the reading used is the public
+//    ggml layout:
+//      Q4_0, 18 bytes: fp16 d, then 16 bytes of 4-bit codes c; byte j holds
+//            element j in its low nibble and element j + 16 in its high one;
+//            w = d * (c - 8).
+//      Q4_1, 20 bytes: fp16 d, fp16 m, then the 16 code bytes as in Q4_0;
+//            w = d * c + m.
+//      Q8_0, 34 bytes: fp16 d, then 32 signed bytes q; w = d * q.
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
 // shapes (2-, 4- and 8-bit), closed forms (all-zero codes, one-hot X, X = 1,
@@ -235,6 +246,58 @@ int oracle_gather_qmm(const uint16_t* X, const uint32_t* Wq, const uint16_t* S, 
       if (A) A[i * N + n] = a;
     }
   }
+  return 0;
+}
+
+// ggml blocks: type 0 = Q4_0, 1 = Q4_1, 2 = Q8_0 (layouts in the header
+// comment).  Dequantized W[N,K] in fp64; returns 2 for a bad shape or type.
+int oracle_ggml_dequant(int type, const uint8_t* blocks, int64_t N, int64_t K, double* W) {
+  if (type < 0 || type > 2 || N < 0 || K < 0 || K % 32 != 0) return 2;
+  const int64_t bytes = type == 0 ? 18 : type == 1 ? 20 : 34;
+  const int64_t nb = K / 32;
+  for (int64_t n = 0; n < N; ++n) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (n * nb + b) * bytes;
+      const double d = half_bits_to_double(static_cast<uint16_t>(blk[0] | (blk[1] << 8)));
+      for (int e = 0; e < 32; ++e) {
+        double w;
+        if (type == 2) {
+          w = d * static_cast<double>(static_cast<int8_t>(blk[2 + e]));
+        } else {
+          const uint8_t* qs = blk + (type == 0 ? 2 : 4);
+          const int c = (e < 16) ? (qs[e] & 15) : (qs[e - 16] >> 4);
+          if (type == 0) {
+            w = d * static_cast<double>(c - 8);
+          } else {
+            const double m = half_bits_to_double(static_cast<uint16_t>(blk[2] | (blk[3] << 8)));
+            w = d * static_cast<double>(c) + m;
+          }
+        }
+        W[n * K + b * 32 + e] = w;
+      }
+    }
+  }
+  return 0;
+}
+
+// Y[M,N] = X . W^T for W in ggml blocks, with A = sum |x w| (as oracle_qmm).
+int oracle_ggml_qmm(int type, const uint16_t* X, const uint8_t* blocks, int64_t M, int64_t N, int64_t K, double* Y,
+                    double* A) {
+  if (M < 0) return 2;
+  std::vector<double> W(static_cast<size_t>(N * K));
+  const int rc = oracle_ggml_dequant(type, blocks, N, K, W.data());
+  if (rc) return rc;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double y = 0.0, a = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = bf16_bits_to_double(X[m * K + k]) * W[n * K + k];
+        y += p;
+        a += std::fabs(p);
+      }
+      Y[m * N + n] = y;
+      if (A) A[m * N + n] = a;
+    }
   return 0;
 }
 

@@ -37,6 +37,8 @@ STREAM_SCALES = 1
 STREAM_X = 2
 STREAM_RESIDUAL = 3
 STREAM_ROUTING = 4
+STREAM_GGML = 5
+GGML_BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
 
 
 def rng_for(seed: int, stream: int) -> np.random.Generator:
@@ -147,6 +149,27 @@ def make_moe(seed: int, E: int, N: int, K: int, bits: int, group_size: int, T: i
     return MoeProblem(E=E, N=N, K=K, bits=bits, group_size=group_size, q=q,
                       scales=scales.reshape(E, N, -1), biases=biases.reshape(E, N, -1), x=make_x(seed, K),
                       experts=make_routing(seed, T, k, E), seed=seed)
+
+
+def make_ggml_blocks(seed: int, N: int, K: int, kind: str) -> np.ndarray:
+    """Random ggml blocks (uint8 [N * K/32, bytes]) for a [N, K] matrix: the
+    fp16 d (and Q4_1's m = fp16(-7.5 d)) drawn like the affine scales and
+    biases, every code byte uniform.  Only random draws and fp16 rounding: the
+    block layout (d first, little-endian) is the format's."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nblk = N * (K // 32)
+    rng = rng_for(seed, STREAM_GGML)
+    d_bits = f64_to_fp16_bits(0.002 * np.abs(rng.standard_normal(nblk)) + 1e-4)
+    head = [d_bits.view(np.uint8).reshape(nblk, 2)]
+    if kind == "q4_1":
+        m_bits = f64_to_fp16_bits(-7.5 * d_bits.view(np.float16).astype(np.float64))
+        head.append(m_bits.view(np.uint8).reshape(nblk, 2))
+    nq = 32 if kind == "q8_0" else 16
+    codes = rng.integers(0, 256, size=(nblk, nq), dtype=np.uint8)
+    out = np.concatenate(head + [codes], axis=1)
+    assert out.shape[1] == GGML_BLOCK_BYTES[kind]
+    return np.ascontiguousarray(out)
 
 
 def make_problem(seed: int, N: int, K: int, bits: int, group_size: int, rows: int = MAX_ROWS) -> Problem:

@@ -283,6 +283,44 @@ def pin_gather(lib):
         raise AssertionError("an expert index out of range must be an error")
 
 
+def pin_ggml(lib):
+    """ggml blocks decoded per the format: constructed blocks whose weights are
+    known by construction (nibble order, the Q4_0 offset 8, Q4_1's m, Q8_0's
+    sign), the row-major block order, and the product against the dequantized
+    matrix (one-hot X picks a column, X = 1 sums a row)."""
+    j = np.arange(16)
+    qs4 = (j | ((15 - j) << 4)).astype(np.uint8)         # element e<16: e; element 16+e: 15-e
+    codes = np.concatenate([j, 15 - j]).astype(np.float64)
+    one, half, m2, quarter = (np.array([v], dtype=np.float16).view(np.uint8) for v in (1.0, 0.5, -2.0, 0.25))
+    b40 = np.concatenate([one, qs4])
+    assert np.array_equal(lib.ggml_dequant("q4_0", b40, 1, 32)[0], codes - 8), "Q4_0"
+    b41 = np.concatenate([half, m2, qs4])
+    assert np.array_equal(lib.ggml_dequant("q4_1", b41, 1, 32)[0], 0.5 * codes - 2.0), "Q4_1"
+    q8 = (np.arange(32) * 8 - 128).astype(np.int8)
+    b80 = np.concatenate([quarter, q8.view(np.uint8)])
+    assert np.array_equal(lib.ggml_dequant("q8_0", b80, 1, 32)[0], 0.25 * q8.astype(np.float64)), "Q8_0"
+    # two rows of two blocks: block (n, b) is the (2n + b)-th, its d = 2^(2n + b)
+    blocks = []
+    for i in range(4):
+        d = np.array([2.0 ** i], dtype=np.float16).view(np.uint8)
+        blocks.append(np.concatenate([d, q8.view(np.uint8)]))
+    w = lib.ggml_dequant("q8_0", np.concatenate(blocks), 2, 64)
+    for n in range(2):
+        for b in range(2):
+            assert np.array_equal(w[n, 32 * b:32 * b + 32], 2.0 ** (2 * n + b) * q8), f"block order ({n},{b})"
+    for kind in ("q4_0", "q4_1", "q8_0"):
+        N, K = 5, 96
+        blk = synth.make_ggml_blocks(998, N, K, kind)
+        W = lib.ggml_dequant(kind, blk, N, K)
+        for k0 in (0, 15, 16, 31, 32, 95):
+            xo = np.zeros((1, K), dtype=np.uint16)
+            xo[0, k0] = BF16_ONE
+            y, _ = lib.ggml_qmm(kind, xo, blk, N)
+            assert np.array_equal(y[0], W[:, k0]), f"{kind} one-hot {k0}"
+        y, a = lib.ggml_qmm(kind, np.full((1, K), BF16_ONE, dtype=np.uint16), blk, N)
+        close(y[0], W.sum(axis=1), a[0], 1e-12, f"{kind} x = 1")
+
+
 def pin_sampled(lib):
     M, N, K, bits, g = 4, 11, 192, 2, 64
     p = synth.make_problem(995, N, K, bits, g, rows=M)
@@ -297,5 +335,5 @@ def pin_sampled(lib):
 # Pins that run fast enough for the mutation test (the exhaustive decoder pin
 # is run once against the real oracle only).
 FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
-             pin_invariants, pin_residual, pin_gather, pin_sampled)
+             pin_invariants, pin_residual, pin_gather, pin_ggml, pin_sampled)
 ALL_PINS = (pin_decoders,) + FAST_PINS

@@ -22,6 +22,9 @@ MUTANTS = [
     ("residual_dropped_from_scale", "A[i] = std::fabs(r) + A[i];", "A[i] = A[i];"),
     ("gather_rhs_ignored", "const int64_t t = lhs[i], e = rhs[i];", "const int64_t t = lhs[i], e = 0;"),
     ("gather_lhs_ignored", "const int64_t t = lhs[i], e = rhs[i];", "const int64_t t = i % T, e = rhs[i];"),
+    ("ggml_nibble_order", "(e < 16) ? (qs[e] & 15) : (qs[e - 16] >> 4)", "(e < 16) ? (qs[e] >> 4) : (qs[e - 16] & 15)"),
+    ("ggml_q4_0_offset", "w = d * static_cast<double>(c - 8);", "w = d * static_cast<double>(c);"),
+    ("ggml_q8_sign", "static_cast<int8_t>(blk[2 + e])", "static_cast<uint8_t>(blk[2 + e])"),
     ("gather_expert_stride", "const int64_t words_per_matrix = N * (K * bits / 32);",
      "const int64_t words_per_matrix = K * bits / 32;"),
 ]
