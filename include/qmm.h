@@ -127,6 +127,28 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
                               const int32_t* lhs, const int32_t* rhs, int P, int T, int E, int N, int K, int bits,
                               int group_size, void* Y, int out_dtype, int variant, int splits, void* stream);
 
+/* ggml block formats, converted on the device to the layout above.  A row of
+ * W is K/32 consecutive blocks of 32 weights; blocks of all rows are
+ * contiguous, row after row.  Byte layouts (the public ggml format; the pages
+ * name the formats, "metal : few-row MMA mat-mul and batched copies for
+ * speculative decoding", Overview):
+ *   QMM_GGML_Q4_0, 18 bytes: fp16 d; 16 bytes of 4-bit codes c, byte j holding
+ *                  weight j in its low nibble and weight j + 16 in its high
+ *                  nibble; w = d (c - 8).
+ *   QMM_GGML_Q4_1, 20 bytes: fp16 d, fp16 m, the 16 code bytes; w = d c + m.
+ *   QMM_GGML_Q8_0, 34 bytes: fp16 d, 32 signed bytes q; w = d q.                */
+typedef enum { QMM_GGML_Q4_0 = 0, QMM_GGML_Q4_1 = 1, QMM_GGML_Q8_0 = 2 } qmm_ggml_type;
+
+/* Exact conversion of a ggml matrix [N, K] (device `blocks`) into Wq
+ * [N, K*bits/32], scales and biases fp16 [N, K/32] (device, caller-owned) for
+ * qmm_small_m* with group_size 32 and bits = 4 (Q4_0, Q4_1) or 8 (Q8_0):
+ * codes unchanged (Q4) or q + 128 (Q8_0), scale d, bias -8 d (Q4_0), m (Q4_1)
+ * or -128 d (Q8_0).  Asynchronous on `stream`.  QMM_ERR_UNSUPPORTED for an
+ * unknown type, QMM_ERR_SHAPE for K not a multiple of 32, QMM_ERR_NULL /
+ * QMM_ERR_ALIGN for the outputs (Wq 4-byte, scales/biases 2-byte aligned).   */
+qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uint32_t* Wq, void* scales,
+                         void* biases, void* stream);
+
 /* Number of uint32 words of a packed [N, K] matrix: N * K * bits / 32
  * (0 if bits is unsupported or K*bits is not a multiple of 32).                 */
 size_t qmm_packed_words(int64_t N, int64_t K, int bits);

@@ -35,6 +35,7 @@ SIGNATURES = {
                                     _vp]),
     "qmm_gather_small_m": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
                                   _i32, _i32, _i32, _vp]),
+    "qmm_from_ggml": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
     "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
     "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
@@ -122,6 +123,29 @@ def repack(wq, bits: int, out=None, inverse: bool = False, stream=None):
     fn = lib().qmm_unrepack if inverse else lib().qmm_repack
     _check(fn(wq.data_ptr(), N, K, bits, out.data_ptr(), handle), "qmm_unrepack" if inverse else "qmm_repack")
     return out
+
+
+GGML_TYPES = {"q4_0": (0, 18, 4), "q4_1": (1, 20, 4), "q8_0": (2, 34, 8)}
+
+
+def from_ggml(kind: str, blocks, N: int, K: int, stream=None):
+    """ggml blocks (CUDA uint8 tensor of N*K/32 blocks) -> (wq, scales, biases)
+    in the affine layout with group size 32; returns the code width too."""
+    import torch
+
+    t, nbytes, bits = GGML_TYPES[kind]
+    if not blocks.is_cuda or not blocks.is_contiguous() or blocks.numel() != N * (K // 32) * nbytes:
+        raise ValueError("blocks must be a contiguous CUDA buffer of N*K/32 blocks")
+    dev = blocks.device
+    wq = torch.empty((N, K * bits // 32), dtype=torch.int32, device=dev)
+    s = torch.empty((N, K // 32), dtype=torch.float16, device=dev)
+    b = torch.empty((N, K // 32), dtype=torch.float16, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib().qmm_from_ggml(t, blocks.data_ptr(), N, K, wq.data_ptr(), s.data_ptr(), b.data_ptr(), handle),
+           "qmm_from_ggml")
+    return wq, s, b, bits
 
 
 def select_variant(M: int, N: int, K: int, bits: int, group_size: int):

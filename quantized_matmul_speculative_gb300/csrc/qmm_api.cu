@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/qmm.h"
@@ -484,7 +485,64 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
 
 }  // namespace
 
+namespace qmm {
+
+// ggml block -> affine layout, one thread per block of 32 weights (the block
+// layouts are described in qmm.h).  Codes keep their values (Q4) or flip the
+// sign bit (Q8_0: q + 128); the fp16 scale is d; the bias is -8 d (Q4_0), m
+// (Q4_1) or -128 d (Q8_0), products by powers of two and so exact in fp16.
+__global__ void ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk,
+                                      uint32_t* __restrict__ Wq, uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nblk) return;
+  const int nbytes = type == 0 ? 18 : type == 1 ? 20 : 34;
+  const uint8_t* blk = blocks + i * nbytes;
+  const uint16_t d = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+  const float df = __half2float(__ushort_as_half(d));
+  S[i] = d;
+  if (type == 2) {
+    for (int w = 0; w < 8; ++w) {
+      const uint8_t* q = blk + 2 + 4 * w;
+      Wq[i * 8 + w] = static_cast<uint32_t>(q[0] ^ 0x80u) | (static_cast<uint32_t>(q[1] ^ 0x80u) << 8) |
+                      (static_cast<uint32_t>(q[2] ^ 0x80u) << 16) | (static_cast<uint32_t>(q[3] ^ 0x80u) << 24);
+    }
+    B[i] = __half_as_ushort(__float2half_rn(-128.f * df));
+    return;
+  }
+  const uint8_t* qs = blk + (type == 0 ? 2 : 4);
+  for (int w = 0; w < 4; ++w) {
+    uint32_t word = 0;
+    for (int t = 0; t < 8; ++t) {
+      const int e = 8 * w + t;
+      const uint32_t c = (e < 16) ? (qs[e] & 15u) : (qs[e - 16] >> 4);
+      word |= c << (4 * t);
+    }
+    Wq[i * 4 + w] = word;
+  }
+  B[i] = (type == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : static_cast<uint16_t>(blk[2] | (blk[3] << 8));
+}
+
+}  // namespace qmm
+
 extern "C" {
+
+qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uint32_t* Wq, void* scales, void* biases,
+                         void* stream) {
+  if (type < QMM_GGML_Q4_0 || type > QMM_GGML_Q8_0) return QMM_ERR_UNSUPPORTED;
+  if (N < 0 || K < 0 || K % 32 != 0 || N > (int64_t(1) << 40) / (K + 1)) return QMM_ERR_SHAPE;
+  const int64_t nblk = N * (K / 32);
+  if (nblk == 0) return QMM_OK;
+  if (blocks == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
+  if (!aligned(Wq, 4) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
+  const int threads = 256;
+  const int64_t grid = (nblk + threads - 1) / threads;
+  if (grid > 0x7fffffff) return QMM_ERR_SHAPE;
+  qmm::ggml_to_affine_kernel<<<static_cast<unsigned int>(grid), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      type, static_cast<const uint8_t*>(blocks), nblk, Wq, static_cast<uint16_t*>(scales),
+      static_cast<uint16_t*>(biases));
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
 
 qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases, int M, int N,
                           int K, int bits, int group_size, void* Y, int out_dtype, int variant, int splits,

@@ -126,6 +126,15 @@ def test_gather_validation_before_launch(lib):
     assert rc(P=0) == 0 and rc(N=0) == 0
 
 
+def test_from_ggml_validates_on_the_host(lib):
+    fake = 0x1000
+    assert lib.qmm_from_ggml(3, fake, 4, 64, fake, fake, fake, None) == 3     # unknown type
+    assert lib.qmm_from_ggml(0, fake, 4, 48, fake, fake, fake, None) == 2     # K not a multiple of 32
+    assert lib.qmm_from_ggml(0, None, 4, 64, fake, fake, fake, None) == 1     # null input
+    assert lib.qmm_from_ggml(1, fake, 4, 64, fake + 2, fake, fake, None) == 4  # misaligned Wq
+    assert lib.qmm_from_ggml(2, None, 0, 64, None, None, None, None) == 0     # empty
+
+
 def test_variant_registry(lib):
     names = binding.variant_names()
     assert len(names) == lib.qmm_num_variants() >= 1

@@ -1,0 +1,90 @@
+"""ggml Q4_0 / Q4_1 / Q8_0 weights on the GPU: qmm_from_ggml converts the
+blocks exactly (the converted matrix dequantizes, in fp64, to exactly the
+oracle's decoding of the blocks), and the product through qmm_small_m on the
+converted weights matches the oracle's ggml product within the library's
+bound |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from qmm_harness import assert_within, sample_positions, to_f64
+from quantized_matmul_speculative_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+KINDS = ["q4_0", "q4_1", "q8_0"]
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_matmul_speculative_gb300 import build
+
+    build.build()
+    binding.lib()
+    return torch
+
+
+@pytest.fixture(autouse=True)
+def no_device_faults(torch_cuda):
+    binding.device_status(clear=True)
+    yield
+    torch_cuda.cuda.synchronize()
+    assert binding.device_status(clear=True) == 0
+
+
+def convert(torch, blocks, N, K, kind):
+    wq, s, b, bits = binding.from_ggml(kind, torch.from_numpy(blocks.reshape(-1)).cuda(), N, K)
+    torch.cuda.synchronize()
+    return wq, s, b, bits
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_conversion_is_exact(torch_cuda, kind):
+    torch = torch_cuda
+    N, K = 37, 320
+    blocks = synth.make_ggml_blocks(8400, N, K, kind)
+    wq, s, b, bits = convert(torch, blocks, N, K, kind)
+    ol = oracle.load()
+    w_conv = ol.dequant(wq.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint16),
+                        b.cpu().numpy().view(np.uint16), K, bits, 32)
+    assert np.array_equal(w_conv, ol.ggml_dequant(kind, blocks, N, K))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_ggml_product(torch_cuda, kind):
+    """Several tiles and a ragged N, M = 1..16 at the dispatcher's choice and
+    on every variant at M = 5, bf16 and fp32; then a 4096x4096 layer at
+    sampled outputs."""
+    torch = torch_cuda
+    ol = oracle.load()
+    N, K = 200, 512
+    blocks = synth.make_ggml_blocks(8500, N, K, kind)
+    wq, s, b, bits = convert(torch, blocks, N, K, kind)
+    xb = synth.make_x(8500, K)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y_ref, a_ref = ol.ggml_qmm(kind, xb, blocks, N)
+    for M in range(1, 17):
+        y = binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32, out_dtype=torch.float32)
+        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{kind} M={M}")
+    for v in range(len(binding.variant_names())):
+        for dt in (torch.float32, torch.bfloat16):
+            try:
+                y = binding.small_m(x[:5].contiguous(), wq, s, b, bits, 32, out_dtype=dt, variant=v, splits=2)
+            except binding.QmmError as e:
+                assert e.status == 3
+                continue
+            assert_within(to_f64(y), y_ref[:5], a_ref[:5], f"{kind} v{v} {dt}")
+
+    N = K = 4096
+    blocks = synth.make_ggml_blocks(8501, N, K, kind)
+    wq, s, b, bits = convert(torch, blocks, N, K, kind)
+    xb = synth.make_x(8501, K)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y_ref, a_ref = ol.ggml_qmm(kind, xb, blocks, N)
+    for M in (1, 8, 16):
+        y = to_f64(binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32))
+        ms, ns = sample_positions(M, N, 256, seed=M)
+        assert_within(y[ms, ns], y_ref[ms, ns], a_ref[ms, ns], f"{kind} 4096 M={M}")
