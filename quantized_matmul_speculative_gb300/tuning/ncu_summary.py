@@ -20,7 +20,7 @@ from pathlib import Path
 CSRC = Path(__file__).resolve().parents[1] / "csrc"
 # Sources of the TMA kernel families; a profile is valid only for the hash of these.
 KERNEL_SOURCES = ("qmm_tma.cuh", "qmm_tma_launch.cuh", "qmm_own.cuh", "qmm_own_launch.cuh", "qmm_group.cuh",
-                  "qmm_device.cuh", "qmm_tiles.h", "qmm_geometry.h")
+                  "qmm_device.cuh", "qmm_gather.cuh", "qmm_tiles.h", "qmm_geometry.h")
 
 RAW_METRICS = [
     ("gpu__time_duration.sum", "duration (serialized, cold)"),
