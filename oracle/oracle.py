@@ -68,8 +68,14 @@ class OracleLib:
         lib.oracle_gather_qmm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, i64, vp, vp]
         lib.oracle_ggml_dequant.argtypes = [c_int, vp, i64, i64, vp]
         lib.oracle_ggml_qmm.argtypes = [c_int, vp, vp, i64, i64, i64, vp, vp]
+        lib.oracle_mx_dequant.argtypes = [c_int, vp, vp, i64, i64, vp]
+        lib.oracle_mx_qmm.argtypes = [c_int, vp, vp, vp, i64, i64, i64, vp, vp]
+        for name in ("oracle_fp4_e2m1", "oracle_fp8_e4m3", "oracle_e8m0"):
+            getattr(lib, name).argtypes = [ctypes.c_uint]
+            getattr(lib, name).restype = ctypes.c_double
         for name in ("oracle_pack", "oracle_unpack", "oracle_qmm", "oracle_qmm_sampled", "oracle_dequant",
-                     "oracle_qmm_residual", "oracle_gather_qmm", "oracle_ggml_dequant", "oracle_ggml_qmm"):
+                     "oracle_qmm_residual", "oracle_gather_qmm", "oracle_ggml_dequant", "oracle_ggml_qmm",
+                     "oracle_mx_dequant", "oracle_mx_qmm"):
             getattr(lib, name).restype = c_int
         self.lib = lib
 
@@ -184,6 +190,37 @@ class OracleLib:
         rc = self.lib.oracle_ggml_qmm(t, _ptr(x), _ptr(blocks), m, n, k, _ptr(y), _ptr(a))
         if rc:
             raise OracleError(f"oracle_ggml_qmm rc={rc}")
+        return y, a
+
+    MX_FORMATS = {"mxfp4": (0, 4), "mxfp8": (1, 8)}
+
+    def mx_decoders(self):
+        """The element and scale decoders: (fp4 e2m1, fp8 e4m3, e8m0) callables."""
+        return self.lib.oracle_fp4_e2m1, self.lib.oracle_fp8_e4m3, self.lib.oracle_e8m0
+
+    def mx_dequant(self, fmt: str, wq, s, k: int) -> np.ndarray:
+        f, bits = self.MX_FORMATS[fmt]
+        wq = np.ascontiguousarray(wq, dtype=np.uint32)
+        s = np.ascontiguousarray(s, dtype=np.uint8)
+        n = wq.shape[0]
+        w = np.empty((n, k), dtype=np.float64)
+        rc = self.lib.oracle_mx_dequant(f, _ptr(wq), _ptr(s), n, k, _ptr(w))
+        if rc:
+            raise OracleError(f"oracle_mx_dequant rc={rc}")
+        return w
+
+    def mx_qmm(self, fmt: str, x_bits, wq, s):
+        f, bits = self.MX_FORMATS[fmt]
+        x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+        wq = np.ascontiguousarray(wq, dtype=np.uint32)
+        s = np.ascontiguousarray(s, dtype=np.uint8)
+        m, k = x.shape
+        n = wq.shape[0]
+        y = np.empty((m, n), dtype=np.float64)
+        a = np.empty((m, n), dtype=np.float64)
+        rc = self.lib.oracle_mx_qmm(f, _ptr(x), _ptr(wq), _ptr(s), m, n, k, _ptr(y), _ptr(a))
+        if rc:
+            raise OracleError(f"oracle_mx_qmm rc={rc}")
         return y, a
 
     def qmm_sampled(self, x_bits, wq, s_bits, b_bits, bits: int, group_size: int, ms, ns):

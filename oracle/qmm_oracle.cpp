@@ -56,6 +56,20 @@
 //      Q4_1, 20 bytes: fp16 d, fp16 m, then the 16 code bytes as in Q4_0;
 //            w = d * c + m.
 //      Q8_0, 34 bytes: fp16 d, then 32 signed bytes q; w = d * q.
+//  * Microscaling fp modes (oracle_mx_dequant, _qmm): groups of 32 codes
+//    along K share one 8-bit power-of-two scale.  The pages list the modes
+//    ("MLX quantized_matmul small-M verify kernels", facts "Fix family 1" and
+//    "qmv_wide covers affine, nvfp4, mxfp4, mxfp8"); the element and scale
+//    encodings are the OCP microscaling ones:
+//      codes  mxfp4: FP4 E2M1, 4 bits (sign, 2 exponent bits with bias 1, 1
+//             mantissa bit): 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives;
+//             packed 8 per word like the 4-bit affine codes.
+//             mxfp8: FP8 E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa
+//             bits; exponent 0 is subnormal; S.1111.111 is NaN, no infinity);
+//             packed 4 per word like the 8-bit affine codes.
+//      scale  E8M0, one byte per (row, group of 32): 2^(E - 127), 255 = NaN;
+//             stored [N, K/32].
+//    w = scale * value(code).
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
 // shapes (2-, 4- and 8-bit), closed forms (all-zero codes, one-hot X, X = 1,
@@ -300,6 +314,61 @@ int oracle_ggml_qmm(int type, const uint16_t* X, const uint8_t* blocks, int64_t 
     }
   return 0;
 }
+
+// Microscaling element and scale decoders (layouts in the header comment).
+double fp4_e2m1_to_double(unsigned c) {
+  const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  const double mag = (e == 0) ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -mag : mag;
+}
+double fp8_e4m3_to_double(unsigned c) {
+  const int sign = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+  double mag;
+  if (e == 15 && m == 7) mag = NAN;
+  else if (e == 0) mag = std::ldexp(m / 8.0, -6);
+  else mag = std::ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+double e8m0_to_double(unsigned e) { return e == 255 ? NAN : std::ldexp(1.0, static_cast<int>(e) - 127); }
+
+// format 0 = mxfp4, 1 = mxfp8.  W[N,K] in fp64; returns 2 for a bad shape or format.
+int oracle_mx_dequant(int format, const uint32_t* Wq, const uint8_t* S, int64_t N, int64_t K, double* W) {
+  if ((format != 0 && format != 1) || N < 0 || K < 0 || K % 32 != 0) return 2;
+  const int bits = format == 0 ? 4 : 8;
+  const int64_t words_per_row = K * bits / 32;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      const unsigned c = code_at(Wq, words_per_row, n, k, bits);
+      const double v = format == 0 ? fp4_e2m1_to_double(c) : fp8_e4m3_to_double(c);
+      W[n * K + k] = e8m0_to_double(S[n * (K / 32) + k / 32]) * v;
+    }
+  return 0;
+}
+
+// Y[M,N] = X . W^T for microscaled W, with A = sum |x w| (as oracle_qmm).
+int oracle_mx_qmm(int format, const uint16_t* X, const uint32_t* Wq, const uint8_t* S, int64_t M, int64_t N,
+                  int64_t K, double* Y, double* A) {
+  if (M < 0) return 2;
+  std::vector<double> W(static_cast<size_t>(N * K));
+  const int rc = oracle_mx_dequant(format, Wq, S, N, K, W.data());
+  if (rc) return rc;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double y = 0.0, a = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = bf16_bits_to_double(X[m * K + k]) * W[n * K + k];
+        y += p;
+        a += std::fabs(p);
+      }
+      Y[m * N + n] = y;
+      if (A) A[m * N + n] = a;
+    }
+  return 0;
+}
+
+double oracle_fp4_e2m1(unsigned c) { return fp4_e2m1_to_double(c & 15); }
+double oracle_fp8_e4m3(unsigned c) { return fp8_e4m3_to_double(c & 255); }
+double oracle_e8m0(unsigned e) { return e8m0_to_double(e & 255); }
 
 // The same definition evaluated only at the listed (m, n) output positions,
 // for spot checks of full-size problems.

@@ -38,6 +38,7 @@ STREAM_X = 2
 STREAM_RESIDUAL = 3
 STREAM_ROUTING = 4
 STREAM_GGML = 5
+STREAM_MX = 6
 GGML_BLOCK_BYTES = {"q4_0": 18, "q4_1": 20, "q8_0": 34}
 
 
@@ -170,6 +171,23 @@ def make_ggml_blocks(seed: int, N: int, K: int, kind: str) -> np.ndarray:
     out = np.concatenate(head + [codes], axis=1)
     assert out.shape[1] == GGML_BLOCK_BYTES[kind]
     return np.ascontiguousarray(out)
+
+
+def make_mx(seed: int, N: int, K: int, fmt: str):
+    """Microscaled weights [N, K]: codes (uint8 [N, K]) uniform over the
+    format's non-NaN codes (all 16 FP4 E2M1 codes; the 254 FP8 E4M3 codes other
+    than 0x7F and 0xFF), and E8M0 scales (uint8 [N, K/32]) uniform in
+    [127 - 12, 127], i.e. 2^-12 .. 1."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    rng = rng_for(seed, STREAM_MX)
+    if fmt == "mxfp4":
+        q = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
+    else:
+        q = rng.integers(0, 254, size=(N, K), dtype=np.uint8)
+        q = np.where(q >= 0x7F, q + 1, q).astype(np.uint8)  # skip 0x7F; 0xFF is never drawn
+    s = rng.integers(127 - 12, 128, size=(N, K // 32), dtype=np.uint8)
+    return q, s
 
 
 def make_problem(seed: int, N: int, K: int, bits: int, group_size: int, rows: int = MAX_ROWS) -> Problem:

@@ -321,6 +321,48 @@ def pin_ggml(lib):
         close(y[0], W.sum(axis=1), a[0], 1e-12, f"{kind} x = 1")
 
 
+def pin_mx(lib):
+    """Microscaling decoders against the OCP tables and independent rational
+    formulas; the product against exact rational sums; one-hot X."""
+    f4, f8, e8 = lib.mx_decoders()
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        ref = e2m1[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert f4(c) == ref and np.signbit(f4(c)) == bool(c & 8), f"e2m1 {c}"
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            assert np.isnan(f8(c)), f"e4m3 {c:#x} is NaN"
+            continue
+        mag = Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        assert Fraction(f8(c)) == (-mag if s else mag), f"e4m3 {c:#x}"
+    assert f8(0x7E) == 448.0 and f8(0x01) == 2.0 ** -9 and f8(0x08) == 2.0 ** -6 and f8(0x38) == 1.0
+    assert e8(127) == 1.0 and e8(0) == 2.0 ** -127 and e8(254) == 2.0 ** 127 and np.isnan(e8(255))
+    for fmt, bits in (("mxfp4", 4), ("mxfp8", 8)):
+        M, N, K = 2, 3, 64
+        q, sc = synth.make_mx(999, N, K, fmt)
+        wq = lib.pack(q, bits)
+        xb = synth.make_x(999, K, rows=M)
+        y, a = lib.mx_qmm(fmt, xb, wq, sc)
+        dec = f4 if fmt == "mxfp4" else f8
+        xs = [[frac_bf16(v) for v in row] for row in xb]
+        for m in range(M):
+            for n in range(N):
+                acc, mag = Fraction(0), Fraction(0)
+                for k in range(K):
+                    t = xs[m][k] * Fraction(2) ** (int(sc[n, k // 32]) - 127) * Fraction(dec(int(q[n, k])))
+                    acc += t
+                    mag += abs(t)
+                assert abs(Fraction(float(y[m, n])) - acc) <= Fraction(1, 10**12) * mag, f"{fmt} y[{m},{n}]"
+                assert abs(Fraction(float(a[m, n])) - mag) <= Fraction(1, 10**12) * mag, f"{fmt} a[{m},{n}]"
+        W = lib.mx_dequant(fmt, wq, sc, K)
+        for k0 in (0, 31, 32, 63):
+            xo = np.zeros((1, K), dtype=np.uint16)
+            xo[0, k0] = BF16_ONE
+            yo, _ = lib.mx_qmm(fmt, xo, wq, sc)
+            assert np.array_equal(yo[0], W[:, k0]), f"{fmt} one-hot {k0}"
+
+
 def pin_sampled(lib):
     M, N, K, bits, g = 4, 11, 192, 2, 64
     p = synth.make_problem(995, N, K, bits, g, rows=M)
@@ -335,5 +377,5 @@ def pin_sampled(lib):
 # Pins that run fast enough for the mutation test (the exhaustive decoder pin
 # is run once against the real oracle only).
 FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
-             pin_invariants, pin_residual, pin_gather, pin_ggml, pin_sampled)
+             pin_invariants, pin_residual, pin_gather, pin_ggml, pin_mx, pin_sampled)
 ALL_PINS = (pin_decoders,) + FAST_PINS

@@ -25,6 +25,9 @@ MUTANTS = [
     ("ggml_nibble_order", "(e < 16) ? (qs[e] & 15) : (qs[e - 16] >> 4)", "(e < 16) ? (qs[e] >> 4) : (qs[e - 16] & 15)"),
     ("ggml_q4_0_offset", "w = d * static_cast<double>(c - 8);", "w = d * static_cast<double>(c);"),
     ("ggml_q8_sign", "static_cast<int8_t>(blk[2 + e])", "static_cast<uint8_t>(blk[2 + e])"),
+    ("e2m1_exponent_bias", "std::ldexp(1.0 + 0.5 * m, e - 1)", "std::ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("e4m3_subnormal", "std::ldexp(m / 8.0, -6)", "std::ldexp(m / 8.0, -7)"),
+    ("e8m0_bias", "static_cast<int>(e) - 127", "static_cast<int>(e) - 128"),
     ("gather_expert_stride", "const int64_t words_per_matrix = N * (K * bits / 32);",
      "const int64_t words_per_matrix = K * bits / 32;"),
 ]
