@@ -402,6 +402,41 @@ def moe_report(torch, dev, stream, peak):
                     "bytes = distinct experts of the routing x expert bytes"}
 
 
+def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):
+    """Microscaling fp modes on the 5120x5120 layer (mma family): us per call
+    and GB/s over codes + one E8M0 byte per 32 weights; same chains as
+    configs_report."""
+    from quantized_matmul_speculative_gb300 import binding
+
+    N = K = 5120
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    handle = stream.cuda_stream
+    out = []
+    for fmt, bits in (("mxfp4", 4), ("mxfp8", 8)):
+        q, sc = synth.make_mx(9000 + bits, N, K, fmt)
+        cb = N * K * bits // 8 + N * K // 32
+        ncopy = max(2, int(np.ceil(4 * l2 / cb)) + 1)
+        wq = torch.from_numpy(binding.pack(q, bits).view(np.int32)).to(dev)
+        s8 = torch.from_numpy(sc).to(dev)
+        copies = [(wq, s8)] + [(wq.clone(), s8.clone()) for _ in range(ncopy - 1)]
+        x = torch.from_numpy(synth.make_x(9000, K).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty((16, N), dtype=torch.bfloat16, device=dev)
+        f = binding.MX_FORMATS[fmt][0]
+        for M in ms:
+            def capture(i, M=M):
+                wq_d, s_d = copies[i % ncopy]
+                rc = binding.lib().qmm_small_m_mx(x.data_ptr(), wq_d.data_ptr(), s_d.data_ptr(), M, N, K, f,
+                                                  y.data_ptr(), binding.OUT_BF16, -1, -1, handle)
+                assert rc == 0, rc
+            us = graph_us_per_call(torch, stream, capture, 64)
+            gbs = cb / (us * 1e-6) / 1e9
+            out.append({"format": fmt, "M": M, "bytes_per_call": cb, "us_per_call": round(us, 3),
+                        "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)})
+        del copies, wq, s8
+        torch.cuda.empty_cache()
+    return {"shape": "5120x5120", "per_m": out, "note": "mma family; E8M0 scale per 32 codes, no bias"}
+
+
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):
     """bf16 dense torch.matmul (cuBLAS) on the 5120x5120 layer, for scale only:
     the dense bf16 weights are 4x the bytes of the 4-bit ones."""
@@ -603,6 +638,7 @@ def run_ours(args, world, rank, local):
         extra["controls"] = dense_control(torch, dev, stream)
         extra["residual"] = residual_report(torch, dev, stream)
         extra["moe"] = moe_report(torch, dev, stream, peak)
+        extra["mx"] = mx_report(torch, dev, stream, peak)
     kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
                       "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
 

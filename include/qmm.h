@@ -149,6 +149,21 @@ typedef enum { QMM_GGML_Q4_0 = 0, QMM_GGML_Q4_1 = 1, QMM_GGML_Q8_0 = 2 } qmm_ggm
 qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uint32_t* Wq, void* scales,
                          void* biases, void* stream);
 
+/* Microscaling fp modes: Y = X . W^T with w = 2^(E - 127) * value(code), one
+ * E8M0 scale byte E per (row, group of 32 along K), scales uint8 [N, K/32];
+ * no bias.  Codes are packed as above: QMM_MXFP4 = FP4 E2M1 (4 bits: sign, 2
+ * exponent bits with bias 1, 1 mantissa bit; values 0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6 and negatives), QMM_MXFP8 = FP8 E4M3 (8 bits: sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, exponent 0 subnormal).  Encodings: the OCP
+ * microscaling format; source of the modes: "MLX quantized_matmul small-M
+ * verify kernels", facts "Fix family 1" / "qmv_wide covers affine, nvfp4,
+ * mxfp4, mxfp8".  Runs on the "mma" variants (variant -1: the first).
+ * K must be a multiple of 32.  An E4M3 NaN code (0x7F, 0xFF) reads as +-480,
+ * an E8M0 255 as NaN.  Errors as qmm_small_m_ex.                               */
+typedef enum { QMM_MXFP4 = 0, QMM_MXFP8 = 1 } qmm_mx_format;
+qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scales, int M, int N, int K, int format,
+                          void* Y, int out_dtype, int variant, int splits, void* stream);
+
 /* Number of uint32 words of a packed [N, K] matrix: N * K * bits / 32
  * (0 if bits is unsupported or K*bits is not a multiple of 32).                 */
 size_t qmm_packed_words(int64_t N, int64_t K, int bits);

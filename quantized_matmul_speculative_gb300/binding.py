@@ -36,6 +36,7 @@ SIGNATURES = {
     "qmm_gather_small_m": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
                                   _i32, _i32, _i32, _vp]),
     "qmm_from_ggml": (_i32, [_i32, _vp, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "qmm_small_m_mx": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "qmm_packed_words": (ctypes.c_size_t, [_i64, _i64, _i32]),
     "qmm_pack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
     "qmm_unpack": (_i32, [_vp, _i64, _i64, _i32, _vp]),
@@ -126,6 +127,31 @@ def repack(wq, bits: int, out=None, inverse: bool = False, stream=None):
 
 
 GGML_TYPES = {"q4_0": (0, 18, 4), "q4_1": (1, 20, 4), "q8_0": (2, 34, 8)}
+MX_FORMATS = {"mxfp4": (0, 4), "mxfp8": (1, 8)}
+
+
+def small_m_mx(x, wq, scales, fmt: str, out=None, out_dtype=None, variant: int = -1, splits: int = -1,
+               stream=None):
+    """Y = X . W^T for microscaled W: ``wq`` int32 [N, K*bits/32] (E2M1 or
+    E4M3 codes), ``scales`` uint8 [N, K/32] (E8M0); CUDA tensors."""
+    import torch
+
+    f, bits = MX_FORMATS[fmt]
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    M, K = x.shape
+    N = wq.shape[0]
+    if wq.shape[1] * 32 != K * bits or tuple(scales.shape) != (N, K // 32) or scales.dtype != torch.uint8:
+        raise ValueError("wq / scales do not match K and the format")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib().qmm_small_m_mx(x.data_ptr(), wq.data_ptr(), scales.data_ptr(), M, N, K, f, out.data_ptr(),
+                                OUT_F32 if out_dtype == torch.float32 else OUT_BF16, variant, splits, handle),
+           "qmm_small_m_mx")
+    return out
 
 
 def from_ggml(kind: str, blocks, N: int, K: int, stream=None):

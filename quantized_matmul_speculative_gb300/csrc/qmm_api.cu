@@ -34,6 +34,11 @@ extern template cudaError_t launch_mma_bg<2, 128>(const CallArgs&, const Variant
 extern template cudaError_t launch_mma_bg<8, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<8, 64>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_bg<8, 128>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template <int FMT>
+cudaError_t launch_mma_mx(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+
 template <int BITS, int GS>
 cudaError_t launch_tma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_tma_bg<4, 32>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
@@ -647,6 +652,48 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
     std::fprintf(stderr, "qmm gather: P=%d T=%d E=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", P, T, E, N, K, bits,
                  group_size, d.name, s);
   const cudaError_t e = launch_mma(a, d, s, st);
+  return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+}
+
+qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scales, int M, int N, int K, int format,
+                          void* Y, int out_dtype, int variant, int splits, void* stream) {
+  if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
+  if (format != QMM_MXFP4 && format != QMM_MXFP8) return QMM_ERR_UNSUPPORTED;
+  if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
+  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family != kFamilyMma))
+    return QMM_ERR_UNSUPPORTED;
+  if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
+  if (K % 32 != 0) return QMM_ERR_SHAPE;
+  if (M == 0 || N == 0) return QMM_OK;
+  const size_t esize = out_dtype == QMM_OUT_F32 ? 4 : 2;
+  if (Y == nullptr) return QMM_ERR_NULL;
+  if (!aligned(Y, esize)) return QMM_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(M) * static_cast<size_t>(N) * esize, st);
+    return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+  }
+  if (X == nullptr || Wq == nullptr || scales == nullptr) return QMM_ERR_NULL;
+  if (!aligned(X, 16) || !aligned(Wq, 16)) return QMM_ERR_ALIGN;
+  CallArgs a;
+  a.X = static_cast<const uint16_t*>(X);
+  a.Wq = Wq;
+  a.S = nullptr;
+  a.B = nullptr;
+  a.S8 = scales;
+  a.Y = Y;
+  a.R = nullptr;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = format == QMM_MXFP4 ? 4 : 8;
+  a.gs = 32;
+  a.out_f32 = out_dtype == QMM_OUT_F32;
+  const VariantDesc& d = kVariants[variant < 0 ? 0 : variant];
+  const int s = splits > 0 ? splits : rule_splits(d, N, K, 32);
+  if (env_flag("QMM_LOG"))
+    std::fprintf(stderr, "qmm mx: M=%d N=%d K=%d format=%d -> %s splits=%d\n", M, N, K, format, d.name, s);
+  const cudaError_t e = (format == QMM_MXFP4) ? launch_mma_mx<0>(a, d, s, st) : launch_mma_mx<1>(a, d, s, st);
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
 }
 

@@ -69,6 +69,35 @@ __device__ __forceinline__ uint32_t bf16x2_times16(uint32_t v) {
 }
 
 // ---------------------------------------------------------------------------
+// Microscaling codes.  An FP4 E2M1 code s|e|m placed at bf16 bits 15 | 7-8 |
+// 6 (sign, low exponent bits, top mantissa bit) is exactly 2^-126 times its
+// value (exponent 0 lands on the bf16 subnormal m * 2^-127), and an FP8 E4M3
+// code s|eeee|mmm placed at bits 15 | 7-10 | 4-6 is exactly 2^-120 times its
+// value; one bf16x2 FMA by 2^126 or 2^120 then gives the value exactly.  A
+// word's pair i holds codes i and i + 16/b, as in unpack_pair.  (An E4M3 NaN
+// code is not propagated: it reads as 480.)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, uint32_t f2) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(f2), "r"(0x80008000u));
+  return r;
+}
+__device__ __forceinline__ uint32_t unpack_fp4_pair(uint32_t w, int i) {
+  const uint32_t u = w >> (4 * i);
+  const uint32_t v = ((u & 0x00070007u) << 6) | ((u & 0x00080008u) << 12);
+  return bf16x2_scale(v, 0x7E807E80u);  // 2^126
+}
+__device__ __forceinline__ uint32_t unpack_fp8_pair(uint32_t w, int i) {
+  const uint32_t u = w >> (8 * i);
+  const uint32_t v = ((u & 0x007F007Fu) << 4) | ((u & 0x00800080u) << 8);
+  return bf16x2_scale(v, 0x7B807B80u);  // 2^120
+}
+// E8M0 scale byte -> fp32: 2^(E - 127); 0 is the fp32 subnormal 2^-127, 255 NaN.
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
+  return __uint_as_float(e == 0 ? 0x00400000u : e == 255 ? 0x7FC00000u : (e << 23));
+}
+
+// ---------------------------------------------------------------------------
 // Code unpack.  A b-bit code c is OR-ed into the low mantissa bits of the bf16
 // pattern 0x4300 (= 128.0, whose unit in the last place is 1), which gives the
 // bf16 value 128 + c exactly.  One 32-bit word yields two such bf16 values per

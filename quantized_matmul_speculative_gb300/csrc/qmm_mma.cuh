@@ -68,6 +68,7 @@ struct MmaParams {
   const int32_t* lhs;
   const int32_t* rhs;
   int P, T, E;
+  const uint8_t* S8;   // microscaled weights: E8M0 scales [N, K/32] (then S, B are unused)
   int tiles;           // CTA row tiles per matrix
   int64_t w_stride;    // packed words per matrix of the stack
   int64_t m_stride;    // scales (and biases) per matrix of the stack
@@ -112,10 +113,15 @@ struct MmaSmem {
   }
 };
 
-template <int BITS, int GS, int NB, int R, int WN, int WK, bool E8>
+template <int BITS, int GS, int NB, int R, int WN, int WK, int CODES>
 __global__ void __launch_bounds__(32 * WN * WK, (32 * WN * WK >= 256) ? 2 : 4)
 qmm_mma_kernel(const MmaParams p) {
   using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
+  constexpr bool E8 = CODES == kCodesAffine8;
+  constexpr bool MX = CODES == kCodesMx4 || CODES == kCodesMx8;
+  static_assert(!MX || GS == 32, "microscaling groups are 32 codes");
+  static_assert(CODES != kCodesMx4 || BITS == 4, "mxfp4 codes are 4 bits");
+  static_assert(CODES != kCodesMx8 || BITS == 8, "mxfp8 codes are 8 bits");
   extern __shared__ __align__(16) unsigned char smem[];
   const MmaSmem<C> L(p.chunk);
   uint16_t* Xs = reinterpret_cast<uint16_t*>(smem);
@@ -166,8 +172,12 @@ qmm_mma_kernel(const MmaParams p) {
     for (int r = tid; r < C::NT; r += C::THREADS) {
       const int n = tile * C::NT + r;
       if (n < p.N && g_lo < g_hi) {
-        prefetch_l2(Sg + static_cast<int64_t>(n) * p.G + g_lo);
-        prefetch_l2(Bg + static_cast<int64_t>(n) * p.G + g_lo);
+        if constexpr (MX) {
+          prefetch_l2(p.S8 + static_cast<int64_t>(n) * p.G + g_lo);
+        } else {
+          prefetch_l2(Sg + static_cast<int64_t>(n) * p.G + g_lo);
+          prefetch_l2(Bg + static_cast<int64_t>(n) * p.G + g_lo);
+        }
       }
     }
   }
@@ -237,6 +247,15 @@ qmm_mma_kernel(const MmaParams p) {
           d2[0] = make_uint2(prmt_lo(v.x, v.y), prmt_lo(h0, h1));
           d2[1] = make_uint2(prmt_hi(v.x, v.y), prmt_hi(h0, h1));
         }
+      } else if constexpr (BITS == 8) {
+        // native 8-bit codes: word wc holds codes 4wc..4wc+3; stage (x0, x2), (x1, x3)
+#pragma unroll
+        for (int wc = 0; wc < C::GW; ++wc) {
+          uint2 v = make_uint2(0, 0);
+          if (m < M) v = ld_nc_v2(p.X + xrow(m) * p.K + k0 + 4 * wc);
+          s += bf16_lo(v.x) + bf16_hi(v.x) + bf16_lo(v.y) + bf16_hi(v.y);
+          *reinterpret_cast<uint2*>(dst + wc * C::VPW) = make_uint2(prmt_lo(v.x, v.y), prmt_hi(v.x, v.y));
+        }
       } else {
 #pragma unroll
         for (int wc = 0; wc < C::GW; ++wc) {
@@ -272,9 +291,13 @@ qmm_mma_kernel(const MmaParams p) {
       float2 sb = make_float2(0.f, 0.f);
       if (n < p.N) {
         const int64_t idx = static_cast<int64_t>(n) * p.G + c0 + jl;
-        const float sc = __half2float(__ushort_as_half(Sg[idx]));
-        const float bi = __half2float(__ushort_as_half(Bg[idx]));
-        sb = make_float2(sc, fmaf(E8 ? -2176.f : -128.f, sc, bi));
+        if constexpr (MX) {
+          sb = make_float2(e8m0_to_float(p.S8[idx]), 0.f);  // no bias, no offset to remove
+        } else {
+          const float sc = __half2float(__ushort_as_half(Sg[idx]));
+          const float bi = __half2float(__ushort_as_half(Bg[idx]));
+          sb = make_float2(sc, fmaf(E8 ? -2176.f : -128.f, sc, bi));
+        }
       }
       meta[rl * p.chunk + jl] = sb;
     }
@@ -324,10 +347,15 @@ qmm_mma_kernel(const MmaParams p) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           uint32_t a[4];
-          a[0] = unpack_pair<BITS>(wcur[r][0][lwi], 2 * s);
-          a[1] = unpack_pair<BITS>(wcur[r][1][lwi], 2 * s);
-          a[2] = unpack_pair<BITS>(wcur[r][0][lwi], 2 * s + 1);
-          a[3] = unpack_pair<BITS>(wcur[r][1][lwi], 2 * s + 1);
+          auto unpack = [&](uint32_t w, int i) {
+            if constexpr (CODES == kCodesMx4) return unpack_fp4_pair(w, i);
+            else if constexpr (CODES == kCodesMx8) return unpack_fp8_pair(w, i);
+            else return unpack_pair<BITS>(w, i);
+          };
+          a[0] = unpack(wcur[r][0][lwi], 2 * s);
+          a[1] = unpack(wcur[r][1][lwi], 2 * s);
+          a[2] = unpack(wcur[r][0][lwi], 2 * s + 1);
+          a[3] = unpack(wcur[r][1][lwi], 2 * s + 1);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) mma_bf16_16816(tmp[r][nb], a, xb[nb].x, xb[nb].y);
         }

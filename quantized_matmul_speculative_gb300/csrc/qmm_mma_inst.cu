@@ -29,4 +29,10 @@ template unsigned int read_device_status<QMM_BITS, QMM_GS>(int);
 template cudaError_t launch_mma_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template cudaError_t launch_tma_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 template cudaError_t launch_own_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+#if QMM_BITS == 4 && QMM_GS == 32
+template cudaError_t launch_mma_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+#endif
+#if QMM_BITS == 8 && QMM_GS == 32
+template cudaError_t launch_mma_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+#endif
 }

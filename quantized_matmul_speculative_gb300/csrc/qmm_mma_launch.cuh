@@ -12,7 +12,7 @@ namespace qmm {
 // Shared memory one CTA may use; keeps two 256-thread CTAs resident per SM.
 constexpr int kMmaSmemBudget = 100 * 1024;
 
-template <int BITS, int GS, int NB, int R, int WN, int WK, bool E8>
+template <int BITS, int GS, int NB, int R, int WN, int WK, int CODES>
 cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) {
   using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
   MmaParams p;
@@ -28,6 +28,7 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   p.out_f32 = a.out_f32;
   p.G = a.K / GS;
   p.gpc = (p.G + splits - 1) / splits;
+  p.S8 = a.S8;
   p.lhs = a.lhs;
   p.rhs = a.rhs;
   p.P = a.P;
@@ -47,7 +48,7 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   if (p.chunk < 1) p.chunk = 1;
   const int smem = MmaSmem<C>(p.chunk).total;
 
-  auto kern = qmm_mma_kernel<BITS, GS, NB, R, WN, WK, E8>;
+  auto kern = qmm_mma_kernel<BITS, GS, NB, R, WN, WK, CODES>;
   static std::mutex mu;
   static int smem_set = 0;
   static bool nonportable_set = false;
@@ -85,11 +86,11 @@ cudaError_t launch_mma_impl(const CallArgs& a, int splits, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int BITS, int GS, int NB, bool E8>
+template <int BITS, int GS, int NB, int CODES>
 cudaError_t launch_mma_tile(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
 #define QMM_TRY_TILE(r, wn, wk)                                                     \
   if (d.R == (r) && d.WN == (wn) && d.WK == (wk))                                   \
-    return launch_mma_impl<BITS, GS, NB, r, wn, wk, E8>(a, splits, stream);
+    return launch_mma_impl<BITS, GS, NB, r, wn, wk, CODES>(a, splits, stream);
   QMM_MMA_TILES(QMM_TRY_TILE)
 #undef QMM_TRY_TILE
   return cudaErrorInvalidValue;
@@ -100,12 +101,21 @@ template <int BITS, int GS>
 cudaError_t launch_mma_bg(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
   if constexpr (BITS == 8) {
     const CallArgs v = as_virtual_nibbles(a);
-    if (v.M <= 8) return launch_mma_tile<4, 2 * GS, 1, true>(v, d, splits, stream);
-    return launch_mma_tile<4, 2 * GS, 2, true>(v, d, splits, stream);
+    if (v.M <= 8) return launch_mma_tile<4, 2 * GS, 1, kCodesAffine8>(v, d, splits, stream);
+    return launch_mma_tile<4, 2 * GS, 2, kCodesAffine8>(v, d, splits, stream);
   } else {
-    if (a.M <= 8) return launch_mma_tile<BITS, GS, 1, false>(a, d, splits, stream);
-    return launch_mma_tile<BITS, GS, 2, false>(a, d, splits, stream);
+    if (a.M <= 8) return launch_mma_tile<BITS, GS, 1, kCodesAffine>(a, d, splits, stream);
+    return launch_mma_tile<BITS, GS, 2, kCodesAffine>(a, d, splits, stream);
   }
+}
+
+// Microscaled weights: FMT 0 = mxfp4 (4-bit codes), 1 = mxfp8 (8-bit codes); groups of 32.
+template <int FMT>
+cudaError_t launch_mma_mx(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
+  constexpr int BITS = FMT == 0 ? 4 : 8;
+  constexpr int CODES = FMT == 0 ? kCodesMx4 : kCodesMx8;
+  if (a.M <= 8) return launch_mma_tile<BITS, 32, 1, CODES>(a, d, splits, stream);
+  return launch_mma_tile<BITS, 32, 2, CODES>(a, d, splits, stream);
 }
 
 }  // namespace qmm

@@ -135,6 +135,27 @@ def test_from_ggml_validates_on_the_host(lib):
     assert lib.qmm_from_ggml(2, None, 0, 64, None, None, None, None) == 0     # empty
 
 
+def test_mx_validation_before_launch(lib):
+    call = lib.qmm_small_m_mx
+    p = 0x10000
+    # (X, Wq, scales, M, N, K, format, Y, out, variant, splits, stream)
+    base = [p, p, p, 4, 64, 256, 0, p, 0, -1, -1, None]
+    pos = {"X": 0, "Wq": 1, "S": 2, "M": 3, "N": 4, "K": 5, "fmt": 6, "Y": 7, "out": 8, "variant": 9, "splits": 10}
+
+    def rc(**kw):
+        a = list(base)
+        for k, v in kw.items():
+            a[pos[k]] = v
+        return call(*a)
+
+    assert rc(M=17) == 2 and rc(K=48) == 2 and rc(fmt=2) == 3 and rc(out=3) == 3 and rc(splits=0) == 3
+    tma = next(i for i, n in enumerate(binding.variant_names()) if n.startswith("tma"))
+    assert rc(variant=tma) == 3
+    assert rc(X=None) == 1 and rc(S=None) == 1 and rc(Y=None) == 1
+    assert rc(X=p + 2) == 4 and rc(Wq=p + 4) == 4
+    assert rc(M=0) == 0 and rc(N=0) == 0
+
+
 def test_variant_registry(lib):
     names = binding.variant_names()
     assert len(names) == lib.qmm_num_variants() >= 1

@@ -1,0 +1,100 @@
+"""GPU parity of the microscaling fp modes (qmm_small_m_mx): mxfp4 (E2M1) and
+mxfp8 (E4M3) codes with E8M0 scales per 32, against the oracle, with the
+library's bound |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5 on the fp32 output.
+
+The bf16 output is checked as the exact round-to-nearest-even of the fp32
+output of the same variant: with E4M3's heavy-tailed weights one product can
+dominate a row (|y| close to sum |x w|), and half a bf16 ulp (up to 2^-8 |y|)
+then exceeds 2e-3 * sum |x w| by itself."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from qmm_harness import assert_within, sample_positions, to_f64
+from quantized_matmul_speculative_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [("mxfp4", 4), ("mxfp8", 8)]
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_matmul_speculative_gb300 import build
+
+    build.build()
+    binding.lib()
+    return torch
+
+
+@pytest.fixture(autouse=True)
+def no_device_faults(torch_cuda):
+    binding.device_status(clear=True)
+    yield
+    torch_cuda.cuda.synchronize()
+    assert binding.device_status(clear=True) == 0
+
+
+def upload(torch, q, sc, bits):
+    wq = torch.from_numpy(binding.pack(q, bits).view(np.int32)).cuda()
+    return wq, torch.from_numpy(sc).cuda()
+
+
+@pytest.mark.parametrize("fmt,bits", FORMATS)
+def test_every_code_value(torch_cuda, fmt, bits):
+    """Each code of the format in turn (one-hot X picks it out): the GPU
+    reproduces the oracle's decoding of every E2M1 / non-NaN E4M3 code."""
+    torch = torch_cuda
+    ncode = 16 if bits == 4 else 256
+    codes = [c for c in range(ncode) if not (bits == 8 and (c & 0x7F) == 0x7F)]
+    N, K = len(codes), 64
+    q = np.zeros((N, K), dtype=np.uint8)
+    q[:, 5] = codes
+    sc = np.full((N, K // 32), 127, dtype=np.uint8)
+    wq, s = upload(torch, q, sc, bits)
+    xb = np.zeros((1, K), dtype=np.uint16)
+    xb[0, 5] = 0x3F80  # bf16 1.0
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y = to_f64(binding.small_m_mx(x, wq, s, fmt, out_dtype=torch.float32))
+    ref, _ = oracle.load().mx_qmm(fmt, xb, binding.pack(q, bits), sc)
+    assert np.array_equal(y[0], ref[0])
+
+
+@pytest.mark.parametrize("fmt,bits", FORMATS)
+def test_mx_products(torch_cuda, fmt, bits):
+    """Several tiles and a ragged N, M = 1..16, every mma variant with split 1
+    and 2, bf16 and fp32; then a 4096x4096 layer at sampled outputs."""
+    torch = torch_cuda
+    ol = oracle.load()
+    N, K = 200, 512
+    q, sc = synth.make_mx(8600, N, K, fmt)
+    wq, s = upload(torch, q, sc, bits)
+    xb = synth.make_x(8600, K)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y_ref, a_ref = ol.mx_qmm(fmt, xb, binding.pack(q, bits), sc)
+    for M in range(1, 17):
+        y = binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.float32)
+        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{fmt} M={M}")
+    mma = [i for i, n in enumerate(binding.variant_names()) if n.startswith("mma")]
+    for v in mma:
+        for sp in (1, 2):
+            for M in (3, 12):
+                y32 = binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.float32, variant=v,
+                                         splits=sp)
+                assert_within(to_f64(y32), y_ref[:M], a_ref[:M], f"{fmt} v{v} s{sp} M={M}")
+                y16 = binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.bfloat16, variant=v,
+                                         splits=sp)
+                assert torch.equal(y16, y32.to(torch.bfloat16)), f"{fmt} v{v} s{sp} M={M}: bf16 = RNE(fp32)"
+    N = K = 4096
+    q, sc = synth.make_mx(8601, N, K, fmt)
+    wq, s = upload(torch, q, sc, bits)
+    xb = synth.make_x(8601, K)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y_ref, a_ref = ol.mx_qmm(fmt, xb, binding.pack(q, bits), sc)
+    for M in (1, 8, 16):
+        y = to_f64(binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.float32))
+        ms, ns = sample_positions(M, N, 256, seed=M)
+        assert_within(y[ms, ns], y_ref[ms, ns], a_ref[ms, ns], f"{fmt} 4096 M={M}")
