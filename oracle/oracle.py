@@ -192,7 +192,7 @@ class OracleLib:
             raise OracleError(f"oracle_ggml_qmm rc={rc}")
         return y, a
 
-    MX_FORMATS = {"mxfp4": (0, 4), "mxfp8": (1, 8)}
+    MX_FORMATS = {"mxfp4": (0, 4), "mxfp8": (1, 8), "nvfp4": (2, 4)}
 
     def mx_decoders(self):
         """The element and scale decoders: (fp4 e2m1, fp8 e4m3, e8m0) callables."""

@@ -69,6 +69,9 @@
 //             packed 4 per word like the 8-bit affine codes.
 //      scale  E8M0, one byte per (row, group of 32): 2^(E - 127), 255 = NaN;
 //             stored [N, K/32].
+//    nvfp4: FP4 E2M1 codes as mxfp4, groups of 16 with an FP8 E4M3 scale
+//    byte each, stored [N, K/16] (a per-tensor scale, where a model has one,
+//    is left to the caller).
 //    w = scale * value(code).
 //
 // Parity pins (tests/test_oracle_pins.py): exact rational brute force on tiny
@@ -331,16 +334,19 @@ double fp8_e4m3_to_double(unsigned c) {
 }
 double e8m0_to_double(unsigned e) { return e == 255 ? NAN : std::ldexp(1.0, static_cast<int>(e) - 127); }
 
-// format 0 = mxfp4, 1 = mxfp8.  W[N,K] in fp64; returns 2 for a bad shape or format.
+// format 0 = mxfp4, 1 = mxfp8, 2 = nvfp4.  W[N,K] in fp64; returns 2 for a
+// bad shape or format.
 int oracle_mx_dequant(int format, const uint32_t* Wq, const uint8_t* S, int64_t N, int64_t K, double* W) {
-  if ((format != 0 && format != 1) || N < 0 || K < 0 || K % 32 != 0) return 2;
-  const int bits = format == 0 ? 4 : 8;
+  if (format < 0 || format > 2 || N < 0 || K < 0 || K % 32 != 0) return 2;
+  const int bits = format == 1 ? 8 : 4;
+  const int64_t g = format == 2 ? 16 : 32;
   const int64_t words_per_row = K * bits / 32;
   for (int64_t n = 0; n < N; ++n)
     for (int64_t k = 0; k < K; ++k) {
       const unsigned c = code_at(Wq, words_per_row, n, k, bits);
-      const double v = format == 0 ? fp4_e2m1_to_double(c) : fp8_e4m3_to_double(c);
-      W[n * K + k] = e8m0_to_double(S[n * (K / 32) + k / 32]) * v;
+      const double v = format == 1 ? fp8_e4m3_to_double(c) : fp4_e2m1_to_double(c);
+      const unsigned sb = S[n * (K / g) + k / g];
+      W[n * K + k] = (format == 2 ? fp8_e4m3_to_double(sb) : e8m0_to_double(sb)) * v;
     }
   return 0;
 }

@@ -176,17 +176,21 @@ def make_ggml_blocks(seed: int, N: int, K: int, kind: str) -> np.ndarray:
 def make_mx(seed: int, N: int, K: int, fmt: str):
     """Microscaled weights [N, K]: codes (uint8 [N, K]) uniform over the
     format's non-NaN codes (all 16 FP4 E2M1 codes; the 254 FP8 E4M3 codes other
-    than 0x7F and 0xFF), and E8M0 scales (uint8 [N, K/32]) uniform in
-    [127 - 12, 127], i.e. 2^-12 .. 1."""
+    than 0x7F and 0xFF), and scale bytes: E8M0 (uint8 [N, K/32]) uniform in
+    [127 - 12, 127], i.e. 2^-12 .. 1; for nvfp4, E4M3 (uint8 [N, K/16]) with a
+    positive normal exponent field in 1..7 and any mantissa, i.e. 2^-6 .. 1.875."""
     if K % 32:
         raise ValueError("K must be a multiple of 32")
     rng = rng_for(seed, STREAM_MX)
-    if fmt == "mxfp4":
+    if fmt in ("mxfp4", "nvfp4"):
         q = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
     else:
         q = rng.integers(0, 254, size=(N, K), dtype=np.uint8)
         q = np.where(q >= 0x7F, q + 1, q).astype(np.uint8)  # skip 0x7F; 0xFF is never drawn
-    s = rng.integers(127 - 12, 128, size=(N, K // 32), dtype=np.uint8)
+    if fmt == "nvfp4":
+        s = (rng.integers(1, 8, size=(N, K // 16)) << 3 | rng.integers(0, 8, size=(N, K // 16))).astype(np.uint8)
+    else:
+        s = rng.integers(127 - 12, 128, size=(N, K // 32), dtype=np.uint8)
     return q, s
 
 

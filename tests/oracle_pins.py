@@ -338,19 +338,27 @@ def pin_mx(lib):
         assert Fraction(f8(c)) == (-mag if s else mag), f"e4m3 {c:#x}"
     assert f8(0x7E) == 448.0 and f8(0x01) == 2.0 ** -9 and f8(0x08) == 2.0 ** -6 and f8(0x38) == 1.0
     assert e8(127) == 1.0 and e8(0) == 2.0 ** -127 and e8(254) == 2.0 ** 127 and np.isnan(e8(255))
-    for fmt, bits in (("mxfp4", 4), ("mxfp8", 8)):
+    for fmt, bits in (("mxfp4", 4), ("mxfp8", 8), ("nvfp4", 4)):
         M, N, K = 2, 3, 64
         q, sc = synth.make_mx(999, N, K, fmt)
         wq = lib.pack(q, bits)
         xb = synth.make_x(999, K, rows=M)
         y, a = lib.mx_qmm(fmt, xb, wq, sc)
-        dec = f4 if fmt == "mxfp4" else f8
+        dec = f8 if fmt == "mxfp8" else f4
+        g = 16 if fmt == "nvfp4" else 32
+
+        def scale(n, k):
+            b = int(sc[n, k // g])
+            if fmt != "nvfp4":
+                return Fraction(2) ** (b - 127)
+            return (1 + Fraction(b & 7, 8)) * Fraction(2) ** (((b >> 3) & 15) - 7)  # normal, positive by draw
+
         xs = [[frac_bf16(v) for v in row] for row in xb]
         for m in range(M):
             for n in range(N):
                 acc, mag = Fraction(0), Fraction(0)
                 for k in range(K):
-                    t = xs[m][k] * Fraction(2) ** (int(sc[n, k // 32]) - 127) * Fraction(dec(int(q[n, k])))
+                    t = xs[m][k] * scale(n, k) * Fraction(dec(int(q[n, k])))
                     acc += t
                     mag += abs(t)
                 assert abs(Fraction(float(y[m, n])) - acc) <= Fraction(1, 10**12) * mag, f"{fmt} y[{m},{n}]"
