@@ -404,17 +404,16 @@ def moe_report(torch, dev, stream, peak):
 
 def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):
     """Microscaling fp modes on the 5120x5120 layer (mma family): us per call
-    and GB/s over codes + one E8M0 byte per 32 weights; same chains as
-    configs_report."""
+    and GB/s over codes + scale bytes; same chains as configs_report."""
     from quantized_matmul_speculative_gb300 import binding
 
     N = K = 5120
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     handle = stream.cuda_stream
     out = []
-    for fmt, bits in (("mxfp4", 4), ("mxfp8", 8)):
-        q, sc = synth.make_mx(9000 + bits, N, K, fmt)
-        cb = N * K * bits // 8 + N * K // 32
+    for fmt, bits, g in (("mxfp4", 4, 32), ("mxfp8", 8, 32), ("nvfp4", 4, 16)):
+        q, sc = synth.make_mx(9000 + bits + g, N, K, fmt)
+        cb = N * K * bits // 8 + N * K // g
         ncopy = max(2, int(np.ceil(4 * l2 / cb)) + 1)
         wq = torch.from_numpy(binding.pack(q, bits).view(np.int32)).to(dev)
         s8 = torch.from_numpy(sc).to(dev)
@@ -434,7 +433,8 @@ def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):
                         "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)})
         del copies, wq, s8
         torch.cuda.empty_cache()
-    return {"shape": "5120x5120", "per_m": out, "note": "mma family; E8M0 scale per 32 codes, no bias"}
+    return {"shape": "5120x5120", "per_m": out,
+            "note": "mma family; one scale byte per 32 codes (E8M0) or per 16 (nvfp4: E4M3), no bias"}
 
 
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):

@@ -158,9 +158,12 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
  * microscaling format; source of the modes: "MLX quantized_matmul small-M
  * verify kernels", facts "Fix family 1" / "qmv_wide covers affine, nvfp4,
  * mxfp4, mxfp8".  Runs on the "mma" variants (variant -1: the first).
+ * QMM_NVFP4: FP4 E2M1 codes with one FP8 E4M3 scale byte per group of 16,
+ * scales uint8 [N, K/16] (a per-tensor scale, where a model has one, is left
+ * to the caller).
  * K must be a multiple of 32.  An E4M3 NaN code (0x7F, 0xFF) reads as +-480,
  * an E8M0 255 as NaN.  Errors as qmm_small_m_ex.                               */
-typedef enum { QMM_MXFP4 = 0, QMM_MXFP8 = 1 } qmm_mx_format;
+typedef enum { QMM_MXFP4 = 0, QMM_MXFP8 = 1, QMM_NVFP4 = 2 } qmm_mx_format;
 qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scales, int M, int N, int K, int format,
                           void* Y, int out_dtype, int variant, int splits, void* stream);
 

@@ -127,21 +127,22 @@ def repack(wq, bits: int, out=None, inverse: bool = False, stream=None):
 
 
 GGML_TYPES = {"q4_0": (0, 18, 4), "q4_1": (1, 20, 4), "q8_0": (2, 34, 8)}
-MX_FORMATS = {"mxfp4": (0, 4), "mxfp8": (1, 8)}
+MX_FORMATS = {"mxfp4": (0, 4, 32), "mxfp8": (1, 8, 32), "nvfp4": (2, 4, 16)}
 
 
 def small_m_mx(x, wq, scales, fmt: str, out=None, out_dtype=None, variant: int = -1, splits: int = -1,
                stream=None):
     """Y = X . W^T for microscaled W: ``wq`` int32 [N, K*bits/32] (E2M1 or
-    E4M3 codes), ``scales`` uint8 [N, K/32] (E8M0); CUDA tensors."""
+    E4M3 codes), ``scales`` uint8 [N, K/32] (E8M0) or [N, K/16] (nvfp4: E4M3);
+    CUDA tensors."""
     import torch
 
-    f, bits = MX_FORMATS[fmt]
+    f, bits, g = MX_FORMATS[fmt]
     if out_dtype is None:
         out_dtype = out.dtype if out is not None else torch.bfloat16
     M, K = x.shape
     N = wq.shape[0]
-    if wq.shape[1] * 32 != K * bits or tuple(scales.shape) != (N, K // 32) or scales.dtype != torch.uint8:
+    if wq.shape[1] * 32 != K * bits or tuple(scales.shape) != (N, K // g) or scales.dtype != torch.uint8:
         raise ValueError("wq / scales do not match K and the format")
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=x.device)

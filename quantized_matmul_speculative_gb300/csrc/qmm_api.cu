@@ -38,6 +38,7 @@ template <int FMT>
 cudaError_t launch_mma_mx(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+extern template cudaError_t launch_mma_mx<2>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 
 template <int BITS, int GS>
 cudaError_t launch_tma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
@@ -658,7 +659,7 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
 qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scales, int M, int N, int K, int format,
                           void* Y, int out_dtype, int variant, int splits, void* stream) {
   if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
-  if (format != QMM_MXFP4 && format != QMM_MXFP8) return QMM_ERR_UNSUPPORTED;
+  if (format != QMM_MXFP4 && format != QMM_MXFP8 && format != QMM_NVFP4) return QMM_ERR_UNSUPPORTED;
   if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
   if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family != kFamilyMma))
     return QMM_ERR_UNSUPPORTED;
@@ -686,14 +687,16 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   a.M = M;
   a.N = N;
   a.K = K;
-  a.bits = format == QMM_MXFP4 ? 4 : 8;
-  a.gs = 32;
+  a.bits = format == QMM_MXFP8 ? 8 : 4;
+  a.gs = format == QMM_NVFP4 ? 16 : 32;
   a.out_f32 = out_dtype == QMM_OUT_F32;
   const VariantDesc& d = kVariants[variant < 0 ? 0 : variant];
-  const int s = splits > 0 ? splits : rule_splits(d, N, K, 32);
+  const int s = splits > 0 ? splits : rule_splits(d, N, K, a.gs);
   if (env_flag("QMM_LOG"))
     std::fprintf(stderr, "qmm mx: M=%d N=%d K=%d format=%d -> %s splits=%d\n", M, N, K, format, d.name, s);
-  const cudaError_t e = (format == QMM_MXFP4) ? launch_mma_mx<0>(a, d, s, st) : launch_mma_mx<1>(a, d, s, st);
+  const cudaError_t e = (format == QMM_MXFP4)   ? launch_mma_mx<0>(a, d, s, st)
+                        : (format == QMM_MXFP8) ? launch_mma_mx<1>(a, d, s, st)
+                                                : launch_mma_mx<2>(a, d, s, st);
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
 }
 

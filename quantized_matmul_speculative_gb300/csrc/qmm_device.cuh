@@ -92,6 +92,11 @@ __device__ __forceinline__ uint32_t unpack_fp8_pair(uint32_t w, int i) {
   const uint32_t v = ((u & 0x007F007Fu) << 4) | ((u & 0x00800080u) << 8);
   return bf16x2_scale(v, 0x7B807B80u);  // 2^120
 }
+// E4M3 byte -> fp32, exactly (same placement as unpack_fp8_pair; NaN codes read as 480).
+__device__ __forceinline__ float e4m3_to_float(uint32_t c) {
+  const uint32_t v = ((c & 0x7Fu) << 4) | ((c & 0x80u) << 8);
+  return __uint_as_float(v << 16) * 1.329227995784915872903807060280344576e36f;  // 2^120
+}
 // E8M0 scale byte -> fp32: 2^(E - 127); 0 is the fp32 subnormal 2^-127, 255 NaN.
 __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
   return __uint_as_float(e == 0 ? 0x00400000u : e == 255 ? 0x7FC00000u : (e << 23));

@@ -22,7 +22,8 @@ struct CallArgs {
   const int32_t* lhs = nullptr;
   const int32_t* rhs = nullptr;
   int P = 0, T = 0, E = 0;
-  // Microscaled weights (S8 non-null): E8M0 scales [N, K/32], no biases.
+  // Microscaled weights (S8 non-null): one scale byte per group (E8M0 per
+  // 32, or E4M3 per 16 for nvfp4), no biases.
   const uint8_t* S8 = nullptr;
 };
 
@@ -31,6 +32,7 @@ constexpr int kCodesAffine = 0;   // b-bit affine codes read natively (2 or 4 bi
 constexpr int kCodesAffine8 = 1;  // 8-bit affine codes as virtual 4-bit codes
 constexpr int kCodesMx4 = 2;      // mxfp4: FP4 E2M1 codes, E8M0 scale per 32
 constexpr int kCodesMx8 = 3;      // mxfp8: FP8 E4M3 codes, E8M0 scale per 32
+constexpr int kCodesNv4 = 4;      // nvfp4: FP4 E2M1 codes, E4M3 scale per 16
 
 // Most entries of a gathered call: the kernels scan the index lists with one
 // entry per thread.

@@ -118,9 +118,10 @@ __global__ void __launch_bounds__(32 * WN * WK, (32 * WN * WK >= 256) ? 2 : 4)
 qmm_mma_kernel(const MmaParams p) {
   using C = MmaCfg<BITS, GS, NB, R, WN, WK>;
   constexpr bool E8 = CODES == kCodesAffine8;
-  constexpr bool MX = CODES == kCodesMx4 || CODES == kCodesMx8;
-  static_assert(!MX || GS == 32, "microscaling groups are 32 codes");
+  constexpr bool MX = CODES == kCodesMx4 || CODES == kCodesMx8 || CODES == kCodesNv4;
+  static_assert(!MX || GS == (CODES == kCodesNv4 ? 16 : 32), "microscaling groups are 32 codes (nvfp4: 16)");
   static_assert(CODES != kCodesMx4 || BITS == 4, "mxfp4 codes are 4 bits");
+  static_assert(CODES != kCodesNv4 || BITS == 4, "nvfp4 codes are 4 bits");
   static_assert(CODES != kCodesMx8 || BITS == 8, "mxfp8 codes are 8 bits");
   extern __shared__ __align__(16) unsigned char smem[];
   const MmaSmem<C> L(p.chunk);
@@ -292,7 +293,8 @@ qmm_mma_kernel(const MmaParams p) {
       if (n < p.N) {
         const int64_t idx = static_cast<int64_t>(n) * p.G + c0 + jl;
         if constexpr (MX) {
-          sb = make_float2(e8m0_to_float(p.S8[idx]), 0.f);  // no bias, no offset to remove
+          const uint32_t b = p.S8[idx];  // no bias, no offset to remove
+          sb = make_float2(CODES == kCodesNv4 ? e4m3_to_float(b) : e8m0_to_float(b), 0.f);
         } else {
           const float sc = __half2float(__ushort_as_half(Sg[idx]));
           const float bi = __half2float(__ushort_as_half(Bg[idx]));
@@ -348,7 +350,7 @@ qmm_mma_kernel(const MmaParams p) {
         for (int r = 0; r < R; ++r) {
           uint32_t a[4];
           auto unpack = [&](uint32_t w, int i) {
-            if constexpr (CODES == kCodesMx4) return unpack_fp4_pair(w, i);
+            if constexpr (CODES == kCodesMx4 || CODES == kCodesNv4) return unpack_fp4_pair(w, i);
             else if constexpr (CODES == kCodesMx8) return unpack_fp8_pair(w, i);
             else return unpack_pair<BITS>(w, i);
           };

@@ -109,13 +109,15 @@ cudaError_t launch_mma_bg(const CallArgs& a, const VariantDesc& d, int splits, c
   }
 }
 
-// Microscaled weights: FMT 0 = mxfp4 (4-bit codes), 1 = mxfp8 (8-bit codes); groups of 32.
+// Microscaled weights: FMT 0 = mxfp4 (4-bit codes, groups of 32), 1 = mxfp8
+// (8-bit codes, groups of 32), 2 = nvfp4 (4-bit codes, groups of 16).
 template <int FMT>
 cudaError_t launch_mma_mx(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream) {
-  constexpr int BITS = FMT == 0 ? 4 : 8;
-  constexpr int CODES = FMT == 0 ? kCodesMx4 : kCodesMx8;
-  if (a.M <= 8) return launch_mma_tile<BITS, 32, 1, CODES>(a, d, splits, stream);
-  return launch_mma_tile<BITS, 32, 2, CODES>(a, d, splits, stream);
+  constexpr int BITS = FMT == 1 ? 8 : 4;
+  constexpr int GS = FMT == 2 ? 16 : 32;
+  constexpr int CODES = FMT == 0 ? kCodesMx4 : FMT == 1 ? kCodesMx8 : kCodesNv4;
+  if (a.M <= 8) return launch_mma_tile<BITS, GS, 1, CODES>(a, d, splits, stream);
+  return launch_mma_tile<BITS, GS, 2, CODES>(a, d, splits, stream);
 }
 
 }  // namespace qmm

@@ -148,7 +148,7 @@ def test_mx_validation_before_launch(lib):
             a[pos[k]] = v
         return call(*a)
 
-    assert rc(M=17) == 2 and rc(K=48) == 2 and rc(fmt=2) == 3 and rc(out=3) == 3 and rc(splits=0) == 3
+    assert rc(M=17) == 2 and rc(K=48) == 2 and rc(fmt=3) == 3 and rc(out=3) == 3 and rc(splits=0) == 3
     tma = next(i for i, n in enumerate(binding.variant_names()) if n.startswith("tma"))
     assert rc(variant=tma) == 3
     assert rc(X=None) == 1 and rc(S=None) == 1 and rc(Y=None) == 1

@@ -1,5 +1,6 @@
 """GPU parity of the microscaling fp modes (qmm_small_m_mx): mxfp4 (E2M1) and
-mxfp8 (E4M3) codes with E8M0 scales per 32, against the oracle, with the
+mxfp8 (E4M3) codes with E8M0 scales per 32, and nvfp4 (E2M1 codes with E4M3
+scales per 16), against the oracle, with the
 library's bound |y - y_ref| <= 2e-3 * sum_k |x w| + 1e-5 on the fp32 output.
 
 The bf16 output is checked as the exact round-to-nearest-even of the fp32
@@ -15,7 +16,7 @@ from quantized_matmul_speculative_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
 
-FORMATS = [("mxfp4", 4), ("mxfp8", 8)]
+FORMATS = [("mxfp4", 4), ("mxfp8", 8), ("nvfp4", 4)]
 
 
 @pytest.fixture(scope="module")
@@ -53,7 +54,8 @@ def test_every_code_value(torch_cuda, fmt, bits):
     N, K = len(codes), 64
     q = np.zeros((N, K), dtype=np.uint8)
     q[:, 5] = codes
-    sc = np.full((N, K // 32), 127, dtype=np.uint8)
+    # scale 1: E8M0 127, or E4M3 0x38 for nvfp4 (groups of 16)
+    sc = np.full((N, K // 16), 0x38, dtype=np.uint8) if fmt == "nvfp4" else np.full((N, K // 32), 127, dtype=np.uint8)
     wq, s = upload(torch, q, sc, bits)
     xb = np.zeros((1, K), dtype=np.uint16)
     xb[0, 5] = 0x3F80  # bf16 1.0
