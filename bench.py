@@ -391,15 +391,18 @@ def moe_report(torch, dev, stream, peak):
         us = graph_us_per_call(torch, stream, capture, 32)
         tma = binding.variant_names().index("tma_w8_2cta")
         us_tma = graph_us_per_call(torch, stream, lambda i, T=T, lhs=lhs, rhs=rhs: capture(i, T, lhs, rhs, tma), 32)
+        mma = binding.variant_names().index("mma_r2_wn2_wk4")
+        us_mma = graph_us_per_call(torch, stream, lambda i, T=T, lhs=lhs, rhs=rhs: capture(i, T, lhs, rhs, mma), 32)
         gbs = ub / (us * 1e-6) / 1e9
         res.append({"T": T, "entries": T * w.k, "experts_in_union": int(len(np.unique(experts))),
                     "union_bytes": ub, "us_per_call": round(us, 3), "union_gbs": round(gbs, 1),
-                    "frac_hbm": round(gbs / peak, 4), "us_per_call_tma_w8_2cta": round(us_tma, 3)})
+                    "frac_hbm": round(gbs / peak, 4), "us_per_call_tma_w8_2cta": round(us_tma, 3),
+                    "us_per_call_mma_r2_wn2_wk4": round(us_mma, 3)})
     del copies, wq, sc, bi
     torch.cuda.empty_cache()
     return {"workload": w.name, "per_t": res,
-            "note": "gathered form at the library's choice (mma family), and forced onto tma_w8_2cta; "
-                    "bytes = distinct experts of the routing x expert bytes"}
+            "note": "gathered form at the library's choice (warp-owned family), and forced onto tma_w8_2cta "
+                    "and mma_r2_wn2_wk4; bytes = distinct experts of the routing x expert bytes"}
 
 
 def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):

@@ -112,12 +112,13 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
  * Source: "MLX quantized_matmul small-M verify kernels", the open question on
  * "dense and MoE (gather_qmm) verify" and the "expert-union cost per verify
  * row".
- * variant = -1 runs the "mma" variants, which take each expert's own entries.
- * A forced "tma" variant (T <= 16, a shape the tma variants take, P at most
- * its thread count) computes all T rows against each expert of the union and
- * writes the rows the entries name (then any number of entries per expert is
- * fine); otherwise it returns QMM_ERR_UNSUPPORTED, as does a "tma_own"
- * variant.  splits as in qmm_small_m_ex.  The index
+ * variant = -1: with T <= 16 and a shape the "tma_own" variants take (see
+ * qmm_small_m_ex), the warp-owned kernel computes all T rows against each
+ * expert of the union and writes the rows the entries name (then any number
+ * of entries per expert is fine); otherwise the "mma" variants take each
+ * expert's own entries.  A forced "tma" or "tma_own" variant takes the first
+ * way (QMM_ERR_UNSUPPORTED if it cannot), a forced "mma" variant the second.
+ * splits as in qmm_small_m_ex.  The index
  * lists are read on the device, after the wait for the preceding kernel: an
  * index out of range, or (mma variants) too many entries for one expert,
  * leaves the affected rows of Y unwritten and sets bit 3 of

@@ -97,6 +97,7 @@ const VariantDesc kVariants[] = {
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
+constexpr int kDefaultGatherOwn = 13;  // tma_own_w8_d2_2cta: the gathered form's default
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 constexpr int kMaxSplits = 16;
 
@@ -570,8 +571,7 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   if (bits != 2 && bits != 4 && bits != 8) return QMM_ERR_UNSUPPORTED;
   if (group_size != 32 && group_size != 64 && group_size != 128) return QMM_ERR_UNSUPPORTED;
   if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
-  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family == kFamilyOwn))
-    return QMM_ERR_UNSUPPORTED;
+  if (variant < -1 || variant >= kNumVariants) return QMM_ERR_UNSUPPORTED;
   if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
   if (K % group_size != 0) return QMM_ERR_SHAPE;
   if (P == 0 || N == 0) return QMM_OK;
@@ -609,13 +609,59 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   a.T = T;
   a.E = E;
   const int fv = forced_variant();
-  if (variant < 0 && fv >= 0 && kVariants[fv].family != kFamilyOwn) variant = fv;
+  if (variant < 0 && fv >= 0) variant = fv;
+
+  // The warp-owned family (the default when it can plan the shape, measured
+  // about twice as fast as the mma family on the 128-expert top-8 stack):
+  // every token row against each expert of the union, like the tma variants,
+  // with per-warp copy rings and no reduction rounds.
+  const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
+  if (variant < 0 && T <= 16) {
+    CallArgs ao = a;
+    ao.M = T;
+    const VariantDesc& dd = kVariants[kDefaultGatherOwn];
+    for (int cc : {4, 2, 1, 8}) {
+      if (splits > 0 && cc != splits) continue;
+      const cudaError_t pe = launch_own(ao, dd, cc, st, true);
+      if (pe == cudaErrorNotSupported) continue;
+      if (pe != cudaSuccess) return fail_cuda(pe);
+      if (env_flag("QMM_LOG"))
+        std::fprintf(stderr, "qmm gather: P=%d T=%d E=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", P, T, E, N, K,
+                     bits, group_size, dd.name, cc);
+      const cudaError_t e = launch_own(ao, dd, cc, st, false);
+      return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+    }
+  }
+  if (own_forced) {
+    if (T > 16) return QMM_ERR_UNSUPPORTED;
+    CallArgs ao = a;
+    ao.M = T;
+    const VariantDesc& dd = kVariants[variant];
+    int c = splits;
+    if (c < 0) {
+      for (int cc : {4, 2, 1, 8}) {
+        const cudaError_t pe = launch_own(ao, dd, cc, st, true);
+        if (pe == cudaSuccess) {
+          c = cc;
+          break;
+        }
+        if (pe != cudaErrorNotSupported) return fail_cuda(pe);
+      }
+      if (c < 0) return QMM_ERR_UNSUPPORTED;
+    }
+    if (env_flag("QMM_LOG"))
+      std::fprintf(stderr, "qmm gather: P=%d T=%d E=%d N=%d K=%d bits=%d g=%d -> %s splits=%d\n", P, T, E, N, K,
+                   bits, group_size, dd.name, c);
+    const cudaError_t e = launch_own(ao, dd, c, st, false);
+    if (e == cudaSuccess) return QMM_OK;
+    if (e == cudaErrorNotSupported) return QMM_ERR_UNSUPPORTED;
+    return fail_cuda(e);
+  }
 
   // A tma variant (forced) computes every token row against each expert of
-  // the union (T <= 16 rows staged once) under the TMA shape rules; the mma
-  // family (the default: measured faster on the 128-expert top-8 stack, where
-  // the tma kernel needs many reduction rounds) takes each expert's own
-  // entries (at most 8 or 16 of them).
+  // the union (T <= 16 rows staged once) under the TMA shape rules (slower on
+  // large unions: many reduction rounds); the mma family (the fallback) takes
+  // each expert's own entries (at most 8 or 16 of them).
   const bool tma_forced = variant >= 0 && kVariants[variant].family == kFamilyTma;
   if (T <= 16 && tma_forced) {
     CallArgs at = a;

@@ -30,6 +30,7 @@
 #include <cuda_runtime.h>
 
 #include "qmm_device.cuh"
+#include "qmm_gather.cuh"
 #include "qmm_geometry.h"
 #include "qmm_group.cuh"
 
@@ -51,6 +52,16 @@ struct OwnParams {
   int maxw;                     // receive slots per (tile, CTA): most warps that meet one tile
   int owned_max;                // most tiles one CTA owns
   int out_f32;
+  // Gathered form (GATHER kernels): as in the TMA family, the tensor maps span
+  // the stack (E*N rows), tile tau is row tile tau % tpe of the expert in
+  // union slot tau / tpe, every token row (M = T) is computed against it and
+  // the entries naming (token, expert) receive the result; `tiles` is the
+  // largest union's tile count and the kernel splits the actual union's.
+  const int32_t* lhs;
+  const int32_t* rhs;
+  int P, E;
+  int tpe;                      // 16-row tiles per matrix of the stack
+  int gather_off;               // byte offset of the gathered lists' shared scratch
 };
 
 // Shared-memory layout of one CTA (bytes).  Only the M staged activation
@@ -78,7 +89,7 @@ struct OwnLayout {
 
 // With W <= 8 two CTAs must fit an SM (the "2cta" shared-memory budget and
 // the next call's CTAs under PDL), which caps registers at 128 per thread.
-template <int BITS, int GS, int NB, int W, int D, bool E8>
+template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
 __global__ void __launch_bounds__(32 * W, (W <= 8) ? 2 : 1)
 qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const OwnParams p) {
@@ -100,14 +111,50 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   uint16_t* Xs = reinterpret_cast<uint16_t*>(smem + L.x_off);
   float* xsum = reinterpret_cast<float*>(smem + L.xs_off);
 
-  const int t_begin = static_cast<int>((static_cast<int64_t>(p.tiles) * q) / p.ncl);
-  const int t_end = static_cast<int>((static_cast<int64_t>(p.tiles) * (q + 1)) / p.ncl);
+  // Gathered form: the index lists may be the previous call's output, so they
+  // (and every weight copy, whose expert they decide) wait for it.
+  GatherLists gl;
+  int tiles = p.tiles;
+  if constexpr (GATHER) {
+    griddep_wait();
+    gl = gather_lists<32 * W>(p.lhs, p.rhs, p.P, p.M, p.E, reinterpret_cast<int*>(smem + p.gather_off));
+    tiles = gl.u * p.tpe;
+  }
+  auto tile_row = [&](int tau) {  // first row of tile tau in the weight tensor maps
+    if constexpr (GATHER) return gl.expert[tau / p.tpe] * p.N + (tau % p.tpe) * 16;
+    else return tau * 16;
+  };
+  auto tile_n0 = [&](int tau) {  // first output column of tile tau
+    if constexpr (GATHER) return (tau % p.tpe) * 16;
+    else return tau * 16;
+  };
+  const int t_begin = static_cast<int>((static_cast<int64_t>(tiles) * q) / p.ncl);
+  const int t_end = static_cast<int>((static_cast<int64_t>(tiles) * (q + 1)) / p.ncl);
   const int nt = t_end - t_begin;
   const int g0 = rank * p.gp;
   const int U = nt * p.kp;
   const int ua = own_unit_begin(warp, U, W);
   const int nu = own_unit_begin(warp + 1, U, W) - ua;
   const int owned = (nt > rank) ? (nt - rank + csize - 1) / csize : 0;
+  // Receive slots per (owned tile, CTA): the plan's, or (gathered: the tile
+  // count is only known here) the most contributors any of this cluster's
+  // tiles has, found by each warp over its lanes.  The planner reserved room
+  // for every possible tile count.
+  int maxw = p.maxw;
+  if constexpr (GATHER) {
+    int mw = 1;
+    for (int i = lane; i < nt; i += 32) {
+      int sl;
+      const int n = own_contributors(i, p.kp, nt * p.kp, W, -1, &sl);
+      mw = n > mw ? n : mw;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const int other = __shfl_xor_sync(0xffffffffu, mw, o);
+      mw = other > mw ? other : mw;
+    }
+    maxw = mw;
+  }
   const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + 2 * 16 * p.mbw * 2);
 
   QMM_TRACE_POINT(0);
@@ -140,7 +187,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       ip = 0;
       ++ii;
     }
-    const int n0 = (t_begin + i) * 16;
+    const int n0 = tile_row(t_begin + i);
     const int gs0 = g0 + part * p.gq;
     const int s = qq % D;
     const uint32_t dst = sbase + static_cast<uint32_t>(L.ring_off + (warp * D + s) * L.stage_bytes);
@@ -172,9 +219,10 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const uint16_t* xrow = GM::x_row(Xs, L.rsx, ln);
   const int gpb = p.bw / GW;  // groups per weight box
 
-  // Y[m, n] for this lane's fragment of tile i.
+  // Y[m, n] for this lane's fragment of tile i (gathered: one store per entry
+  // naming (token m, the tile's expert)).
   auto write_y = [&](int i, const float (&v)[NB][4]) {
-    const int n_lo = (t_begin + i) * 16 + ln.g;
+    const int n_lo = tile_n0(t_begin + i) + ln.g;
     const int n_hi = n_lo + 8;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -183,8 +231,14 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
         const int m = 8 * nb + 2 * ln.t + (e & 1);
         const int n = (e < 2) ? n_lo : n_hi;
         if (m < p.M && n < p.N) {
-          const int64_t off = static_cast<int64_t>(m) * p.N + n;
-          store_y(p.Y, p.R, off, v[nb][e], p.out_f32);
+          if constexpr (GATHER) {
+            const int sl = (t_begin + i) / p.tpe;
+            for (int j = gl.start[sl]; j < gl.start[sl + 1]; ++j)
+              if (gl.token[j] == m)
+                store_y(p.Y, nullptr, static_cast<int64_t>(gl.entry[j]) * p.N + n, v[nb][e], p.out_f32);
+          } else {
+            store_y(p.Y, p.R, static_cast<int64_t>(m) * p.N + n, v[nb][e], p.out_f32);
+          }
         }
       }
     }
@@ -202,7 +256,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     }
     const uint32_t owner = static_cast<uint32_t>(i % csize);
     const int o = i / csize;
-    const uint32_t dst = sbase + static_cast<uint32_t>(L.recv_off + ((o * csize + rank) * p.maxw + slot) * L.slot_bytes +
+    const uint32_t dst = sbase + static_cast<uint32_t>(L.recv_off + ((o * csize + rank) * maxw + slot) * L.slot_bytes +
                                                         lane * 16 * NB);
     const uint32_t rbar = mapa_shared(recv_bar(o), owner);
 #pragma unroll
@@ -315,7 +369,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     if (csize == 1 && n == 1) continue;  // written by its only contributor
     mbar_wait(recv_bar(o), 0, kStatusTimeoutFull);
     const float* rv = reinterpret_cast<const float*>(smem + L.recv_off) +
-                      static_cast<int64_t>(o * csize * p.maxw) * (L.slot_bytes / 4) + lane * 4 * NB;
+                      static_cast<int64_t>(o * csize * maxw) * (L.slot_bytes / 4) + lane * 4 * NB;
     float v[NB][4];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
@@ -323,7 +377,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       for (int e = 0; e < 4; ++e) v[nb][e] = 0.f;
     for (int r2 = 0; r2 < csize; ++r2)
       for (int k = 0; k < n; ++k) {
-        const float* src = rv + (r2 * p.maxw + k) * (L.slot_bytes / 4);
+        const float* src = rv + (r2 * maxw + k) * (L.slot_bytes / 4);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           const float4 x4 = *reinterpret_cast<const float4*>(src + 4 * nb);

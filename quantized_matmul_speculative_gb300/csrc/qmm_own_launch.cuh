@@ -18,7 +18,7 @@ namespace qmm {
 // Plan one call: K-piece, parts per tile, box widths, clusters, receive
 // slots and shared memory.  Returns cudaErrorNotSupported (and launches
 // nothing) when (W, D, csize, CTAs per SM) cannot run the shape.
-template <int BITS, int GS, int NB, int W, int D, bool E8>
+template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
 cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, OwnParams* p, int* smem, int* budget) {
   constexpr int GW = GroupMath<BITS, GS, NB>::GW;
   constexpr int MP = 8 * NB;
@@ -35,8 +35,20 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   p->gp = G / csize;
   p->gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p->gp) - 1) / static_cast<unsigned long long>(p->gp);
   p->tiles = (a.N + 15) / 16;
+  p->tpe = p->tiles;
+  p->lhs = a.lhs;
+  p->rhs = a.rhs;
+  p->P = a.P;
+  p->E = a.E;
+  p->gather_off = 0;
+  if constexpr (GATHER) {
+    // every entry scanned by one thread; tiles of the largest possible union
+    if (a.P > 32 * W || a.P > kMaxGatherEntries || a.E < 1) return cudaErrorNotSupported;
+    p->tiles = (a.E < a.P ? a.E : a.P) * p->tpe;
+  }
+  const int gather_bytes = GATHER ? kGatherSmemInts * 4 : 0;
 
-  auto kern = qmm_own_kernel<BITS, GS, NB, W, D, E8>;
+  auto kern = qmm_own_kernel<BITS, GS, NB, W, D, E8, GATHER>;
   int sm_bytes = 0, optin = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
@@ -99,7 +111,29 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     }
     const int owned_max = (nt_max + csize - 1) / csize;
     const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, mbw, owned_max, csize, maxw, a.M);
-    if (L.total > *budget) continue;
+    int total = L.total;
+    if constexpr (GATHER) {
+      // The union decides the tile count nt <= nt_max in the kernel, which
+      // then strides the receive slots by maxw(nt): reserve the largest
+      // owned(nt) * maxw(nt) (owned by CTA rank 0, the most).
+      int64_t slots = 0;
+      for (int nt = 1; nt <= nt_max; ++nt) {
+        int mw = 1;
+        for (int i = 0; i < nt; ++i) {
+          int sl;
+          const int n = own_contributors(i, kp, nt * kp, W, -1, &sl);
+          mw = n > mw ? n : mw;
+        }
+        const int64_t need = static_cast<int64_t>((nt + csize - 1) / csize) * mw;
+        slots = need > slots ? need : slots;
+      }
+      total = L.recv_off + static_cast<int>(slots) * csize * L.slot_bytes;
+      const int x_end = L.x_off + MP * L.rsx * 2;
+      if (total < x_end) total = x_end;
+      total = ((total + 15) & ~15) + gather_bytes;
+      maxw = 0;  // the kernel finds its own
+    }
+    if (total > *budget) continue;
     p->kp = kp;
     p->gq = gq;
     p->bw = bw;
@@ -107,26 +141,28 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     p->mbw = mbw;
     p->maxw = maxw;
     p->owned_max = owned_max;
-    *smem = L.total;
+    p->gather_off = GATHER ? total - gather_bytes : 0;
+    *smem = total;
     found = true;
     if (nt_min * kp >= 2 * W) break;
   }
   return found ? cudaSuccess : cudaErrorNotSupported;
 }
 
-template <int BITS, int GS, int NB, int W, int D, bool E8>
+template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
 cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int wave, cudaStream_t stream,
                             bool plan_only) {
   OwnParams p;
   int smem = 0, budget = 0;
-  const cudaError_t pe = own_plan<BITS, GS, NB, W, D, E8>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
+  const cudaError_t pe = own_plan<BITS, GS, NB, W, D, E8, GATHER>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
+  const int64_t map_rows = GATHER ? static_cast<int64_t>(a.E) * a.N : a.N;  // gathered: the whole stack
   if (pe != cudaSuccess || plan_only) return pe;
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorUnknown;
   CUtensorMap tmap, tmap_s, tmap_b;
   {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(a.K) * BITS / 32, static_cast<cuuint64_t>(map_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(a.K) * BITS / 8};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.bw), 16u};
     const cuuint32_t estride[2] = {1u, 1u};
@@ -137,7 +173,7 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
   }
   const int G = a.K / GS;
   for (int arr = 0; arr < 2; ++arr) {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(a.N)};
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(map_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
     const cuuint32_t estride[2] = {1u, 1u};
@@ -169,14 +205,16 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D, E8>, tmap, tmap_s, tmap_b, p);
+  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D, E8, GATHER>, tmap, tmap_s, tmap_b, p);
 }
 
 template <int BITS, int GS, int NB, bool E8>
 cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
 #define QMM_TRY_OWN(w, dd)                 \
   if (d.WN == (w) && d.R == (dd))          \
-    return launch_own_impl<BITS, GS, NB, w, dd, E8>(a, csize, d.WK, d.wave, stream, plan_only);
+    return (a.rhs != nullptr)                                                                    \
+               ? launch_own_impl<BITS, GS, NB, w, dd, E8, true>(a, csize, d.WK, d.wave, stream, plan_only) \
+               : launch_own_impl<BITS, GS, NB, w, dd, E8, false>(a, csize, d.WK, d.wave, stream, plan_only);
   QMM_OWN_TILES(QMM_TRY_OWN)
 #undef QMM_TRY_OWN
   return cudaErrorNotSupported;

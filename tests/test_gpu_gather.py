@@ -58,9 +58,9 @@ def oracle_ref(mp: synth.MoeProblem, T, lhs, rhs):
 
 
 def gather_variants():
-    """The mma variants and the tma variants (not the warp-owned ones)."""
-    return [i for i, n in enumerate(binding.variant_names()) if n.startswith("mma") or
-            (n.startswith("tma") and not n.startswith("tma_own"))]
+    """Every variant: mma (each expert's own entries), tma and warp-owned
+    (every token against each expert of the union)."""
+    return list(range(len(binding.variant_names())))
 
 
 @pytest.mark.parametrize("groups", [4, 8], ids=["G4_mma_only", "G8_tma_too"])
@@ -77,7 +77,7 @@ def test_gather_small_stacks(torch_cuda, bits, gs, groups):
         ds = DeviceStack(torch, mp)
         lhs, rhs = mp.lists()
         y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
-        y = ds.run(torch, T, lhs, rhs, out_dtype=torch.float32)  # the library's choice (mma)
+        y = ds.run(torch, T, lhs, rhs, out_dtype=torch.float32)  # the library's choice
         assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} default")
         for v in gather_variants():
             for s in (1, 2):
@@ -86,7 +86,7 @@ def test_gather_small_stacks(torch_cuda, bits, gs, groups):
                         y = ds.run(torch, T, lhs, rhs, out_dtype=dt, variant=v, splits=s)
                     except binding.QmmError as e:
                         assert e.status == 3 and binding.variant_names()[v].startswith("tma")
-                        continue
+                        continue  # a tma / warp-owned variant that cannot plan this shape
                     ran_tma |= binding.variant_names()[v].startswith("tma")
                     assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
     assert ran_tma == (groups == 8)
@@ -104,7 +104,8 @@ def test_gather_arbitrary_lists_and_determinism(torch_cuda, K):
     rhs = np.array([4, 1, 4, 1, 0, 1, 1, 4], dtype=np.int32)
     y_ref, a_ref = oracle_ref(mp, 4, lhs, rhs)
     tma = binding.variant_names().index("tma_w8_2cta")
-    for v in ([-1, tma] if K == 512 else [-1]):
+    own = binding.variant_names().index("tma_own_w8_d2_2cta")
+    for v in ([-1, tma, own] if K == 512 else [-1]):
         first = ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32, variant=v)
         assert_within(to_f64(first), y_ref, a_ref, f"hand-made list v{v}")
         assert torch.equal(first[1], first[6]), "a repeated entry gets the same row"
@@ -114,15 +115,17 @@ def test_gather_arbitrary_lists_and_determinism(torch_cuda, K):
 
 @pytest.mark.parametrize("T", [1, 4, 8])
 def test_gather_moe_workload_full(torch_cuda, T):
-    """The 128-expert top-8 gate+up stack at verify widths: every output."""
+    """The 128-expert top-8 gate+up stack at verify widths: every output, at
+    the library's choice and on a forced warp-owned variant."""
     torch = torch_cuda
     w = workloads.MOE_GATE_UP
     mp = synth.make_moe(w.seed, w.E, w.N, w.K, w.bits, w.group_size, T, w.k)
     ds = DeviceStack(torch, mp)
     lhs, rhs = mp.lists()
     y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
-    y = ds.run(torch, T, lhs, rhs)
-    assert_within(to_f64(y), y_ref, a_ref, f"moe T={T}")
+    for v in (-1, binding.variant_names().index("mma_r2_wn2_wk4")):
+        y = ds.run(torch, T, lhs, rhs, variant=v)
+        assert_within(to_f64(y), y_ref, a_ref, f"moe T={T} v{v}")
 
 
 @pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])
@@ -137,7 +140,8 @@ def test_gather_invalid_index_flagged(torch_cuda, K):
     ok = np.array([0, 2, 3])
     y_ref, a_ref = oracle_ref(mp, 4, lhs[ok], rhs[ok])
     tma = binding.variant_names().index("tma_w8_2cta")
-    for v in ([-1, tma] if K == 512 else [-1]):
+    own = binding.variant_names().index("tma_own_w8_d2_2cta")
+    for v in ([-1, tma, own] if K == 512 else [-1]):
         out = torch.full((4, 64), 5.0, dtype=torch.float32, device="cuda")
         ds.run(torch, 4, lhs, rhs, out=out, variant=v)
         torch.cuda.synchronize()
@@ -147,9 +151,10 @@ def test_gather_invalid_index_flagged(torch_cuda, K):
 
 
 def test_gather_too_many_entries_for_one_expert_flagged(torch_cuda):
-    """On the mma variants, a ninth entry for one expert with T <= 8 is flagged
-    and that expert's rows stay unwritten; a forced tma variant (8 groups per
-    row) takes the same list."""
+    """On the mma variants (4 groups per row: the default falls back to them),
+    a ninth entry for one expert with T <= 8 is flagged and that expert's rows
+    stay unwritten; the row-stacking variants (8 groups per row) take the same
+    list."""
     torch = torch_cuda
     mp = synth.make_moe(8301, 4, 64, 256, 4, 64, 4, 1)
     ds = DeviceStack(torch, mp)
@@ -162,6 +167,7 @@ def test_gather_too_many_entries_for_one_expert_flagged(torch_cuda):
     assert bool((out9 == 5.0).all())
     mp8 = synth.make_moe(8302, 4, 64, 512, 4, 64, 4, 1)
     ds8 = DeviceStack(torch, mp8)
-    y = ds8.run(torch, 4, lhs9, rhs9, out_dtype=torch.float32, variant=binding.variant_names().index("tma_w8_2cta"))
     y_ref, a_ref = oracle_ref(mp8, 4, lhs9, rhs9)
-    assert_within(to_f64(y), y_ref, a_ref, "nine entries for one expert on the tma path")
+    for v in (-1, binding.variant_names().index("tma_w8_2cta")):
+        y = ds8.run(torch, 4, lhs9, rhs9, out_dtype=torch.float32, variant=v)
+        assert_within(to_f64(y), y_ref, a_ref, f"nine entries for one expert, v{v}")
