@@ -406,8 +406,8 @@ def moe_report(torch, dev, stream, peak):
 
 
 def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):
-    """Microscaling fp modes on the 5120x5120 layer (mma family): us per call
-    and GB/s over codes + scale bytes; same chains as configs_report."""
+    """Microscaling fp modes on the 5120x5120 layer at the library's choice: us
+    per call and GB/s over codes + scale bytes; same chains as configs_report."""
     from quantized_matmul_speculative_gb300 import binding
 
     N = K = 5120
@@ -437,7 +437,8 @@ def mx_report(torch, dev, stream, peak, ms=(1, 8, 16)):
         del copies, wq, s8
         torch.cuda.empty_cache()
     return {"shape": "5120x5120", "per_m": out,
-            "note": "mma family; one scale byte per 32 codes (E8M0) or per 16 (nvfp4: E4M3), no bias"}
+            "note": "library's choice (warp-owned family); one scale byte per 32 codes (E8M0) or per 16 "
+                    "(nvfp4: E4M3), no bias"}
 
 
 def dense_control(torch, dev, stream, ms=(1, 8, 16)):

@@ -158,7 +158,10 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
  * bias 7, 3 mantissa bits, exponent 0 subnormal).  Encodings: the OCP
  * microscaling format; source of the modes: "MLX quantized_matmul small-M
  * verify kernels", facts "Fix family 1" / "qmv_wide covers affine, nvfp4,
- * mxfp4, mxfp8".  Runs on the "mma" variants (variant -1: the first).
+ * mxfp4, mxfp8".  variant -1: the warp-owned family when it can plan the
+ * shape (K/g a multiple of 16 and of the cluster size, scales 16-byte
+ * aligned), else the first "mma" variant; a forced "mma" or "tma_own"
+ * variant is used as given, a "tma" variant returns QMM_ERR_UNSUPPORTED.
  * QMM_NVFP4: FP4 E2M1 codes with one FP8 E4M3 scale byte per group of 16,
  * scales uint8 [N, K/16] (a per-tensor scale, where a model has one, is left
  * to the caller).

@@ -39,6 +39,11 @@ cudaError_t launch_mma_mx(const CallArgs&, const VariantDesc&, int, cudaStream_t
 extern template cudaError_t launch_mma_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
 extern template cudaError_t launch_mma_mx<2>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template <int FMT>
+cudaError_t launch_own_mx(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
+extern template cudaError_t launch_own_mx<2>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 
 template <int BITS, int GS>
 cudaError_t launch_tma_bg(const CallArgs&, const VariantDesc&, int, cudaStream_t);
@@ -707,7 +712,7 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   if (M < 0 || M > 16 || N < 0 || K < 0) return QMM_ERR_SHAPE;
   if (format != QMM_MXFP4 && format != QMM_MXFP8 && format != QMM_NVFP4) return QMM_ERR_UNSUPPORTED;
   if (out_dtype != QMM_OUT_BF16 && out_dtype != QMM_OUT_F32) return QMM_ERR_UNSUPPORTED;
-  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family != kFamilyMma))
+  if (variant < -1 || variant >= kNumVariants || (variant >= 0 && kVariants[variant].family == kFamilyTma))
     return QMM_ERR_UNSUPPORTED;
   if (splits == 0 || splits < -1 || splits > kMaxSplits) return QMM_ERR_UNSUPPORTED;
   if (K % 32 != 0) return QMM_ERR_SHAPE;
@@ -736,6 +741,28 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   a.bits = format == QMM_MXFP8 ? 8 : 4;
   a.gs = format == QMM_NVFP4 ? 16 : 32;
   a.out_f32 = out_dtype == QMM_OUT_F32;
+  // The warp-owned family when it can plan the shape (variant -1: the
+  // gathered form's default variant; or a forced warp-owned variant), else mma.
+  auto own_mx = [&](const VariantDesc& dd, int cc, bool plan_only) {
+    return (format == QMM_MXFP4)   ? launch_own_mx<0>(a, dd, cc, st, plan_only)
+           : (format == QMM_MXFP8) ? launch_own_mx<1>(a, dd, cc, st, plan_only)
+                                   : launch_own_mx<2>(a, dd, cc, st, plan_only);
+  };
+  const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
+  if (variant < 0 || own_forced) {
+    const VariantDesc& dd = kVariants[own_forced ? variant : kDefaultGatherOwn];
+    for (int cc : {4, 2, 1, 8}) {
+      if (splits > 0 && cc != splits) continue;
+      const cudaError_t pe = own_mx(dd, cc, true);
+      if (pe == cudaErrorNotSupported) continue;
+      if (pe != cudaSuccess) return fail_cuda(pe);
+      if (env_flag("QMM_LOG"))
+        std::fprintf(stderr, "qmm mx: M=%d N=%d K=%d format=%d -> %s splits=%d\n", M, N, K, format, dd.name, cc);
+      const cudaError_t e = own_mx(dd, cc, false);
+      return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+    }
+    if (own_forced) return QMM_ERR_UNSUPPORTED;
+  }
   const VariantDesc& d = kVariants[variant < 0 ? 0 : variant];
   const int s = splits > 0 ? splits : rule_splits(d, N, K, a.gs);
   if (env_flag("QMM_LOG"))

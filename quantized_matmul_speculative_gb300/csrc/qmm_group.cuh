@@ -24,12 +24,20 @@
 #include <cuda_fp16.h>
 
 #include "qmm_device.cuh"
+#include "qmm_internal.h"
 
 namespace qmm {
 
-template <int BITS, int GS, int NB, bool E8 = false>
+// CODES: kCodesAffine (b-bit affine), kCodesAffine8 (8-bit affine as virtual
+// nibbles), or a microscaling format (kCodesMx4, kCodesMx8, kCodesNv4: the
+// codes' values enter the MMA exactly, see unpack_fp4_pair / unpack_fp8_pair,
+// and the fold multiplies by the group's decoded scale byte; no bias).
+template <int BITS, int GS, int NB, int CODES = kCodesAffine>
 struct GroupMath {
+  static constexpr bool E8 = CODES == kCodesAffine8;
+  static constexpr bool MX = CODES == kCodesMx4 || CODES == kCodesMx8 || CODES == kCodesNv4;
   static_assert(!E8 || BITS == 4, "8-bit codes run as virtual 4-bit codes");
+  static_assert(!MX || BITS == (CODES == kCodesMx8 ? 8 : 4), "microscaling code width");
   static constexpr float OFFSET = E8 ? 2176.f : 128.f;  // sum of the unpack offsets per code
   static constexpr int VPW = 32 / BITS;               // codes per 32-bit word
   static constexpr int HALF = VPW / 2;                // code pairs per word
@@ -54,9 +62,12 @@ struct GroupMath {
     if constexpr (E8) {
       stage_x_e8(X, K / 2, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads);
       return;
+    } else if constexpr (BITS == 8) {
+      stage_x_8(X, K, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads);
+      return;
     }
     constexpr int CH = GS / VPW;  // tasks per unit (2..16, divides 32)
-    constexpr int TQ = VPW / 8;   // 16-byte loads per task
+    constexpr int TQ = VPW >= 8 ? VPW / 8 : 1;  // 16-byte loads per task (8-bit codes returned above)
     constexpr int BATCH = 4;
     static_assert(32 % CH == 0, "a unit's tasks must share a warp");
     const int ntask = M * gp * CH;
@@ -148,6 +159,50 @@ struct GroupMath {
     }
   }
 
+  // stage_x for native 8-bit codes (FP8 E4M3): a task is one packed word of 4
+  // codes, i.e. 4 activations of one row (8 bytes), staged as (x0, x2), (x1, x3).
+  __device__ static void stage_x_8(const uint16_t* X, int K, int M, int g0, int gp, unsigned long long gp_magic,
+                                   uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
+    constexpr int CH = GS / VPW;  // words per row and group
+    constexpr int BATCH = 4;
+    static_assert(32 % CH == 0, "a unit's tasks must share a warp");
+    const int ntask = M * gp * CH;
+    for (int base = 0; base < ntask; base += BATCH * nthreads) {
+      uint2 v[BATCH];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * nthreads + tid;
+        const int unit = u / CH;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
+        const int j = unit - m * gp;
+        const uint16_t* src = X + static_cast<int64_t>(m) * K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * 4;
+        v[b] = (u < ntask) ? ld_nc_v2(src) : make_uint2(0, 0);
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int u = base + b * nthreads + tid;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
+        const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
+        const int j = unit - m * gp;
+        float sum = add_bf16x2_f32(v[b].y, add_bf16x2_f32(v[b].x, 0.f));
+        if (u < ntask)
+          *reinterpret_cast<uint2*>(Xs + m * rsx + j * GS + c * VPW) =
+              make_uint2(prmt_lo(v[b].x, v[b].y), prmt_hi(v[b].x, v[b].y));
+#pragma unroll
+        for (int o = CH / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (u < ntask && c == 0) xsum[j * MP + m] = sum;
+      }
+    }
+  }
+
+  // The A operand pair i of a packed word for this code format.
+  __device__ static uint32_t unpack(uint32_t w, int i) {
+    if constexpr (CODES == kCodesMx4 || CODES == kCodesNv4) return unpack_fp4_pair(w, i);
+    else if constexpr (CODES == kCodesMx8) return unpack_fp8_pair(w, i);
+    else return unpack_pair<BITS>(w, i);
+  }
+
   // Fragment geometry of a lane: rows g and g + 8 of the 16-row block,
   // activation columns 2t, 2t + 1 (+ 8 per activation tile), the word offset
   // of its weight words within a row and group, and (for words shared by TPW
@@ -189,10 +244,10 @@ struct GroupMath {
       const int lwi = (TPW == 1) ? st / SPW : 0;
       const int sub = (TPW == 1) ? st % SPW : tsub + st;
       uint32_t a[4];
-      a[0] = unpack_pair<BITS>(wl[lwi], 2 * sub);
-      a[1] = unpack_pair<BITS>(wh[lwi], 2 * sub);
-      a[2] = unpack_pair<BITS>(wl[lwi], 2 * sub + 1);
-      a[3] = unpack_pair<BITS>(wh[lwi], 2 * sub + 1);
+      a[0] = unpack(wl[lwi], 2 * sub);
+      a[1] = unpack(wh[lwi], 2 * sub);
+      a[2] = unpack(wl[lwi], 2 * sub + 1);
+      a[3] = unpack(wh[lwi], 2 * sub + 1);
       const int ko = (TPW == 1) ? (lwi * VPW + 4 * sub) : 4 * st;
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -217,6 +272,20 @@ struct GroupMath {
       ffma2(acc[nb][0], acc[nb][1], b_lo, b_lo, xs.x, xs.y);
       ffma2(acc[nb][0], acc[nb][1], s_lo, s_lo, tmp[nb][0], tmp[nb][1]);
       ffma2(acc[nb][2], acc[nb][3], b_hi, b_hi, xs.x, xs.y);
+      ffma2(acc[nb][2], acc[nb][3], s_hi, s_hi, tmp[nb][2], tmp[nb][3]);
+    }
+  }
+
+  // Microscaling fold: acc += s * P with s the group's decoded scale byte
+  // (E8M0, or E4M3 for nvfp4).  meta_j -> the byte of (row g, this group); row
+  // g + 8 at + 8 * mbw (mbw: bytes per staged scale row).
+  __device__ static void fold_mx(const uint8_t* meta_j, int mbw, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
+    const uint32_t blo = meta_j[0], bhi = meta_j[8 * mbw];
+    const float s_lo = (CODES == kCodesNv4) ? e4m3_to_float(blo) : e8m0_to_float(blo);
+    const float s_hi = (CODES == kCodesNv4) ? e4m3_to_float(bhi) : e8m0_to_float(bhi);
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      ffma2(acc[nb][0], acc[nb][1], s_lo, s_lo, tmp[nb][0], tmp[nb][1]);
       ffma2(acc[nb][2], acc[nb][3], s_hi, s_hi, tmp[nb][2], tmp[nb][3]);
     }
   }

@@ -31,11 +31,14 @@ template cudaError_t launch_tma_bg<QMM_BITS, QMM_GS>(const CallArgs&, const Vari
 template cudaError_t launch_own_bg<QMM_BITS, QMM_GS>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 #if QMM_BITS == 4 && QMM_GS == 32
 template cudaError_t launch_mma_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template cudaError_t launch_own_mx<0>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 #endif
 #if QMM_BITS == 4 && QMM_GS == 64
 template cudaError_t launch_mma_mx<2>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template cudaError_t launch_own_mx<2>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 #endif
 #if QMM_BITS == 8 && QMM_GS == 32
 template cudaError_t launch_mma_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t);
+template cudaError_t launch_own_mx<1>(const CallArgs&, const VariantDesc&, int, cudaStream_t, bool);
 #endif
 }

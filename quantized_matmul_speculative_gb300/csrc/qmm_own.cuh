@@ -70,7 +70,9 @@ struct OwnParams {
 // and those rows only feed output columns that are never stored.
 struct OwnLayout {
   int x_off, xs_off, ring_off, w_bytes, stage_bytes, recv_off, slot_bytes, total, rsx;
-  __host__ __device__ OwnLayout(int W, int D, int gp, int gs, int mp, int nb, int nbox, int bw, int mbw,
+  // meta_row: bytes of scale/bias data per weight row of a unit (affine: fp16
+  // scales and biases, 2 * mbw halves; microscaling: mbw scale bytes).
+  __host__ __device__ OwnLayout(int W, int D, int gp, int gs, int mp, int nb, int nbox, int bw, int meta_row,
                                 int owned_max, int csize, int maxw, int m) {
     const int nbar = W * D + owned_max;  // full barriers of the rings, then one per owned tile
     rsx = gp * gs + 4;                   // X row stride (halves): 8 bytes past a 16-byte multiple
@@ -78,7 +80,7 @@ struct OwnLayout {
     xs_off = (x_off + m * rsx * 2 + 15) & ~15;
     ring_off = (xs_off + gp * mp * 4 + 127) & ~127;
     w_bytes = nbox * 16 * bw * 4;
-    stage_bytes = (w_bytes + 2 * 16 * mbw * 2 + 127) & ~127;
+    stage_bytes = (w_bytes + 16 * meta_row + 127) & ~127;
     recv_off = ring_off + W * D * stage_bytes;
     slot_bytes = 32 * 16 * nb;  // 32 lanes x 4 floats x activation tiles
     total = recv_off + owned_max * csize * maxw * slot_bytes;
@@ -89,11 +91,12 @@ struct OwnLayout {
 
 // With W <= 8 two CTAs must fit an SM (the "2cta" shared-memory budget and
 // the next call's CTAs under PDL), which caps registers at 128 per thread.
-template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
+template <int BITS, int GS, int NB, int W, int D, int CODES, bool GATHER>
 __global__ void __launch_bounds__(32 * W, (W <= 8) ? 2 : 1)
 qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const OwnParams p) {
-  using GM = GroupMath<BITS, GS, NB, E8>;
+  using GM = GroupMath<BITS, GS, NB, CODES>;
+  constexpr bool MX = GM::MX;  // one scale byte per (row, group), no bias
   constexpr int MP = GM::MP;
   constexpr int GW = GM::GW;
   extern __shared__ __align__(128) unsigned char own_smem[];
@@ -101,7 +104,8 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int csize = static_cast<int>(gridDim.x);  // CTAs per cluster (cluster spans x)
   const int rank = static_cast<int>(blockIdx.x);
   const int q = static_cast<int>(blockIdx.y);
-  const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, p.mbw, p.owned_max, csize, p.maxw, p.M);
+  const int meta_row = MX ? p.mbw : 4 * p.mbw;
+  const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, meta_row, p.owned_max, csize, p.maxw, p.M);
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -155,7 +159,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     }
     maxw = mw;
   }
-  const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + 2 * 16 * p.mbw * 2);
+  const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + 16 * meta_row);
 
   QMM_TRACE_POINT(0);
   if (lane == 0)
@@ -194,9 +198,14 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     mbar_arrive_expect_tx(full_bar(s), unit_bytes);
     for (int b = 0; b < p.nbox; ++b)
       tma_load_2d(dst + static_cast<uint32_t>(b * 16 * p.bw * 4), &tmap, gs0 * GW + b * p.bw, n0, full_bar(s));
-    const int mx0 = (gs0 / 8) * 8;  // 16-byte aligned start of the scale/bias box
-    tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
-    tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 16 * p.mbw * 2), &tmap_b, mx0, n0, full_bar(s));
+    if constexpr (MX) {
+      const int mx0 = (gs0 / 16) * 16;  // 16-byte aligned start of the scale-byte box
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+    } else {
+      const int mx0 = (gs0 / 8) * 8;  // 16-byte aligned start of the scale/bias box
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 16 * p.mbw * 2), &tmap_b, mx0, n0, full_bar(s));
+    }
   };
   if (lane == 0) {
     if (warp == 0) {
@@ -304,6 +313,8 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     // Scales then biases: [16 rows][mbw halves] each, from group (g0 + part*gq) rounded down to 8.
     const int gs0 = g0 + part * p.gq;
     const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + ln.g * p.mbw + (gs0 % 8);
+    // (microscaling: [16 rows][mbw scale bytes], from group gs0 rounded down to 16)
+    const uint8_t* meta8 = stage + L.w_bytes + ln.g * p.mbw + (gs0 % 16);
     const int jr = part * p.gq;  // the unit's first group within the K-piece
     const uint16_t* xu = xrow + jr * GS;
     const float* xsu = xsum + jr * MP;
@@ -322,7 +333,10 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       GM::load_words(next_words(), p.bw, wl, wh);
       GM::mma(wl, wh, xu + j * GS, L.rsx, ln.tsub, tmp);
     };
-    auto fold = [&](int j, const float (&tmp)[NB][4]) { GM::fold(meta + j, p.mbw, xsu + j * MP, ln.t, tmp, acc); };
+    auto fold = [&](int j, const float (&tmp)[NB][4]) {
+      if constexpr (MX) GM::fold_mx(meta8 + j, p.mbw, tmp, acc);
+      else GM::fold(meta + j, p.mbw, xsu + j * MP, ln.t, tmp, acc);
+    };
     int j = 0;
     for (; NB == 1 && j + 3 < p.gq; j += 4) {  // four independent MMA chains
       float t0[NB][4], t1[NB][4], t2[NB][4], t3[NB][4];

@@ -18,13 +18,21 @@ namespace qmm {
 // Plan one call: K-piece, parts per tile, box widths, clusters, receive
 // slots and shared memory.  Returns cudaErrorNotSupported (and launches
 // nothing) when (W, D, csize, CTAs per SM) cannot run the shape.
-template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
+template <int BITS, int GS, int NB, int W, int D, int CODES, bool GATHER>
 cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, OwnParams* p, int* smem, int* budget) {
-  constexpr int GW = GroupMath<BITS, GS, NB>::GW;
+  using GM = GroupMath<BITS, GS, NB, CODES>;
+  constexpr int GW = GM::GW;
+  constexpr bool MX = GM::MX;
   constexpr int MP = 8 * NB;
   const int G = a.K / GS;
-  if (G % 8 != 0 || G % csize != 0) return cudaErrorNotSupported;  // scale/bias rows must be 16-byte strided
-  if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
+  if (G % csize != 0) return cudaErrorNotSupported;
+  if (MX) {
+    // one scale byte per group: the rows of the byte tensor map must be 16-byte strided
+    if (G % 16 != 0 || (reinterpret_cast<uintptr_t>(a.S8) & 15)) return cudaErrorNotSupported;
+  } else {
+    if (G % 8 != 0) return cudaErrorNotSupported;  // scale/bias rows must be 16-byte strided
+    if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
+  }
   p->X = a.X;
   p->Y = a.Y;
   p->R = a.R;
@@ -48,7 +56,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   }
   const int gather_bytes = GATHER ? kGatherSmemInts * 4 : 0;
 
-  auto kern = qmm_own_kernel<BITS, GS, NB, W, D, E8, GATHER>;
+  auto kern = qmm_own_kernel<BITS, GS, NB, W, D, CODES, GATHER>;
   int sm_bytes = 0, optin = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
@@ -98,8 +106,10 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
       if (w <= 256 && w % 4 == 0) bw = w;
     }
     if (bw == 0) continue;
-    const int mbw = (7 + gq + 7) / 8 * 8;  // any start within 8 groups of the box start
+    // scale box width: any start within 8 groups (fp16) or 16 groups (bytes) of the box start
+    const int mbw = MX ? (15 + gq + 15) / 16 * 16 : (7 + gq + 7) / 8 * 8;
     if (mbw > 256) continue;
+    const int meta_row = MX ? mbw : 4 * mbw;
     int maxw = 1;
     for (int nt : {nt_min, nt_max}) {
       if (nt < 1) continue;
@@ -110,7 +120,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
       }
     }
     const int owned_max = (nt_max + csize - 1) / csize;
-    const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, mbw, owned_max, csize, maxw, a.M);
+    const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, meta_row, owned_max, csize, maxw, a.M);
     int total = L.total;
     if constexpr (GATHER) {
       // The union decides the tile count nt <= nt_max in the kernel, which
@@ -149,12 +159,13 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   return found ? cudaSuccess : cudaErrorNotSupported;
 }
 
-template <int BITS, int GS, int NB, int W, int D, bool E8, bool GATHER>
+template <int BITS, int GS, int NB, int W, int D, int CODES, bool GATHER>
 cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int wave, cudaStream_t stream,
                             bool plan_only) {
   OwnParams p;
   int smem = 0, budget = 0;
-  const cudaError_t pe = own_plan<BITS, GS, NB, W, D, E8, GATHER>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
+  const cudaError_t pe = own_plan<BITS, GS, NB, W, D, CODES, GATHER>(a, csize, ctas_per_sm, wave, &p, &smem, &budget);
+  constexpr bool MX = GroupMath<BITS, GS, NB, CODES>::MX;
   const int64_t map_rows = GATHER ? static_cast<int64_t>(a.E) * a.N : a.N;  // gathered: the whole stack
   if (pe != cudaSuccess || plan_only) return pe;
 
@@ -172,7 +183,19 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
       return cudaErrorInvalidValue;
   }
   const int G = a.K / GS;
-  for (int arr = 0; arr < 2; ++arr) {
+  if (MX) {
+    // one byte per (row, group); the bias map is not read (a copy stands in for it)
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(map_rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
+    const cuuint32_t estride[2] = {1u, 1u};
+    if (encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.S8), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    tmap_b = tmap_s;
+  }
+  for (int arr = 0; arr < (MX ? 0 : 2); ++arr) {
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(map_rows)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G) * 2};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
@@ -205,16 +228,26 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D, E8, GATHER>, tmap, tmap_s, tmap_b, p);
+  return cudaLaunchKernelEx(&cfg, qmm_own_kernel<BITS, GS, NB, W, D, CODES, GATHER>, tmap, tmap_s, tmap_b, p);
 }
 
-template <int BITS, int GS, int NB, bool E8>
+// Gathered calls exist for the affine code formats only.
+template <int BITS, int GS, int NB, int W, int D, int CODES>
+cudaError_t launch_own_impl_g(const CallArgs& a, int csize, int ctas_per_sm, int wave, cudaStream_t stream,
+                              bool plan_only) {
+  if (a.rhs == nullptr) return launch_own_impl<BITS, GS, NB, W, D, CODES, false>(a, csize, ctas_per_sm, wave, stream,
+                                                                                   plan_only);
+  if constexpr (CODES == kCodesAffine || CODES == kCodesAffine8)
+    return launch_own_impl<BITS, GS, NB, W, D, CODES, true>(a, csize, ctas_per_sm, wave, stream, plan_only);
+  else
+    return cudaErrorNotSupported;
+}
+
+template <int BITS, int GS, int NB, int CODES>
 cudaError_t launch_own_tile(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
 #define QMM_TRY_OWN(w, dd)                 \
   if (d.WN == (w) && d.R == (dd))          \
-    return (a.rhs != nullptr)                                                                    \
-               ? launch_own_impl<BITS, GS, NB, w, dd, E8, true>(a, csize, d.WK, d.wave, stream, plan_only) \
-               : launch_own_impl<BITS, GS, NB, w, dd, E8, false>(a, csize, d.WK, d.wave, stream, plan_only);
+    return launch_own_impl_g<BITS, GS, NB, w, dd, CODES>(a, csize, d.WK, d.wave, stream, plan_only);
   QMM_OWN_TILES(QMM_TRY_OWN)
 #undef QMM_TRY_OWN
   return cudaErrorNotSupported;
@@ -224,12 +257,22 @@ template <int BITS, int GS>
 cudaError_t launch_own_bg(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
   if constexpr (BITS == 8) {
     const CallArgs v = as_virtual_nibbles(a);
-    if (v.M <= 8) return launch_own_tile<4, 2 * GS, 1, true>(v, d, csize, stream, plan_only);
-    return launch_own_tile<4, 2 * GS, 2, true>(v, d, csize, stream, plan_only);
+    if (v.M <= 8) return launch_own_tile<4, 2 * GS, 1, kCodesAffine8>(v, d, csize, stream, plan_only);
+    return launch_own_tile<4, 2 * GS, 2, kCodesAffine8>(v, d, csize, stream, plan_only);
   } else {
-    if (a.M <= 8) return launch_own_tile<BITS, GS, 1, false>(a, d, csize, stream, plan_only);
-    return launch_own_tile<BITS, GS, 2, false>(a, d, csize, stream, plan_only);
+    if (a.M <= 8) return launch_own_tile<BITS, GS, 1, kCodesAffine>(a, d, csize, stream, plan_only);
+    return launch_own_tile<BITS, GS, 2, kCodesAffine>(a, d, csize, stream, plan_only);
   }
+}
+
+// Microscaled weights on the warp-owned family: FMT 0 = mxfp4, 1 = mxfp8, 2 = nvfp4.
+template <int FMT>
+cudaError_t launch_own_mx(const CallArgs& a, const VariantDesc& d, int csize, cudaStream_t stream, bool plan_only) {
+  constexpr int BITS = FMT == 1 ? 8 : 4;
+  constexpr int GS = FMT == 2 ? 16 : 32;
+  constexpr int CODES = FMT == 0 ? kCodesMx4 : FMT == 1 ? kCodesMx8 : kCodesNv4;
+  if (a.M <= 8) return launch_own_tile<BITS, GS, 1, CODES>(a, d, csize, stream, plan_only);
+  return launch_own_tile<BITS, GS, 2, CODES>(a, d, csize, stream, plan_only);
 }
 
 }  // namespace qmm

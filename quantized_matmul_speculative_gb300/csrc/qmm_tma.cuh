@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(32 * (W + 1), (W <= 8) ? 2 : 1)
 qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_s,
                const __grid_constant__ CUtensorMap tmap_b, const TmaParams p) {
   using C = TmaCfg<BITS, GS, NB, W, SMAX>;
-  using GM = GroupMath<BITS, GS, NB, E8>;
+  using GM = GroupMath<BITS, GS, NB, E8 ? kCodesAffine8 : kCodesAffine>;
   static_assert((2 * SMAX + 1) * 8 <= 512, "mbarriers must fit below the stages");
   const int S = p.stages;
   extern __shared__ __align__(128) unsigned char tma_smem[];
