@@ -64,7 +64,9 @@ typedef enum {
                            /* aligned to their element size                        */
   QMM_ERR_CUDA = 5,        /* the CUDA runtime reported an error; see               */
                            /* qmm_last_cuda_error()                                 */
-  QMM_ERR_TABLE = 6        /* the dispatch table has no usable entry                */
+  QMM_ERR_TABLE = 6        /* the dispatch table is unusable: the QMM_TABLE file    */
+                           /* cannot be read or holds no entry, or the shape's     */
+                           /* entry names an unknown variant or split count        */
 } qmm_status;
 
 typedef enum { QMM_OUT_BF16 = 0, QMM_OUT_F32 = 1 } qmm_out_dtype;
@@ -197,7 +199,12 @@ qmm_status qmm_repack(const uint32_t* Wq, int64_t N, int64_t K, int bits, uint32
 qmm_status qmm_unrepack(const uint32_t* Wq_native, int64_t N, int64_t K, int bits, uint32_t* Wq, void* stream);
 
 /* Introspection of the dispatcher: the variant and split count qmm_small_m
- * would use, or -1 (and *splits untouched) if the shape is unsupported.         */
+ * would use, or -1 (and *splits untouched) if the shape is unsupported or the
+ * table is unusable.  The table is compiled in; the environment variable
+ * QMM_TABLE=<path> replaces it, for the whole process, by a file in the
+ * format of the compiled one (lines "{M, N, K, bits, group, variant, splits},",
+ * text after "//" ignored).  QMM_FORCE_VARIANT=<name or id> and
+ * QMM_FORCE_SPLITS=<n> override the choice; QMM_LOG=1 prints it to stderr.      */
 int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* splits);
 
 int qmm_num_variants(void);

@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -119,6 +120,44 @@ const TableEntry kTable[] = {
 };
 constexpr int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
 
+// The dispatch table in use: the compiled-in one, or the file QMM_TABLE names
+// (read once per process, in the format of qmm_dispatch_table.inc: one
+// "{M, N, K, bits, group, variant, splits}," entry per line, anything after
+// "//" ignored).  A QMM_TABLE file that cannot be read or holds no entry is a
+// table error: every dispatched call then returns QMM_ERR_TABLE.
+struct ActiveTable {
+  std::vector<TableEntry> entries;
+  bool error = false;
+  ActiveTable() {
+    const char* path = std::getenv("QMM_TABLE");
+    if (path == nullptr || path[0] == '\0') {
+      entries.assign(kTable, kTable + kTableSize);
+      return;
+    }
+    FILE* f = std::fopen(path, "r");
+    if (f == nullptr) {
+      error = true;
+      return;
+    }
+    char line[512];
+    while (std::fgets(line, sizeof(line), f) != nullptr) {
+      char* c = std::strstr(line, "//");
+      if (c != nullptr) *c = '\0';
+      TableEntry e;
+      if (std::sscanf(line, " { %d , %d , %d , %d , %d , %d , %d }", &e.M, &e.N, &e.K, &e.bits, &e.gs, &e.variant,
+                      &e.splits) == 7)
+        entries.push_back(e);
+    }
+    std::fclose(f);
+    error = entries.empty();
+  }
+};
+
+const ActiveTable& active_table() {
+  static const ActiveTable t;  // thread-safe one-time initialization
+  return t;
+}
+
 bool env_flag(const char* name) {
   const char* v = std::getenv(name);
   return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
@@ -162,9 +201,10 @@ int rule_splits(const VariantDesc& d, int N, int K, int gs) {
 // measured M of the same (N, K, bits, gs) that uses the same number of 8-row
 // activation tiles; -1 if the shape was not swept.
 int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
+  const std::vector<TableEntry>& table = active_table().entries;
   int best = -1, best_d = 1 << 30;
-  for (int i = 0; i < kTableSize; ++i) {
-    const TableEntry& e = kTable[i];
+  for (int i = 0; i < static_cast<int>(table.size()); ++i) {
+    const TableEntry& e = table[i];
     if (e.variant < 0 || e.N != N || e.K != K || e.bits != bits || e.gs != gs) continue;
     if ((e.M <= 8) != (M <= 8)) continue;
     const int d = e.M > M ? e.M - M : M - e.M;
@@ -174,8 +214,11 @@ int table_lookup(int M, int N, int K, int bits, int gs, int* splits) {
     }
   }
   if (best < 0) return -1;
-  *splits = kTable[best].splits;
-  return kTable[best].variant;
+  *splits = table[best].splits;
+  // host-side fault injection for the error-path tests: the entry reads as corrupt
+  const char* inject = std::getenv("QMM_TEST_INJECT");
+  if (inject != nullptr && std::strcmp(inject, "bad_table") == 0) return kNumVariants + 1000;
+  return table[best].variant;
 }
 
 // Cluster size for the TMA family on shapes the sweep did not cover: the
@@ -203,10 +246,15 @@ int rule_tma_cluster(const CallArgs& a, const VariantDesc& d) {
   return best;
 }
 
+// The variant and split count for a call: the table's entry for the shape,
+// else the rule-based choice.  -2 for a table error (an unreadable QMM_TABLE
+// file, or an entry whose variant or split count is out of range).
 int select_variant(const CallArgs& a, int* splits) {
+  if (active_table().error) return -2;
   int s = -1;
   const int v = table_lookup(a.M, a.N, a.K, a.bits, a.gs, &s);
-  if (v >= 0 && v < kNumVariants && s >= 1 && s <= kMaxSplits) {
+  if (v >= 0) {
+    if (v >= kNumVariants || s < 1 || s > kMaxSplits) return -2;
     *splits = s;
     return v;
   }
@@ -357,6 +405,7 @@ int qmm_select_variant(int M, int N, int K, int bits, int group_size, int* split
   a.gs = group_size;
   int s = 1;
   const int v = select_variant(a, &s);
+  if (v < 0) return -1;
   if (splits) *splits = s;
   return v;
 }
@@ -435,6 +484,7 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
   if (v < 0) {
     int ts = 1;
     v = select_variant(a, &ts);
+    if (v < 0) return QMM_ERR_TABLE;
     if (s < 0) s = ts;
     // The table's choice was measured on this shape; if it cannot be planned
     // here (another device, or a resource limit that changed), take the

@@ -2,6 +2,7 @@
 packs bit-exactly like the oracle's packer, and rejects bad arguments on the
 host before touching the device."""
 import ctypes
+import os
 import re
 from pathlib import Path
 
@@ -154,6 +155,44 @@ def test_mx_validation_before_launch(lib):
     assert rc(X=None) == 1 and rc(S=None) == 1 and rc(Y=None) == 1
     assert rc(X=p + 2) == 4 and rc(Wq=p + 4) == 4
     assert rc(M=0) == 0 and rc(N=0) == 0
+
+
+def test_bad_table_injection_returns_table_error(lib, monkeypatch):
+    """A corrupt table entry (host-side injection) is a table error, found before
+    any CUDA call (the pointers are never dereferenced)."""
+    p = 0x10000
+    v, s = binding.select_variant(4, 5120, 5120, 4, 64)
+    assert v is not None
+    monkeypatch.setenv("QMM_TEST_INJECT", "bad_table")
+    assert lib.qmm_select_variant(4, 5120, 5120, 4, 64, None) == -1
+    assert lib.qmm_small_m_ex(p, p, p, p, 4, 5120, 5120, 4, 64, p, 0, -1, -1, None) == 6
+
+
+def test_runtime_table_file(tmp_path):
+    """QMM_TABLE replaces the compiled-in table (read once per process, so the
+    check runs in fresh processes); an unreadable file is a table error."""
+    import subprocess
+    import sys
+
+    names = binding.variant_names()
+    mma = names.index("mma_r1_wn2_wk4")
+    table = tmp_path / "table.inc"
+    table.write_text(f"// a one-entry table\n{{4, 5120, 5120, 4, 64, {mma}, 3}},  // forced for the test\n")
+    code = ("import sys; sys.path.insert(0, {root!r}); from quantized_matmul_speculative_gb300 import binding; "
+            "print(binding.select_variant(4, 5120, 5120, 4, 64), binding.select_variant(4, 4096, 4096, 4, 64))")
+    root = str(Path(__file__).resolve().parents[1])
+    env = dict(os.environ, QMM_TABLE=str(table))
+    out = subprocess.run([sys.executable, "-c", code.format(root=root)], env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    first, second = out.stdout.strip().split(") (")
+    assert first == f"({mma}, 3"
+    assert second.rstrip(")").split(", ")[0] != "None"  # not in the file: the rule's choice
+    env["QMM_TABLE"] = str(tmp_path / "missing.inc")
+    out = subprocess.run([sys.executable, "-c", code.format(root=root)], env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "(None, None) (None, None)"
 
 
 def test_variant_registry(lib):
