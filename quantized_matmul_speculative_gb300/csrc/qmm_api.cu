@@ -104,6 +104,7 @@ const VariantDesc kVariants[] = {
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
 constexpr int kDefaultGatherOwn = 13;  // tma_own_w8_d2_2cta: the gathered form's default
+constexpr int kDefaultOwnWide = 8;     // tma_own_w16_d2_1cta: microscaling modes at M > 12
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 constexpr int kMaxSplits = 16;
 
@@ -791,8 +792,10 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   a.bits = format == QMM_MXFP8 ? 8 : 4;
   a.gs = format == QMM_NVFP4 ? 16 : 32;
   a.out_f32 = out_dtype == QMM_OUT_F32;
-  // The warp-owned family when it can plan the shape (variant -1: the
-  // gathered form's default variant; or a forced warp-owned variant), else mma.
+  // The warp-owned family when it can plan the shape, else mma.  Variant -1:
+  // tma_own_w8_d2_2cta, or tma_own_w16_d2_1cta above 12 rows (a sweep over the
+  // warp-owned variants on 5120^2 and 8192^2 for all three formats), the first
+  // cluster size of (4, 2, 1, 8) that plans; or a forced warp-owned variant.
   auto own_mx = [&](const VariantDesc& dd, int cc, bool plan_only) {
     return (format == QMM_MXFP4)   ? launch_own_mx<0>(a, dd, cc, st, plan_only)
            : (format == QMM_MXFP8) ? launch_own_mx<1>(a, dd, cc, st, plan_only)
@@ -800,7 +803,7 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   };
   const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
   if (variant < 0 || own_forced) {
-    const VariantDesc& dd = kVariants[own_forced ? variant : kDefaultGatherOwn];
+    const VariantDesc& dd = kVariants[own_forced ? variant : (M > 12 ? kDefaultOwnWide : kDefaultGatherOwn)];
     for (int cc : {4, 2, 1, 8}) {
       if (splits > 0 && cc != splits) continue;
       const cudaError_t pe = own_mx(dd, cc, true);
