@@ -276,3 +276,33 @@ def test_repack_round_trip_and_use(torch_cuda):
     y = binding.small_m(dp.x[:5].contiguous(), native, dp.s, dp.b, 4, 64, out_dtype=torch.float32)
     assert_within(to_f64(y), y_ref, a_ref, "repacked weights")
 
+
+
+# ------------------------------------------------------------- large extents
+@pytest.mark.parametrize("N,K,bits,gs,M", [(64, 65536, 4, 128, 16), (262144, 256, 4, 64, 3), (96, 32768, 8, 32, 9)],
+                         ids=["K65536", "N262144", "K32768_8bit"])
+def test_large_extents(torch_cuda, N, K, bits, gs, M):
+    """A very long K (the activations no longer fit one CTA's shared memory
+    unless K is split) and a very tall N, on every variant that takes the
+    shape, against the oracle (full for long K, sampled for tall N)."""
+    torch = torch_cuda
+    p = synth.make_problem(9500 + N % 1000 + K % 997, N, K, bits, gs)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    full = N * K <= 64 * 65536
+    if full:
+        y_ref, a_ref = ref.full(M)
+    ms, ns = sample_positions(M, N, 256, seed=7)
+    if not full:
+        y_ref_s, a_ref_s = ref.sampled(M, ms, ns)
+    ran = 0
+    for v in [-1] + variants():
+        y = dp.run(M, out_dtype=torch.float32, variant=v, allow_unsupported=True)
+        if y is None:
+            continue
+        ran += 1
+        y = to_f64(y)
+        if full:
+            assert_within(y, y_ref, a_ref, f"N={N} K={K} v{v}")
+        else:
+            assert_within(y[ms, ns], y_ref_s, a_ref_s, f"N={N} K={K} v{v}")
+    assert ran >= 2
