@@ -217,3 +217,34 @@ def test_repack_validates_on_the_host(lib):
         assert fn(fake, 4, 64, 4, None, None) == 1            # null destination
         assert fn(None, 0, 64, 4, None, None) == 0            # empty: nothing to do
         assert fn(fake, 4, 64, 4, fake, None) == 0            # in place: the layouts coincide
+
+
+def test_dispatch_table_covers_every_workload():
+    """The compiled-in table (generated from the committed sweep) names real
+    variants with valid split counts, its comments agree with the variant ids,
+    and every workload shape has an entry for each activation-tile class it is
+    run at (the dispatcher takes the nearest measured M of the same class)."""
+    from quantized_matmul_speculative_gb300 import workloads
+
+    inc = Path(__file__).resolve().parents[1] / "quantized_matmul_speculative_gb300" / "csrc" / "qmm_dispatch_table.inc"
+    names = binding.variant_names()
+    entries = {}
+    for line in inc.read_text().splitlines():
+        m = re.match(r"\{(-?\d+), (\d+), (\d+), (\d+), (\d+), (-?\d+), (-?\d+)\},\s*//\s*(\S+)", line)
+        if not m:
+            continue
+        M, N, K, bits, gs, v, s = (int(m.group(i)) for i in range(1, 8))
+        if v < 0:
+            continue  # the sentinel
+        assert 0 <= v < len(names) and 1 <= s <= 16, line
+        assert names[v] == m.group(8), f"table comment {m.group(8)} != variant {v} ({names[v]})"
+        entries.setdefault((N, K, bits, gs), set()).add(M <= 8)
+    for w in workloads.ALL:
+        for sh in w.shapes:
+            for bits, gs in (w.variants or ((w.bits, w.group_size),)):
+                classes = {M <= 8 for M in w.ms}
+                have = entries.get((sh.N, sh.K, bits, gs), set())
+                assert classes <= have, f"{w.name} {sh.name} {bits}b g{gs}: table lacks M classes {classes - have}"
+                for M in w.ms:
+                    v, s = binding.select_variant(M, sh.N, sh.K, bits, gs)
+                    assert v is not None and 1 <= s <= 16
