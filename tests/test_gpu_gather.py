@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle
-from qmm_harness import assert_within, to_f64
+from qmm_harness import assert_within, check, to_f64
 from quantized_matmul_speculative_gb300 import binding, synth, workloads
 
 pytestmark = pytest.mark.gpu
@@ -88,7 +88,7 @@ def test_gather_small_stacks(torch_cuda, bits, gs, groups):
                         assert e.status == 3 and binding.variant_names()[v].startswith("tma")
                         continue  # a tma / warp-owned variant that cannot plan this shape
                     ran_tma |= binding.variant_names()[v].startswith("tma")
-                    assert_within(to_f64(y), y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
+                    check(y, y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
     assert ran_tma == (groups == 8)
 
 
@@ -125,7 +125,7 @@ def test_gather_moe_workload_full(torch_cuda, T):
     y_ref, a_ref = oracle_ref(mp, T, lhs, rhs)
     for v in (-1, binding.variant_names().index("mma_r2_wn2_wk4")):
         y = ds.run(torch, T, lhs, rhs, variant=v)
-        assert_within(to_f64(y), y_ref, a_ref, f"moe T={T} v{v}")
+        check(y, y_ref, a_ref, f"moe T={T} v{v}")
 
 
 @pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])

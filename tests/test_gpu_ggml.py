@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 from oracle import oracle
-from qmm_harness import assert_within, sample_positions, to_f64
+from qmm_harness import check, sample_positions
 from quantized_matmul_speculative_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
@@ -68,7 +68,7 @@ def test_ggml_product(torch_cuda, kind):
     y_ref, a_ref = ol.ggml_qmm(kind, xb, blocks, N)
     for M in range(1, 17):
         y = binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32, out_dtype=torch.float32)
-        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{kind} M={M}")
+        check(y, y_ref[:M], a_ref[:M], f"{kind} M={M}")
     for v in range(len(binding.variant_names())):
         for dt in (torch.float32, torch.bfloat16):
             try:
@@ -76,7 +76,7 @@ def test_ggml_product(torch_cuda, kind):
             except binding.QmmError as e:
                 assert e.status == 3
                 continue
-            assert_within(to_f64(y), y_ref[:5], a_ref[:5], f"{kind} v{v} {dt}")
+            check(y, y_ref[:5], a_ref[:5], f"{kind} v{v} {dt}")
 
     N = K = 4096
     blocks = synth.make_ggml_blocks(8501, N, K, kind)
@@ -85,6 +85,6 @@ def test_ggml_product(torch_cuda, kind):
     x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
     y_ref, a_ref = ol.ggml_qmm(kind, xb, blocks, N)
     for M in (1, 8, 16):
-        y = to_f64(binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32))
+        y = binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32)
         ms, ns = sample_positions(M, N, 256, seed=M)
-        assert_within(y[ms, ns], y_ref[ms, ns], a_ref[ms, ns], f"{kind} 4096 M={M}")
+        check(y, y_ref[ms, ns], a_ref[ms, ns], f"{kind} 4096 M={M}", at=(ms, ns))

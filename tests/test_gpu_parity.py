@@ -5,10 +5,9 @@ shapes are checked element by element against the full oracle; full-size
 workload shapes are checked on sampled outputs the oracle computes one by one,
 in the same launch configuration the benchmark uses (the dispatcher's choice).
 """
-import numpy as np
 import pytest
 
-from qmm_harness import DeviceProblem, OracleRef, assert_within, sample_positions, to_f64
+from qmm_harness import DeviceProblem, OracleRef, assert_within, check, sample_positions, to_f64
 from quantized_matmul_speculative_gb300 import binding, synth, workloads
 
 pytestmark = pytest.mark.gpu
@@ -65,7 +64,7 @@ def test_small_shapes_all_m(torch_cuda, bits, gs):
                 assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"v{v} s{splits} M={M} f32")
             y = dp.run(16, variant=v, splits=splits, allow_unsupported=is_tma(v))
             if y is not None:
-                assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} M=16 bf16")
+                check(y, y_ref, a_ref, f"v{v} s{splits} M=16 bf16")
     assert ran_tma, "no TMA variant ran on this shape"
 
 
@@ -95,13 +94,13 @@ def test_single_layer_workload_full(torch_cuda):
     dp, ref = DeviceProblem(p), OracleRef(p)
     y_ref, a_ref = ref.full(4)
     y = dp.run(4)
-    assert_within(to_f64(y), y_ref, a_ref, "dispatcher")
+    check(y, y_ref, a_ref, "dispatcher")
     for v in variants():
         for splits in (1, 2, 4, 8):
             for dt in (torch.bfloat16, torch.float32):
                 y = dp.run(4, out_dtype=dt, variant=v, splits=splits, allow_unsupported=is_tma(v))
                 if y is not None:
-                    assert_within(to_f64(y), y_ref, a_ref, f"v{v} s{splits} {dt}")
+                    check(y, y_ref, a_ref, f"v{v} s{splits} {dt}")
 
 
 def test_m_sweep_5120_full(torch_cuda):
@@ -113,7 +112,7 @@ def test_m_sweep_5120_full(torch_cuda):
     y_ref, a_ref = ref.full(16)
     for M in w.ms:
         y = dp.run(M)
-        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"M={M}")
+        check(y, y_ref[:M], a_ref[:M], f"M={M}")
 
 
 @pytest.mark.parametrize("shape_index", range(4))
@@ -123,10 +122,10 @@ def test_dense27b_layer_sampled(torch_cuda, shape_index):
     p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
     dp, ref = DeviceProblem(p), OracleRef(p)
     for M in w.ms:
-        y = to_f64(dp.run(M))
+        y = dp.run(M)
         ms, ns = sample_positions(M, sh.N, 192, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
-        assert_within(y[ms, ns], y_ref, a_ref, f"{sh.name} M={M}")
+        check(y, y_ref, a_ref, f"{sh.name} M={M}", at=(ms, ns))
 
 
 @pytest.mark.parametrize("bits,gs", workloads.GROUP_BIT_SWEEP.variants)
@@ -136,10 +135,10 @@ def test_group_bit_sweep_sampled(torch_cuda, bits, gs):
     p = synth.make_problem(workloads.shape_seed(w, 0, bits=bits, group_size=gs), sh.N, sh.K, bits, gs)
     dp, ref = DeviceProblem(p), OracleRef(p)
     for M in w.ms:
-        y = to_f64(dp.run(M))
+        y = dp.run(M)
         ms, ns = sample_positions(M, sh.N, 96, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
-        assert_within(y[ms, ns], y_ref, a_ref, f"{bits}b g{gs} M={M}")
+        check(y, y_ref, a_ref, f"{bits}b g{gs} M={M}", at=(ms, ns))
 
 
 @pytest.mark.parametrize("shape_index", range(4))
@@ -149,10 +148,10 @@ def test_verify_step_shapes_sampled(torch_cuda, shape_index):
     p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
     dp, ref = DeviceProblem(p), OracleRef(p)
     for M in w.ms:
-        y = to_f64(dp.run(M))
+        y = dp.run(M)
         ms, ns = sample_positions(M, sh.N, 96, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
-        assert_within(y[ms, ns], y_ref, a_ref, f"{sh.name} M={M}")
+        check(y, y_ref, a_ref, f"{sh.name} M={M}", at=(ms, ns))
 
 
 @pytest.mark.parametrize("shape_index", range(2))
@@ -164,10 +163,10 @@ def test_int8_affine_sampled(torch_cuda, shape_index):
     p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
     dp, ref = DeviceProblem(p), OracleRef(p)
     for M in w.ms:
-        y = to_f64(dp.run(M))
+        y = dp.run(M)
         ms, ns = sample_positions(M, sh.N, 128, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
-        assert_within(y[ms, ns], y_ref, a_ref, f"int8 {sh.name} M={M}")
+        check(y, y_ref, a_ref, f"int8 {sh.name} M={M}", at=(ms, ns))
 
 
 # ------------------------------------------------------------- properties
