@@ -40,9 +40,9 @@ RAW_METRICS = [
 ]
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         h.update((CSRC / name).read_bytes())
     return h.hexdigest()[:16]
 
@@ -95,7 +95,10 @@ def main():
     ap.add_argument("--list-cmd", required=True)
     ap.add_argument("--full-cmd", required=True)
     ap.add_argument("--note", default="")
+    ap.add_argument("--sources", default=",".join(KERNEL_SOURCES),
+                    help="comma-separated csrc files whose hash the summary records (default: the TMA families')")
     a = ap.parse_args()
+    sources = tuple(x for x in a.sources.split(",") if x)
     lt = launch_table(Path(a.launches))
     rm = raw_metrics(Path(a.raw))
     reads = [to_float(v) for v in rm["dram__bytes_read.sum"][0]]
@@ -103,11 +106,14 @@ def main():
     unit_r, unit_w = rm["dram__bytes_read.sum"][1], rm["dram__bytes_write.sum"][1]
     mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     per_launch = [r * mult.get(unit_r, 1) + w * mult.get(unit_w, 1) for r, w in zip(reads, writes)]
-    family = next((f for f in ("qmm_own_kernel", "qmm_tma_kernel", "qmm_mma_kernel") if f in rm["kernel"]), rm["kernel"])
+    families = ("qmm_own_kernel", "qmm_tma_kernel", "qmm_mma_kernel", "ggml_to_affine_kernel")
+    family = next((f for f in families if f in rm["kernel"]), rm["kernel"])
     lines = [f"# ncu summary: {family} on {a.workload}", ""]
     if a.note:
         lines += [a.note, ""]
-    lines += ["kernel_source_hash: " + kernel_hash(),
+    if sources != KERNEL_SOURCES:
+        lines += ["Hashed sources: " + ", ".join(f"`{x}`" for x in sources), ""]
+    lines += ["kernel_source_hash: " + kernel_hash(sources),
               f"dram_bytes_per_launch: {sum(per_launch) / len(per_launch):.0f}", "",
               "## Launch list (per-launch times are cold-cache and serialized; compare shares)", "",
               "Command:", "", "```", a.list_cmd, "```", "",
