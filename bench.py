@@ -221,6 +221,7 @@ def configs_report(torch, dev, stream, peak):
     plan += [(workloads.GROUP_BIT_SWEEP, b, g, (1, 4, 8, 16)) for b, g in workloads.GROUP_BIT_SWEEP.variants]
     plan.append((workloads.VERIFY_STEP, None, None, (1, 4, 8)))
     plan.append((workloads.INT8_AFFINE, None, None, (1, 4, 8, 16)))
+    plan.append((workloads.QMV_WIDE_GATE_UP, None, None, (1, 2, 4, 8, 16)))
     for w, bits, gs, ms in plan:
         bits = bits or w.bits
         gs = gs or w.group_size

@@ -103,8 +103,9 @@ const VariantDesc kVariants[] = {
 };
 constexpr int kDefaultTma = 3;     // two CTAs per SM
 constexpr int kDefaultTma1 = 5;    // one CTA per SM, for wide K-pieces
-constexpr int kDefaultGatherOwn = 13;  // tma_own_w8_d2_2cta: the gathered form's default
-constexpr int kDefaultOwnWide = 8;     // tma_own_w16_d2_1cta: microscaling modes at M > 12
+constexpr int kDefaultOwn = 13;      // tma_own_w8_d2_2cta: the gathered form's default, and the
+                                      // fallback where the tma family cannot plan
+constexpr int kDefaultOwnWide = 8;   // tma_own_w16_d2_1cta: the same above 12 rows
 constexpr int kNumVariants = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
 constexpr int kMaxSplits = 16;
 
@@ -247,6 +248,23 @@ int rule_tma_cluster(const CallArgs& a, const VariantDesc& d) {
   return best;
 }
 
+// Warp-owned default for shapes the TMA family cannot plan (scale rows that
+// are not 16-byte strided): the two-CTA variant up to 12 rows, the one-CTA one
+// above (and each as the other's fallback, when shared memory is short), with
+// the first cluster size of (4, 2, 1, 8) the planner accepts; -1 if none.
+int rule_own(const CallArgs& a, int* splits) {
+  const int order[2] = {a.M > 12 ? kDefaultOwnWide : kDefaultOwn, a.M > 12 ? kDefaultOwn : kDefaultOwnWide};
+  for (int v : order) {
+    for (int c : {4, 2, 1, 8}) {
+      if (launch_own(a, kVariants[v], c, nullptr, true) == cudaSuccess) {
+        *splits = c;
+        return v;
+      }
+    }
+  }
+  return -1;
+}
+
 // The variant and split count for a call: the table's entry for the shape,
 // else the rule-based choice.  -2 for a table error (an unreadable QMM_TABLE
 // file, or an entry whose variant or split count is out of range).
@@ -266,6 +284,8 @@ int select_variant(const CallArgs& a, int* splits) {
       return v;
     }
   }
+  const int ov = rule_own(a, splits);
+  if (ov >= 0) return ov;
   *splits = rule_splits(kVariants[0], a.N, a.K, a.gs);
   return 0;
 }
@@ -504,6 +524,7 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
           break;
         }
       }
+      if (v < 0) v = rule_own(a, &s);
       if (v < 0) {
         v = 0;
         s = rule_splits(kVariants[0], a.N, a.K, a.gs);
@@ -675,7 +696,7 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   if (variant < 0 && T <= 16) {
     CallArgs ao = a;
     ao.M = T;
-    const VariantDesc& dd = kVariants[kDefaultGatherOwn];
+    const VariantDesc& dd = kVariants[kDefaultOwn];
     for (int cc : {4, 2, 1, 8}) {
       if (splits > 0 && cc != splits) continue;
       const cudaError_t pe = launch_own(ao, dd, cc, st, true);
@@ -803,7 +824,7 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   };
   const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
   if (variant < 0 || own_forced) {
-    const VariantDesc& dd = kVariants[own_forced ? variant : (M > 12 ? kDefaultOwnWide : kDefaultGatherOwn)];
+    const VariantDesc& dd = kVariants[own_forced ? variant : (M > 12 ? kDefaultOwnWide : kDefaultOwn)];
     for (int cc : {4, 2, 1, 8}) {
       if (splits > 0 && cc != splits) continue;
       const cudaError_t pe = own_mx(dd, cc, true);

@@ -258,14 +258,14 @@ struct GroupMath {
   }
 
   // acc += s * P + (b - OFFSET s) * sum x for one group.  meta_j -> fp16 scale of
-  // (row g, this group); row g + 8 at + 8 * mbw, the biases at + 16 * mbw and
-  // + 24 * mbw.  xs_j -> the group's activation sums (MP floats).
-  __device__ static void fold(const uint16_t* meta_j, int mbw, const float* xs_j, int t, const float (&tmp)[NB][4],
-                              float (&acc)[NB][4]) {
+  // (row g, this group); row g + 8 at + 8 * mbw, the biases at + bofs and
+  // + bofs + 8 * mbw.  xs_j -> the group's activation sums (MP floats).
+  __device__ static void fold(const uint16_t* meta_j, int mbw, int bofs, const float* xs_j, int t,
+                              const float (&tmp)[NB][4], float (&acc)[NB][4]) {
     const float s_lo = __half2float(__ushort_as_half(meta_j[0]));
     const float s_hi = __half2float(__ushort_as_half(meta_j[8 * mbw]));
-    const float b_lo = fmaf(-OFFSET, s_lo, __half2float(__ushort_as_half(meta_j[16 * mbw])));
-    const float b_hi = fmaf(-OFFSET, s_hi, __half2float(__ushort_as_half(meta_j[24 * mbw])));
+    const float b_lo = fmaf(-OFFSET, s_lo, __half2float(__ushort_as_half(meta_j[bofs])));
+    const float b_hi = fmaf(-OFFSET, s_hi, __half2float(__ushort_as_half(meta_j[bofs + 8 * mbw])));
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const float2 xs = *reinterpret_cast<const float2*>(xs_j + 8 * nb + 2 * t);

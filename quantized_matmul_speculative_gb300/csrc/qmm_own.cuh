@@ -46,7 +46,12 @@ struct OwnParams {
   int kp;                       // parts per tile K-piece
   int gq;                       // groups per part (gp / kp)
   int bw, nbox;                 // weight box width (words) and boxes per unit: nbox * bw = gq * words per group
-  int mbw;                      // scale/bias box width (halves)
+  int mbw;                      // scale/bias box width (halves); G with meta_tile
+  int bofs;                     // halves from a stage's scales to its biases: 16 * mbw, or with
+                                // meta_tile 16 * G rounded up to 128 bytes
+  int meta_tile;                // 1: a stage holds its tile's scales and biases for all G groups
+                                // ([16 rows][G] each), copied through a [rows*G/8, 8] view of the
+                                // [rows, G] arrays: their rows are not 16-byte strided (G % 8 != 0)
   int tiles;                    // 16-row tiles of W
   int ncl;                      // clusters in the grid
   int maxw;                     // receive slots per (tile, CTA): most warps that meet one tile
@@ -70,8 +75,9 @@ struct OwnParams {
 // and those rows only feed output columns that are never stored.
 struct OwnLayout {
   int x_off, xs_off, ring_off, w_bytes, stage_bytes, recv_off, slot_bytes, total, rsx;
-  // meta_row: bytes of scale/bias data per weight row of a unit (affine: fp16
-  // scales and biases, 2 * mbw halves; microscaling: mbw scale bytes).
+  // meta_row: shared-memory bytes of scale/bias data per weight row of a unit
+  // (affine: fp16 scales and biases, (bofs + 16 mbw) / 8, i.e. 4 mbw unless the
+  // biases are placed further; microscaling: mbw scale bytes).
   __host__ __device__ OwnLayout(int W, int D, int gp, int gs, int mp, int nb, int nbox, int bw, int meta_row,
                                 int owned_max, int csize, int maxw, int m) {
     const int nbar = W * D + owned_max;  // full barriers of the rings, then one per owned tile
@@ -104,7 +110,8 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int csize = static_cast<int>(gridDim.x);  // CTAs per cluster (cluster spans x)
   const int rank = static_cast<int>(blockIdx.x);
   const int q = static_cast<int>(blockIdx.y);
-  const int meta_row = MX ? p.mbw : 4 * p.mbw;
+  // shared memory per weight row of a stage for its metadata (bytes), and the bytes the copies deliver
+  const int meta_row = MX ? p.mbw : (p.bofs + 16 * p.mbw) / 8;
   const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, meta_row, p.owned_max, csize, p.maxw, p.M);
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x;
@@ -159,7 +166,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     }
     maxw = mw;
   }
-  const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + 16 * meta_row);
+  const uint32_t unit_bytes = static_cast<uint32_t>(L.w_bytes + (MX ? 16 * p.mbw : 64 * p.mbw));
 
   QMM_TRACE_POINT(0);
   if (lane == 0)
@@ -201,10 +208,15 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     if constexpr (MX) {
       const int mx0 = (gs0 / 16) * 16;  // 16-byte aligned start of the scale-byte box
       tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+    } else if (p.meta_tile) {
+      // rows n0 .. n0+15 of a [rows, G] array are the 2G view rows from n0*G/8 (n0*G is a multiple of 8)
+      const int vr = static_cast<int>((static_cast<int64_t>(n0) * p.mbw) >> 3);
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, 0, vr, full_bar(s));
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 2 * p.bofs), &tmap_b, 0, vr, full_bar(s));
     } else {
       const int mx0 = (gs0 / 8) * 8;  // 16-byte aligned start of the scale/bias box
       tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
-      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 16 * p.mbw * 2), &tmap_b, mx0, n0, full_bar(s));
+      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes + 2 * p.bofs), &tmap_b, mx0, n0, full_bar(s));
     }
   };
   if (lane == 0) {
@@ -310,9 +322,11 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     const unsigned char* stage = smem + L.ring_off + (warp * D + s) * L.stage_bytes;
     // Weights: [box][16 rows][bw words]; a group never straddles two boxes.
     const uint32_t* wst = reinterpret_cast<const uint32_t*>(stage) + ln.g * p.bw + ln.wofs;
-    // Scales then biases: [16 rows][mbw halves] each, from group (g0 + part*gq) rounded down to 8.
+    // Scales then biases: [16 rows][mbw halves] each, from group (g0 + part*gq) rounded down to 8
+    // (meta_tile: from group 0).
     const int gs0 = g0 + part * p.gq;
-    const uint16_t* meta = reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + ln.g * p.mbw + (gs0 % 8);
+    const uint16_t* meta =
+        reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + ln.g * p.mbw + (p.meta_tile ? gs0 : gs0 % 8);
     // (microscaling: [16 rows][mbw scale bytes], from group gs0 rounded down to 16)
     const uint8_t* meta8 = stage + L.w_bytes + ln.g * p.mbw + (gs0 % 16);
     const int jr = part * p.gq;  // the unit's first group within the K-piece
@@ -335,7 +349,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     };
     auto fold = [&](int j, const float (&tmp)[NB][4]) {
       if constexpr (MX) GM::fold_mx(meta8 + j, p.mbw, tmp, acc);
-      else GM::fold(meta + j, p.mbw, xsu + j * MP, ln.t, tmp, acc);
+      else GM::fold(meta + j, p.mbw, p.bofs, xsu + j * MP, ln.t, tmp, acc);
     };
     int j = 0;
     for (; NB == 1 && j + 3 < p.gq; j += 4) {  // four independent MMA chains

@@ -26,13 +26,23 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   constexpr int MP = 8 * NB;
   const int G = a.K / GS;
   if (G % csize != 0) return cudaErrorNotSupported;
+  bool meta_tile = false;
   if (MX) {
     // one scale byte per group: the rows of the byte tensor map must be 16-byte strided
     if (G % 16 != 0 || (reinterpret_cast<uintptr_t>(a.S8) & 15)) return cudaErrorNotSupported;
   } else {
-    if (G % 8 != 0) return cudaErrorNotSupported;  // scale/bias rows must be 16-byte strided
     if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
+    if (G % 8 != 0) {
+      // Scale/bias rows that are not 16-byte strided: each stage takes its whole tile's
+      // metadata as one box of 2G rows of a [rows*G/8, 8] view, which must hold every
+      // element (rows*G % 8 == 0; a gathered stack's matrices start on view rows too) and
+      // fit one box (2G <= 256).
+      const int64_t rows = GATHER ? static_cast<int64_t>(a.E) * a.N : a.N;
+      if (G > 128 || (rows * G) % 8 != 0 || (static_cast<int64_t>(a.N) * G) % 8 != 0) return cudaErrorNotSupported;
+      meta_tile = true;
+    }
   }
+  p->meta_tile = meta_tile ? 1 : 0;
   p->X = a.X;
   p->Y = a.Y;
   p->R = a.R;
@@ -107,9 +117,11 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     }
     if (bw == 0) continue;
     // scale box width: any start within 8 groups (fp16) or 16 groups (bytes) of the box start
-    const int mbw = MX ? (15 + gq + 15) / 16 * 16 : (7 + gq + 7) / 8 * 8;
+    const int mbw = MX ? (15 + gq + 15) / 16 * 16 : meta_tile ? G : (7 + gq + 7) / 8 * 8;
     if (mbw > 256) continue;
-    const int meta_row = MX ? mbw : 4 * mbw;
+    // the bias box starts 128-byte aligned in the stage, like every TMA destination
+    const int bofs = meta_tile ? (16 * G + 63) / 64 * 64 : 16 * mbw;
+    const int meta_row = MX ? mbw : (bofs + 16 * mbw) / 8;
     int maxw = 1;
     for (int nt : {nt_min, nt_max}) {
       if (nt < 1) continue;
@@ -149,6 +161,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     p->bw = bw;
     p->nbox = gq * GW / bw;
     p->mbw = mbw;
+    p->bofs = bofs;
     p->maxw = maxw;
     p->owned_max = owned_max;
     p->gather_off = GATHER ? total - gather_bytes : 0;
@@ -196,9 +209,13 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
     tmap_b = tmap_s;
   }
   for (int arr = 0; arr < (MX ? 0 : 2); ++arr) {
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(map_rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
+    // [rows, G] with a box of mbw groups x 16 rows; or (meta_tile) the [rows*G/8, 8] view, box 8 x 2G
+    const cuuint64_t gdim[2] = {p.meta_tile ? 8u : static_cast<cuuint64_t>(G),
+                                p.meta_tile ? static_cast<cuuint64_t>(map_rows) * G / 8
+                                            : static_cast<cuuint64_t>(map_rows)};
+    const cuuint64_t gstride[1] = {p.meta_tile ? 16u : static_cast<cuuint64_t>(G) * 2};
+    const cuuint32_t box[2] = {p.meta_tile ? 8u : static_cast<cuuint32_t>(p.mbw),
+                               p.meta_tile ? static_cast<cuuint32_t>(2 * G) : 16u};
     const cuuint32_t estride[2] = {1u, 1u};
     void* base = const_cast<uint16_t*>(arr ? a.B : a.S);
     if (encode(arr ? &tmap_b : &tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, gdim, gstride, box, estride,

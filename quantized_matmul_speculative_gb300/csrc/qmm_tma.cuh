@@ -262,7 +262,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   };
   // Fold group j's scale and bias into acc.
   auto group_fold = [&](const uint16_t* meta, int j, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
-    GM::fold(meta + j, p.mbw, xsum + j * C::MP, t, tmp, acc);
+    GM::fold(meta + j, p.mbw, 16 * p.mbw, xsum + j * C::MP, t, tmp, acc);
   };
 
   int s = 0, ph = 0;  // stage and phase parity of tile i

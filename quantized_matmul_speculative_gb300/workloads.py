@@ -96,10 +96,18 @@ INT8_AFFINE = Workload(
     shapes=(Shape("square", 5120, 5120), Shape("gate_up", 15360, 3840)),
     bits=8, group_size=64, ms=tuple(range(1, 17)), seed_base=6000,
     note="8-bit affine g64: the 5120x5120 layer and a 15360x3840 gate/up projection (the shape of the "
-         "pages' int8 qmv_wide measurement; its 60 groups per row take the mma family)",
+         "pages' int8 qmv_wide measurement; 60 groups per row, so its scale rows are not 16-byte strided)",
 )
 
-ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP, INT8_AFFINE)
+QMV_WIDE_GATE_UP = Workload(
+    name="qmv_wide_gate_up_15360x3840_4b_g64",
+    shapes=(Shape("gate_up", 15360, 3840),),
+    bits=4, group_size=64, ms=tuple(range(1, 17)), seed_base=8000,
+    note="the 15360x3840 gate/up projection of the pages' int4 qmv_wide measurement, 4-bit g64, M = 1..16 "
+         "(60 groups per row: scale rows not 16-byte strided)",
+)
+
+ALL = (SINGLE_LAYER, M_SWEEP, DENSE_27B_LAYER, GROUP_BIT_SWEEP, VERIFY_STEP, INT8_AFFINE, QMV_WIDE_GATE_UP)
 
 
 @dataclass(frozen=True)

@@ -63,15 +63,16 @@ def gather_variants():
     return list(range(len(binding.variant_names())))
 
 
-@pytest.mark.parametrize("groups", [4, 8], ids=["G4_mma_only", "G8_tma_too"])
+@pytest.mark.parametrize("groups", [4, 8], ids=["G4", "G8"])
 @pytest.mark.parametrize("bits,gs", [(4, 64), (2, 32), (8, 32), (4, 128)])
 def test_gather_small_stacks(torch_cuda, bits, gs, groups):
     """Ragged N, T = 1..16 tokens routed to k = 1..4 distinct experts, every
-    mma and tma variant, split 1 and 2, bf16 and fp32.  With 4 groups per row
-    only the mma variants take the shape."""
+    variant, split 1 and 2, bf16 and fp32.  With 4 groups per row (scale rows
+    not 16-byte strided) the row-stacking TMA variants cannot plan the shape and
+    the warp-owned ones take each tile's metadata whole."""
     torch = torch_cuda
     E, N, K = 6, 200, groups * gs
-    ran_tma = False
+    ran_tma = ran_own = False
     for T, k in ((1, 1), (3, 2), (8, 4), (16, 2), (5, 4)):
         mp = synth.make_moe(8100 + T * 10 + k + bits * 100 + gs + groups, E, N, K, bits, gs, T, k)
         ds = DeviceStack(torch, mp)
@@ -87,16 +88,18 @@ def test_gather_small_stacks(torch_cuda, bits, gs, groups):
                     except binding.QmmError as e:
                         assert e.status == 3 and binding.variant_names()[v].startswith("tma")
                         continue  # a tma / warp-owned variant that cannot plan this shape
-                    ran_tma |= binding.variant_names()[v].startswith("tma")
+                    ran_tma |= binding.variant_names()[v].startswith("tma_w")
+                    ran_own |= binding.variant_names()[v].startswith("tma_own")
                     check(y, y_ref, a_ref, f"T={T} k={k} v{v} s{s} {dt}")
-    assert ran_tma == (groups == 8)
+    assert ran_own and ran_tma == (groups == 8)
 
 
-@pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])
+@pytest.mark.parametrize("K", [256, 512], ids=["G4", "G8"])
 def test_gather_arbitrary_lists_and_determinism(torch_cuda, K):
     """A hand-made list with a repeated (token, expert) entry, unsorted experts
-    and an expert used by one entry only, on the default (mma) path and (8
-    groups per row) a forced tma variant; repeats are bit-identical."""
+    and an expert used by one entry only, at the library's choice, on a forced
+    mma and warp-owned variant and (8 groups per row) a forced tma variant;
+    repeats are bit-identical."""
     torch = torch_cuda
     mp = synth.make_moe(8200, 5, 136, K, 4, 64, 4, 1)
     ds = DeviceStack(torch, mp)
@@ -105,7 +108,8 @@ def test_gather_arbitrary_lists_and_determinism(torch_cuda, K):
     y_ref, a_ref = oracle_ref(mp, 4, lhs, rhs)
     tma = binding.variant_names().index("tma_w8_2cta")
     own = binding.variant_names().index("tma_own_w8_d2_2cta")
-    for v in ([-1, tma, own] if K == 512 else [-1]):
+    mma = binding.variant_names().index("mma_r2_wn2_wk4")
+    for v in ([-1, mma, tma, own] if K == 512 else [-1, mma, own]):
         first = ds.run(torch, 4, lhs, rhs, out_dtype=torch.float32, variant=v)
         assert_within(to_f64(first), y_ref, a_ref, f"hand-made list v{v}")
         assert torch.equal(first[1], first[6]), "a repeated entry gets the same row"
@@ -128,7 +132,7 @@ def test_gather_moe_workload_full(torch_cuda, T):
         check(y, y_ref, a_ref, f"moe T={T} v{v}")
 
 
-@pytest.mark.parametrize("K", [256, 512], ids=["mma", "tma"])
+@pytest.mark.parametrize("K", [256, 512], ids=["G4", "G8"])
 def test_gather_invalid_index_flagged(torch_cuda, K):
     """An expert index out of range: its row stays unwritten, the others are
     right, and the device status word reports bit 3."""
@@ -141,7 +145,8 @@ def test_gather_invalid_index_flagged(torch_cuda, K):
     y_ref, a_ref = oracle_ref(mp, 4, lhs[ok], rhs[ok])
     tma = binding.variant_names().index("tma_w8_2cta")
     own = binding.variant_names().index("tma_own_w8_d2_2cta")
-    for v in ([-1, tma, own] if K == 512 else [-1]):
+    mma = binding.variant_names().index("mma_r2_wn2_wk4")
+    for v in ([-1, mma, tma, own] if K == 512 else [-1, mma, own]):
         out = torch.full((4, 64), 5.0, dtype=torch.float32, device="cuda")
         ds.run(torch, 4, lhs, rhs, out=out, variant=v)
         torch.cuda.synchronize()
@@ -151,23 +156,26 @@ def test_gather_invalid_index_flagged(torch_cuda, K):
 
 
 def test_gather_too_many_entries_for_one_expert_flagged(torch_cuda):
-    """On the mma variants (4 groups per row: the default falls back to them),
-    a ninth entry for one expert with T <= 8 is flagged and that expert's rows
-    stay unwritten; the row-stacking variants (8 groups per row) take the same
-    list."""
+    """On the mma variants, a ninth entry for one expert with T <= 8 is flagged
+    and that expert's rows stay unwritten; the library's choice (warp-owned)
+    and the row-stacking variants (8 groups per row) take the same list."""
     torch = torch_cuda
+    names = binding.variant_names()
     mp = synth.make_moe(8301, 4, 64, 256, 4, 64, 4, 1)
     ds = DeviceStack(torch, mp)
     lhs9 = np.array([0, 1, 2, 3, 0, 1, 2, 3, 0], dtype=np.int32)
     rhs9 = np.zeros(9, dtype=np.int32)
     out9 = torch.full((9, 64), 5.0, dtype=torch.float32, device="cuda")
-    ds.run(torch, 4, lhs9, rhs9, out=out9)
+    ds.run(torch, 4, lhs9, rhs9, out=out9, variant=names.index("mma_r2_wn2_wk4"))
     torch.cuda.synchronize()
     assert binding.device_status(clear=True) & 8
     assert bool((out9 == 5.0).all())
+    y_ref, a_ref = oracle_ref(mp, 4, lhs9, rhs9)
+    y = ds.run(torch, 4, lhs9, rhs9, out_dtype=torch.float32)
+    assert_within(to_f64(y), y_ref, a_ref, "nine entries for one expert, 4 groups per row, default")
     mp8 = synth.make_moe(8302, 4, 64, 512, 4, 64, 4, 1)
     ds8 = DeviceStack(torch, mp8)
     y_ref, a_ref = oracle_ref(mp8, 4, lhs9, rhs9)
-    for v in (-1, binding.variant_names().index("tma_w8_2cta")):
+    for v in (-1, names.index("tma_w8_2cta")):
         y = ds8.run(torch, 4, lhs9, rhs9, out_dtype=torch.float32, variant=v)
         assert_within(to_f64(y), y_ref, a_ref, f"nine entries for one expert, v{v}")

@@ -154,11 +154,13 @@ def test_verify_step_shapes_sampled(torch_cuda, shape_index):
         check(y, y_ref, a_ref, f"{sh.name} M={M}", at=(ms, ns))
 
 
-@pytest.mark.parametrize("shape_index", range(2))
-def test_int8_affine_sampled(torch_cuda, shape_index):
-    """8-bit affine g64, M = 1..16 through the dispatcher: 5120x5120 and the
-    15360x3840 gate/up shape (60 groups per row: the mma family)."""
-    w = workloads.INT8_AFFINE
+@pytest.mark.parametrize("wname,shape_index", [("int8_affine_8b_g64", 0), ("int8_affine_8b_g64", 1),
+                                               ("qmv_wide_gate_up_15360x3840_4b_g64", 0)])
+def test_int8_and_qmv_wide_sampled(torch_cuda, wname, shape_index):
+    """M = 1..16 through the dispatcher: 8-bit affine g64 on 5120x5120 and on
+    the 15360x3840 gate/up shape, and that shape at 4 bits (60 groups per row:
+    scale rows that are not 16-byte strided)."""
+    w = workloads.BY_NAME[wname]
     sh = w.shapes[shape_index]
     p = synth.make_problem(workloads.shape_seed(w, shape_index), sh.N, sh.K, w.bits, w.group_size)
     dp, ref = DeviceProblem(p), OracleRef(p)
@@ -166,7 +168,52 @@ def test_int8_affine_sampled(torch_cuda, shape_index):
         y = dp.run(M)
         ms, ns = sample_positions(M, sh.N, 128, seed=M)
         y_ref, a_ref = ref.sampled(M, ms, ns)
-        check(y, y_ref, a_ref, f"int8 {sh.name} M={M}", at=(ms, ns))
+        check(y, y_ref, a_ref, f"{w.name} {sh.name} M={M}", at=(ms, ns))
+
+
+# ------------------------------------- scale rows that are not 16-byte strided
+# (bits, group size, groups per row G, N): G % 8 != 0, so a [N, G] fp16 row is
+# not a 16-byte multiple; N * G % 8 == 0 except in the last two, and the last
+# has G > 128.
+UNSTRIDED = [(4, 64, 60, 200), (4, 64, 45, 64), (8, 64, 60, 48), (2, 32, 30, 96), (4, 128, 30, 32),
+             (4, 64, 84, 160), (4, 32, 100, 64), (4, 64, 1, 16), (4, 64, 3, 40), (4, 64, 12, 18),
+             (4, 64, 60, 17), (4, 32, 130, 16)]
+
+
+@pytest.mark.parametrize("bits,gs,G,N", UNSTRIDED)
+def test_unstrided_scale_rows(torch_cuda, bits, gs, G, N):
+    """The warp-owned variants take such shapes (each stage holds its tile's
+    metadata for every group) when N * G is a multiple of 8 and G <= 128, and
+    refuse the others; the row-stacking TMA variants never run them.  Every
+    variant that runs, split 1..4, M = 1, 8, 9, 16, against the oracle; at
+    M = 1 the dispatcher falls back to a warp-owned variant exactly when one of
+    its two warp-owned defaults can plan the shape (the whole-tile metadata
+    takes 64 G bytes of every stage, so large G can run out of shared memory)."""
+    torch = torch_cuda
+    K = G * gs
+    p = synth.make_problem(9700 + G + N + bits, N, K, bits, gs)
+    dp, ref = DeviceProblem(p), OracleRef(p)
+    y_ref, a_ref = ref.full(16)
+    names = binding.variant_names()
+    own_ok = N * G % 8 == 0 and G <= 128
+    defaults = {"tma_own_w8_d2_2cta", "tma_own_w16_d2_1cta"}  # the dispatcher's warp-owned fallbacks
+    ran_own = default_ran_m1 = False
+    for v in variants():
+        for splits in (1, 2, 3, 4):
+            for M in (1, 8, 9, 16):
+                y = dp.run(M, out_dtype=torch.float32, variant=v, splits=splits, allow_unsupported=is_tma(v))
+                if y is None:  # (a warp-owned variant may also refuse for shared memory or G % splits)
+                    continue
+                assert not names[v].startswith("tma_w"), f"{names[v]} planned G={G}"
+                assert own_ok or not names[v].startswith("tma_own"), f"{names[v]} took N*G % 8 != 0 or G > 128"
+                ran_own |= names[v].startswith("tma_own")
+                default_ran_m1 |= M == 1 and names[v] in defaults
+                assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"G={G} N={N} {names[v]}/{splits} M={M}")
+    assert ran_own == own_ok
+    v, s = binding.select_variant(1, N, K, bits, gs)
+    assert names[v].startswith("tma_own") == default_ran_m1, f"dispatcher chose {names[v]} for G={G} M=1"
+    for M in (1, 9, 16):
+        check(dp.run(M), y_ref[:M], a_ref[:M], f"G={G} N={N} dispatcher M={M}")
 
 
 # ------------------------------------------------------------- properties
