@@ -571,39 +571,72 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
 
 namespace qmm {
 
-// ggml block -> affine layout, one thread per block of 32 weights (the block
-// layouts are described in qmm.h).  Codes keep their values (Q4) or flip the
-// sign bit (Q8_0: q + 128); the fp16 scale is d; the bias is -8 d (Q4_0), m
-// (Q4_1) or -128 d (Q8_0), products by powers of two and so exact in fp16.
-__global__ void ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk,
-                                      uint32_t* __restrict__ Wq, uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= nblk) return;
+// ggml block -> affine layout (the block layouts are described in qmm.h).
+// A CTA of kGgmlThreads threads converts as many consecutive blocks: it first
+// copies their bytes into shared memory with coalesced loads (4-byte words when
+// the span is 4-byte aligned), then each thread rewrites one block.  Codes keep
+// their values (Q4) or flip the sign bit (Q8_0: q + 128); the fp16 scale is d;
+// the bias is -8 d (Q4_0), m (Q4_1) or -128 d (Q8_0), products by powers of two
+// and so exact in fp16.  A block's code words are stored as 16-byte vectors
+// when Wq is 16-byte aligned.
+constexpr int kGgmlThreads = 256;
+
+__global__ void __launch_bounds__(kGgmlThreads)
+ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk, uint32_t* __restrict__ Wq,
+                      uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
+  __shared__ __align__(16) uint8_t span[kGgmlThreads * 34];
   const int nbytes = type == 0 ? 18 : type == 1 ? 20 : 34;
-  const uint8_t* blk = blocks + i * nbytes;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kGgmlThreads;
+  const int count = static_cast<int>((nblk - first < kGgmlThreads) ? nblk - first : kGgmlThreads);
+  const uint8_t* src = blocks + first * nbytes;
+  const int bytes = count * nbytes;
+  int done = 0;
+  if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
+    const int words = bytes >> 2;
+    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(span);
+    for (int w = threadIdx.x; w < words; w += kGgmlThreads) d32[w] = __ldg(s32 + w);
+    done = words << 2;
+  }
+  for (int b = done + threadIdx.x; b < bytes; b += kGgmlThreads) span[b] = __ldg(src + b);
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) >= count) return;
+  const int64_t i = first + threadIdx.x;
+  const uint8_t* blk = span + threadIdx.x * nbytes;
   const uint16_t d = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
   const float df = __half2float(__ushort_as_half(d));
   S[i] = d;
+  uint32_t words[8];
+  int nw;
   if (type == 2) {
+    nw = 8;
     for (int w = 0; w < 8; ++w) {
       const uint8_t* q = blk + 2 + 4 * w;
-      Wq[i * 8 + w] = static_cast<uint32_t>(q[0] ^ 0x80u) | (static_cast<uint32_t>(q[1] ^ 0x80u) << 8) |
-                      (static_cast<uint32_t>(q[2] ^ 0x80u) << 16) | (static_cast<uint32_t>(q[3] ^ 0x80u) << 24);
+      words[w] = static_cast<uint32_t>(q[0] ^ 0x80u) | (static_cast<uint32_t>(q[1] ^ 0x80u) << 8) |
+                 (static_cast<uint32_t>(q[2] ^ 0x80u) << 16) | (static_cast<uint32_t>(q[3] ^ 0x80u) << 24);
     }
     B[i] = __half_as_ushort(__float2half_rn(-128.f * df));
-    return;
-  }
-  const uint8_t* qs = blk + (type == 0 ? 2 : 4);
-  for (int w = 0; w < 4; ++w) {
-    uint32_t word = 0;
-    for (int t = 0; t < 8; ++t) {
-      const int e = 8 * w + t;
-      const uint32_t c = (e < 16) ? (qs[e] & 15u) : (qs[e - 16] >> 4);
-      word |= c << (4 * t);
+  } else {
+    nw = 4;
+    const uint8_t* qs = blk + (type == 0 ? 2 : 4);
+    for (int w = 0; w < 4; ++w) {
+      uint32_t word = 0;
+      for (int t = 0; t < 8; ++t) {
+        const int e = 8 * w + t;
+        const uint32_t c = (e < 16) ? (qs[e] & 15u) : (qs[e - 16] >> 4);
+        word |= c << (4 * t);
+      }
+      words[w] = word;
     }
-    Wq[i * 4 + w] = word;
+    B[i] = (type == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : static_cast<uint16_t>(blk[2] | (blk[3] << 8));
   }
-  B[i] = (type == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : static_cast<uint16_t>(blk[2] | (blk[3] << 8));
+  uint32_t* dst = Wq + i * nw;
+  if ((reinterpret_cast<uintptr_t>(Wq) & 15) == 0) {
+    for (int v = 0; v < nw / 4; ++v)
+      reinterpret_cast<uint4*>(dst)[v] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
+  } else {
+    for (int w = 0; w < nw; ++w) dst[w] = words[w];
+  }
 }
 
 }  // namespace qmm
@@ -618,10 +651,10 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
   if (nblk == 0) return QMM_OK;
   if (blocks == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
   if (!aligned(Wq, 4) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
-  const int threads = 256;
-  const int64_t grid = (nblk + threads - 1) / threads;
+  const int64_t grid = (nblk + qmm::kGgmlThreads - 1) / qmm::kGgmlThreads;
   if (grid > 0x7fffffff) return QMM_ERR_SHAPE;
-  qmm::ggml_to_affine_kernel<<<static_cast<unsigned int>(grid), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+  qmm::ggml_to_affine_kernel<<<static_cast<unsigned int>(grid), qmm::kGgmlThreads, 0,
+                               static_cast<cudaStream_t>(stream)>>>(
       type, static_cast<const uint8_t*>(blocks), nblk, Wq, static_cast<uint16_t*>(scales),
       static_cast<uint16_t*>(biases));
   const cudaError_t e = cudaGetLastError();

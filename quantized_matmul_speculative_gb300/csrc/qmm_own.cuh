@@ -51,7 +51,8 @@ struct OwnParams {
                                 // meta_tile 16 * G rounded up to 128 bytes
   int meta_tile;                // 1: a stage holds its tile's scales and biases for all G groups
                                 // ([16 rows][G] each), copied through a [rows*G/8, 8] view of the
-                                // [rows, G] arrays: their rows are not 16-byte strided (G % 8 != 0)
+                                // [rows, G] arrays: their rows are not 16-byte strided (G % 8 != 0);
+                                // microscaling: the scale bytes, through a [rows*G/16, 16] view
   int tiles;                    // 16-row tiles of W
   int ncl;                      // clusters in the grid
   int maxw;                     // receive slots per (tile, CTA): most warps that meet one tile
@@ -206,8 +207,13 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     for (int b = 0; b < p.nbox; ++b)
       tma_load_2d(dst + static_cast<uint32_t>(b * 16 * p.bw * 4), &tmap, gs0 * GW + b * p.bw, n0, full_bar(s));
     if constexpr (MX) {
-      const int mx0 = (gs0 / 16) * 16;  // 16-byte aligned start of the scale-byte box
-      tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+      if (p.meta_tile) {  // rows n0 .. n0+15 are the G view rows from n0*G/16
+        const int vr = static_cast<int>((static_cast<int64_t>(n0) * p.mbw) >> 4);
+        tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, 0, vr, full_bar(s));
+      } else {
+        const int mx0 = (gs0 / 16) * 16;  // 16-byte aligned start of the scale-byte box
+        tma_load_2d(dst + static_cast<uint32_t>(L.w_bytes), &tmap_s, mx0, n0, full_bar(s));
+      }
     } else if (p.meta_tile) {
       // rows n0 .. n0+15 of a [rows, G] array are the 2G view rows from n0*G/8 (n0*G is a multiple of 8)
       const int vr = static_cast<int>((static_cast<int64_t>(n0) * p.mbw) >> 3);
@@ -327,8 +333,8 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     const int gs0 = g0 + part * p.gq;
     const uint16_t* meta =
         reinterpret_cast<const uint16_t*>(stage + L.w_bytes) + ln.g * p.mbw + (p.meta_tile ? gs0 : gs0 % 8);
-    // (microscaling: [16 rows][mbw scale bytes], from group gs0 rounded down to 16)
-    const uint8_t* meta8 = stage + L.w_bytes + ln.g * p.mbw + (gs0 % 16);
+    // (microscaling: [16 rows][mbw scale bytes], from group gs0 rounded down to 16, or from group 0)
+    const uint8_t* meta8 = stage + L.w_bytes + ln.g * p.mbw + (p.meta_tile ? gs0 : gs0 % 16);
     const int jr = part * p.gq;  // the unit's first group within the K-piece
     const uint16_t* xu = xrow + jr * GS;
     const float* xsu = xsum + jr * MP;

@@ -28,8 +28,13 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   if (G % csize != 0) return cudaErrorNotSupported;
   bool meta_tile = false;
   if (MX) {
-    // one scale byte per group: the rows of the byte tensor map must be 16-byte strided
-    if (G % 16 != 0 || (reinterpret_cast<uintptr_t>(a.S8) & 15)) return cudaErrorNotSupported;
+    // one scale byte per group: rows that are not 16-byte strided (G % 16 != 0) are copied a
+    // whole tile at a time through a [rows*G/16, 16] view (rows*G % 16 == 0, one box: G <= 256)
+    if (reinterpret_cast<uintptr_t>(a.S8) & 15) return cudaErrorNotSupported;
+    if (G % 16 != 0) {
+      if (G > 256 || (static_cast<int64_t>(a.N) * G) % 16 != 0) return cudaErrorNotSupported;
+      meta_tile = true;
+    }
   } else {
     if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorNotSupported;
     if (G % 8 != 0) {
@@ -117,7 +122,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     }
     if (bw == 0) continue;
     // scale box width: any start within 8 groups (fp16) or 16 groups (bytes) of the box start
-    const int mbw = MX ? (15 + gq + 15) / 16 * 16 : meta_tile ? G : (7 + gq + 7) / 8 * 8;
+    const int mbw = meta_tile ? G : MX ? (15 + gq + 15) / 16 * 16 : (7 + gq + 7) / 8 * 8;
     if (mbw > 256) continue;
     // the bias box starts 128-byte aligned in the stage, like every TMA destination
     const int bofs = meta_tile ? (16 * G + 63) / 64 * 64 : 16 * mbw;
@@ -197,10 +202,14 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
   }
   const int G = a.K / GS;
   if (MX) {
-    // one byte per (row, group); the bias map is not read (a copy stands in for it)
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(map_rows)};
-    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(G)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.mbw), 16u};
+    // one byte per (row, group); the bias map is not read (a copy stands in for it).  [rows, G]
+    // with a box of mbw groups x 16 rows, or (meta_tile) the [rows*G/16, 16] view, box 16 x G
+    const cuuint64_t gdim[2] = {p.meta_tile ? 16u : static_cast<cuuint64_t>(G),
+                                p.meta_tile ? static_cast<cuuint64_t>(map_rows) * G / 16
+                                            : static_cast<cuuint64_t>(map_rows)};
+    const cuuint64_t gstride[1] = {p.meta_tile ? 16u : static_cast<cuuint64_t>(G)};
+    const cuuint32_t box[2] = {p.meta_tile ? 16u : static_cast<cuuint32_t>(p.mbw),
+                               p.meta_tile ? static_cast<cuuint32_t>(G) : 16u};
     const cuuint32_t estride[2] = {1u, 1u};
     if (encode(&tmap_s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.S8), gdim, gstride, box, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

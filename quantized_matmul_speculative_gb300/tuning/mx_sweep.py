@@ -5,6 +5,10 @@ graph of 48 calls over rotating weight copies (> 4x L2), median of 5 replays.
 One JSON object per (shape, format, M) with the four fastest choices.
 
     python -m quantized_matmul_speculative_gb300.tuning.mx_sweep --out mx_sweep.jsonl
+        [--shapes 2880x2880,5120x5120] [--with-mma]
+
+--shapes replaces the two square shapes (N x K); --with-mma times the mma
+variants too.
 """
 from __future__ import annotations
 
@@ -24,17 +28,22 @@ from quantized_matmul_speculative_gb300 import binding, build, synth  # noqa: E4
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", required=True)
+    ap.add_argument("--shapes", default="5120x5120,8192x8192")
+    ap.add_argument("--with-mma", action="store_true")
     args = ap.parse_args()
+    shapes = [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
     import torch
 
     build.build()
     binding.lib()
     names = binding.variant_names()
     own = [i for i, n in enumerate(names) if n.startswith("tma_own") and not n.endswith("_half")]
+    if args.with_mma:
+        own += [i for i, n in enumerate(names) if n.startswith("mma")]
     st = torch.cuda.Stream()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     out = open(args.out, "w")
-    for N, K in ((5120, 5120), (8192, 8192)):
+    for N, K in shapes:
         for fmt, (f, bits, g) in binding.MX_FORMATS.items():
             q, sc = synth.make_mx(1, N, K, fmt)
             cb = N * K * bits // 8 + N * K // g

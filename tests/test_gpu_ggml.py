@@ -88,3 +88,30 @@ def test_ggml_product(torch_cuda, kind):
         y = binding.small_m(x[:M].contiguous(), wq, s, b, bits, 32)
         ms, ns = sample_positions(M, N, 256, seed=M)
         check(y, y_ref[ms, ns], a_ref[ms, ns], f"{kind} 4096 M={M}", at=(ms, ns))
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_conversion_unaligned_buffers(torch_cuda, kind):
+    """The conversion's byte-wise staging (a block buffer that starts on an odd
+    address) and its word-wise stores (code words 4- but not 16-byte aligned),
+    over a partial last CTA of blocks: still exact."""
+    torch = torch_cuda
+    N, K = 29, 352  # 319 blocks: one full CTA of 256 and a partial one
+    blocks = synth.make_ggml_blocks(8700, N, K, kind)
+    t, nbytes, bits = binding.GGML_TYPES[kind]
+    raw = torch.zeros(blocks.size + 1, dtype=torch.uint8, device="cuda")
+    raw[1:] = torch.from_numpy(blocks.reshape(-1)).cuda()
+    words = N * K * bits // 32
+    wq_buf = torch.zeros(words + 1, dtype=torch.int32, device="cuda")
+    s = torch.empty((N, K // 32), dtype=torch.float16, device="cuda")
+    b = torch.empty((N, K // 32), dtype=torch.float16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = binding.lib().qmm_from_ggml(t, raw.data_ptr() + 1, N, K, wq_buf.data_ptr() + 4, s.data_ptr(), b.data_ptr(),
+                                     stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    ol = oracle.load()
+    w_conv = ol.dequant(wq_buf[1:].cpu().numpy().view(np.uint32).reshape(N, -1), s.cpu().numpy().view(np.uint16),
+                        b.cpu().numpy().view(np.uint16), K, bits, 32)
+    assert np.array_equal(w_conv, ol.ggml_dequant(kind, blocks, N, K))
+    assert int(wq_buf[0]) == 0, "a word before Wq was written"

@@ -110,17 +110,31 @@ def test_mx_products(torch_cuda, fmt, bits):
 
 
 @pytest.mark.parametrize("fmt,bits", FORMATS)
-def test_mx_fallback_shape(torch_cuda, fmt, bits):
-    """K = 256 leaves 8 (mx) or 16 (nvfp4: still fine) scale bytes per row: the
-    default falls back to the mma family where the warp-owned one cannot
-    plan; both give the oracle's result."""
+@pytest.mark.parametrize("N,K", [(72, 256), (71, 256), (64, 2880), (16, 8224)])
+def test_mx_unstrided_scale_rows(torch_cuda, fmt, bits, N, K):
+    """Scale-byte rows that are not 16-byte strided (K/g not a multiple of 16:
+    8 or 90 bytes per row; nvfp4's 16 and 180): the warp-owned family copies
+    each tile's scale bytes whole when N * K/g is a multiple of 16 and K/g <=
+    256, and refuses otherwise (71 rows; 257 groups), where the default falls
+    back to the mma family.  Default, a forced warp-owned and a forced mma
+    variant against the oracle."""
     torch = torch_cuda
-    N, K = 72, 256
-    q, sc = synth.make_mx(8602, N, K, fmt)
+    q, sc = synth.make_mx(8602 + N + K, N, K, fmt)
     wq, s = upload(torch, q, sc, bits)
     xb = synth.make_x(8602, K)
     x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
     y_ref, a_ref = oracle.load().mx_qmm(fmt, xb, binding.pack(q, bits), sc)
+    G = K // binding.MX_FORMATS[fmt][2]
+    own_ok = (N * G) % 16 == 0 and G <= 256
+    names = binding.variant_names()
     for M in (1, 9):
         y = binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.float32)
-        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{fmt} K=256 M={M}")
+        assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{fmt} N={N} K={K} M={M} default")
+        for v in (names.index("tma_own_w8_d2_2cta"), names.index("mma_r2_wn2_wk4")):
+            try:
+                y = binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=torch.float32, variant=v)
+            except binding.QmmError as e:
+                assert e.status == 3 and names[v].startswith("tma_own") and not own_ok, f"{names[v]}: {e}"
+                continue
+            assert own_ok or not names[v].startswith("tma_own"), f"{names[v]} took G={G} N={N}"
+            assert_within(to_f64(y), y_ref[:M], a_ref[:M], f"{fmt} N={N} K={K} M={M} {names[v]}")
