@@ -572,37 +572,20 @@ qmm_status run_call(const void* X, const uint32_t* Wq, const void* scales, const
 namespace qmm {
 
 // ggml block -> affine layout (the block layouts are described in qmm.h).
-// A CTA of kGgmlThreads threads converts as many consecutive blocks: it first
-// copies their bytes into shared memory with coalesced loads (4-byte words when
-// the span is 4-byte aligned), then each thread rewrites one block.  Codes keep
-// their values (Q4) or flip the sign bit (Q8_0: q + 128); the fp16 scale is d;
-// the bias is -8 d (Q4_0), m (Q4_1) or -128 d (Q8_0), products by powers of two
-// and so exact in fp16.  A block's code words are stored as 16-byte vectors
-// when Wq is 16-byte aligned.
+// A CTA of kGgmlThreads threads converts kGgmlBlocks consecutive blocks: it
+// first copies their bytes into shared memory with coalesced loads (4-byte
+// words, eight in flight per thread, when the span is 4-byte aligned), then
+// each thread rewrites blocks t, t + kGgmlThreads.  Codes keep their values
+// (Q4) or flip the sign bit (Q8_0: q + 128); the fp16 scale is d; the bias is
+// -8 d (Q4_0), m (Q4_1) or -128 d (Q8_0), products by powers of two and so
+// exact in fp16.  A block's code words are stored as 16-byte vectors when Wq
+// is 16-byte aligned.
 constexpr int kGgmlThreads = 256;
+constexpr int kGgmlBlocks = 512;
 
-__global__ void __launch_bounds__(kGgmlThreads)
-ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk, uint32_t* __restrict__ Wq,
-                      uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
-  __shared__ __align__(16) uint8_t span[kGgmlThreads * 34];
-  const int nbytes = type == 0 ? 18 : type == 1 ? 20 : 34;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kGgmlThreads;
-  const int count = static_cast<int>((nblk - first < kGgmlThreads) ? nblk - first : kGgmlThreads);
-  const uint8_t* src = blocks + first * nbytes;
-  const int bytes = count * nbytes;
-  int done = 0;
-  if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
-    const int words = bytes >> 2;
-    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
-    uint32_t* d32 = reinterpret_cast<uint32_t*>(span);
-    for (int w = threadIdx.x; w < words; w += kGgmlThreads) d32[w] = __ldg(s32 + w);
-    done = words << 2;
-  }
-  for (int b = done + threadIdx.x; b < bytes; b += kGgmlThreads) span[b] = __ldg(src + b);
-  __syncthreads();
-  if (static_cast<int>(threadIdx.x) >= count) return;
-  const int64_t i = first + threadIdx.x;
-  const uint8_t* blk = span + threadIdx.x * nbytes;
+// Block i (bytes at blk) into its code words, scale and bias.
+__device__ __forceinline__ void convert_ggml_block(int type, const uint8_t* blk, int64_t i, uint32_t* __restrict__ Wq,
+                                                   uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
   const uint16_t d = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
   const float df = __half2float(__ushort_as_half(d));
   S[i] = d;
@@ -639,6 +622,36 @@ ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk
   }
 }
 
+__global__ void __launch_bounds__(kGgmlThreads)
+ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk, uint32_t* __restrict__ Wq,
+                      uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
+  __shared__ __align__(16) uint8_t span[kGgmlBlocks * 34];
+  const int nbytes = type == 0 ? 18 : type == 1 ? 20 : 34;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kGgmlBlocks;
+  const int count = static_cast<int>((nblk - first < kGgmlBlocks) ? nblk - first : kGgmlBlocks);
+  const uint8_t* src = blocks + first * nbytes;
+  const int bytes = count * nbytes;
+  int done = 0;
+  if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
+    const int words = bytes >> 2;
+    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(span);
+    int w = threadIdx.x;
+    for (; w + 7 * kGgmlThreads < words; w += 8 * kGgmlThreads) {  // eight loads in flight
+      uint32_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldg(s32 + w + k * kGgmlThreads);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) d32[w + k * kGgmlThreads] = v[k];
+    }
+    for (; w < words; w += kGgmlThreads) d32[w] = __ldg(s32 + w);
+    done = words << 2;
+  }
+  for (int b = done + threadIdx.x; b < bytes; b += kGgmlThreads) span[b] = __ldg(src + b);
+  __syncthreads();
+  for (int t = threadIdx.x; t < count; t += kGgmlThreads) convert_ggml_block(type, span + t * nbytes, first + t, Wq, S, B);
+}
+
 }  // namespace qmm
 
 extern "C" {
@@ -651,7 +664,7 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
   if (nblk == 0) return QMM_OK;
   if (blocks == nullptr || Wq == nullptr || scales == nullptr || biases == nullptr) return QMM_ERR_NULL;
   if (!aligned(Wq, 4) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
-  const int64_t grid = (nblk + qmm::kGgmlThreads - 1) / qmm::kGgmlThreads;
+  const int64_t grid = (nblk + qmm::kGgmlBlocks - 1) / qmm::kGgmlBlocks;
   if (grid > 0x7fffffff) return QMM_ERR_SHAPE;
   qmm::ggml_to_affine_kernel<<<static_cast<unsigned int>(grid), qmm::kGgmlThreads, 0,
                                static_cast<cudaStream_t>(stream)>>>(

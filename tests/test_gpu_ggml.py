@@ -96,7 +96,7 @@ def test_conversion_unaligned_buffers(torch_cuda, kind):
     address) and its word-wise stores (code words 4- but not 16-byte aligned),
     over a partial last CTA of blocks: still exact."""
     torch = torch_cuda
-    N, K = 29, 352  # 319 blocks: one full CTA of 256 and a partial one
+    N, K = 29, 640  # 580 blocks: one full CTA of 512 blocks and a partial one
     blocks = synth.make_ggml_blocks(8700, N, K, kind)
     t, nbytes, bits = binding.GGML_TYPES[kind]
     raw = torch.zeros(blocks.size + 1, dtype=torch.uint8, device="cuda")
