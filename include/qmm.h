@@ -83,8 +83,11 @@ qmm_status qmm_small_m(const void* X, const uint32_t* Wq, const void* scales, co
  * the number of CTAs that split K inside one thread-block cluster (splits = -1:
  * the table's or the variant's default; 1..16 otherwise).  A (variant, splits)
  * pair the shape cannot use returns QMM_ERR_UNSUPPORTED and launches nothing:
- * the "tma" variants need K/group_size to be a multiple of 8 and of splits,
- * and 16-byte aligned scales and biases.                                       */
+ * the "tma" variants need K/group_size (G) to be a multiple of splits and
+ * 16-byte aligned scales and biases; the row-stacking "tma_w*" ones also need
+ * G to be a multiple of 8, the warp-owned "tma_own_*" ones take other G when
+ * N*G is a multiple of 8 and G <= 128 (each stage then holds its tile's scales
+ * and biases for all G groups), shared memory permitting.                     */
 qmm_status qmm_small_m_ex(const void* X, const uint32_t* Wq, const void* scales, const void* biases,
                           int M, int N, int K, int bits, int group_size, void* Y,
                           int out_dtype, int variant, int splits, void* stream);
@@ -161,8 +164,9 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
  * microscaling format; source of the modes: "MLX quantized_matmul small-M
  * verify kernels", facts "Fix family 1" / "qmv_wide covers affine, nvfp4,
  * mxfp4, mxfp8".  variant -1: the warp-owned family when it can plan the
- * shape (K/g a multiple of 16 and of the cluster size, scales 16-byte
- * aligned), else the first "mma" variant; a forced "mma" or "tma_own"
+ * shape (K/g a multiple of the cluster size, scales 16-byte aligned, and K/g
+ * a multiple of 16 or else N*K/g a multiple of 16 with K/g <= 256), else the
+ * first "mma" variant; a forced "mma" or "tma_own"
  * variant is used as given, a "tma" variant returns QMM_ERR_UNSUPPORTED.
  * QMM_NVFP4: FP4 E2M1 codes with one FP8 E4M3 scale byte per group of 16,
  * scales uint8 [N, K/16] (a per-tensor scale, where a model has one, is left
