@@ -44,7 +44,7 @@ def random_case(seed):
     return rng, bits, gs, n, groups * gs, m
 
 
-@pytest.mark.parametrize("seed", range(32))
+@pytest.mark.parametrize("seed", range(128))
 def test_random_shape(torch_cuda, seed):
     torch = torch_cuda
     rng, bits, gs, n, k, m = random_case(seed)
