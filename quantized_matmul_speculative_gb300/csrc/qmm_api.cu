@@ -583,54 +583,67 @@ namespace qmm {
 constexpr int kGgmlThreads = 256;
 constexpr int kGgmlBlocks = 512;
 
-// Block i (bytes at blk) into its code words, scale and bias.
-__device__ __forceinline__ void convert_ggml_block(int type, const uint8_t* blk, int64_t i, uint32_t* __restrict__ Wq,
-                                                   uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
-  const uint16_t d = static_cast<uint16_t>(blk[0] | (blk[1] << 8));
+// Four bytes at a 2-byte aligned shared-memory address, as a little-endian word.
+__device__ __forceinline__ uint32_t ggml_word(const uint8_t* p) {
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
+  return static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 16);
+}
+
+// The low nibbles of the eight bytes of (lo, hi), byte k's at bits 4k.
+__device__ __forceinline__ uint32_t ggml_low_nibbles(uint32_t lo, uint32_t hi) {
+  auto four = [](uint32_t x) {
+    x &= 0x0F0F0F0Fu;
+    x = (x | (x >> 4)) & 0x00FF00FFu;
+    return (x | (x >> 8)) & 0x0000FFFFu;
+  };
+  return four(lo) | (four(hi) << 16);
+}
+
+// Block i (bytes at blk, 2-byte aligned) into its code words, scale and bias.
+// Q4: byte j of the 16 code bytes holds weight j (low nibble) and weight j+16
+// (high nibble), so word 0 = the low nibbles of bytes 0..7, word 1 = those of
+// bytes 8..15, words 2 and 3 = the high nibbles.
+template <int TYPE>
+__device__ __forceinline__ void convert_ggml_block(const uint8_t* blk, int64_t i, uint32_t* __restrict__ Wq,
+                                                   uint16_t* __restrict__ S, uint16_t* __restrict__ B, bool vec) {
+  const uint16_t d = *reinterpret_cast<const uint16_t*>(blk);
   const float df = __half2float(__ushort_as_half(d));
   S[i] = d;
-  uint32_t words[8];
-  int nw;
-  if (type == 2) {
-    nw = 8;
-    for (int w = 0; w < 8; ++w) {
-      const uint8_t* q = blk + 2 + 4 * w;
-      words[w] = static_cast<uint32_t>(q[0] ^ 0x80u) | (static_cast<uint32_t>(q[1] ^ 0x80u) << 8) |
-                 (static_cast<uint32_t>(q[2] ^ 0x80u) << 16) | (static_cast<uint32_t>(q[3] ^ 0x80u) << 24);
-    }
+  constexpr int NW = TYPE == 2 ? 8 : 4;
+  uint32_t w[NW];
+  if constexpr (TYPE == 2) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = ggml_word(blk + 2 + 4 * k) ^ 0x80808080u;
     B[i] = __half_as_ushort(__float2half_rn(-128.f * df));
   } else {
-    nw = 4;
-    const uint8_t* qs = blk + (type == 0 ? 2 : 4);
-    for (int w = 0; w < 4; ++w) {
-      uint32_t word = 0;
-      for (int t = 0; t < 8; ++t) {
-        const int e = 8 * w + t;
-        const uint32_t c = (e < 16) ? (qs[e] & 15u) : (qs[e - 16] >> 4);
-        word |= c << (4 * t);
-      }
-      words[w] = word;
-    }
-    B[i] = (type == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : static_cast<uint16_t>(blk[2] | (blk[3] << 8));
+    const uint8_t* qs = blk + (TYPE == 0 ? 2 : 4);
+    const uint32_t b0 = ggml_word(qs), b1 = ggml_word(qs + 4), b2 = ggml_word(qs + 8), b3 = ggml_word(qs + 12);
+    w[0] = ggml_low_nibbles(b0, b1);
+    w[1] = ggml_low_nibbles(b2, b3);
+    w[2] = ggml_low_nibbles(b0 >> 4, b1 >> 4);
+    w[3] = ggml_low_nibbles(b2 >> 4, b3 >> 4);
+    B[i] = (TYPE == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : *reinterpret_cast<const uint16_t*>(blk + 2);
   }
-  uint32_t* dst = Wq + i * nw;
-  if ((reinterpret_cast<uintptr_t>(Wq) & 15) == 0) {
-    for (int v = 0; v < nw / 4; ++v)
-      reinterpret_cast<uint4*>(dst)[v] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
+  uint32_t* dst = Wq + i * NW;
+  if (vec) {
+#pragma unroll
+    for (int v = 0; v < NW / 4; ++v) reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
   } else {
-    for (int w = 0; w < nw; ++w) dst[w] = words[w];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) dst[k] = w[k];
   }
 }
 
+template <int TYPE>
 __global__ void __launch_bounds__(kGgmlThreads)
-ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk, uint32_t* __restrict__ Wq,
+ggml_to_affine_kernel(const uint8_t* __restrict__ blocks, int64_t nblk, uint32_t* __restrict__ Wq,
                       uint16_t* __restrict__ S, uint16_t* __restrict__ B) {
-  __shared__ __align__(16) uint8_t span[kGgmlBlocks * 34];
-  const int nbytes = type == 0 ? 18 : type == 1 ? 20 : 34;
+  constexpr int kBytes = TYPE == 0 ? 18 : TYPE == 1 ? 20 : 34;
+  __shared__ __align__(16) uint8_t span[kGgmlBlocks * kBytes];
   const int64_t first = static_cast<int64_t>(blockIdx.x) * kGgmlBlocks;
   const int count = static_cast<int>((nblk - first < kGgmlBlocks) ? nblk - first : kGgmlBlocks);
-  const uint8_t* src = blocks + first * nbytes;
-  const int bytes = count * nbytes;
+  const uint8_t* src = blocks + first * kBytes;
+  const int bytes = count * kBytes;
   int done = 0;
   if ((reinterpret_cast<uintptr_t>(src) & 3) == 0) {
     const int words = bytes >> 2;
@@ -649,7 +662,9 @@ ggml_to_affine_kernel(int type, const uint8_t* __restrict__ blocks, int64_t nblk
   }
   for (int b = done + threadIdx.x; b < bytes; b += kGgmlThreads) span[b] = __ldg(src + b);
   __syncthreads();
-  for (int t = threadIdx.x; t < count; t += kGgmlThreads) convert_ggml_block(type, span + t * nbytes, first + t, Wq, S, B);
+  const bool vec = (reinterpret_cast<uintptr_t>(Wq) & 15) == 0;
+  for (int t = threadIdx.x; t < count; t += kGgmlThreads)
+    convert_ggml_block<TYPE>(span + t * kBytes, first + t, Wq, S, B, vec);
 }
 
 }  // namespace qmm
@@ -666,10 +681,14 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
   if (!aligned(Wq, 4) || !aligned(scales, 2) || !aligned(biases, 2)) return QMM_ERR_ALIGN;
   const int64_t grid = (nblk + qmm::kGgmlBlocks - 1) / qmm::kGgmlBlocks;
   if (grid > 0x7fffffff) return QMM_ERR_SHAPE;
-  qmm::ggml_to_affine_kernel<<<static_cast<unsigned int>(grid), qmm::kGgmlThreads, 0,
-                               static_cast<cudaStream_t>(stream)>>>(
-      type, static_cast<const uint8_t*>(blocks), nblk, Wq, static_cast<uint16_t*>(scales),
-      static_cast<uint16_t*>(biases));
+  const uint8_t* blk = static_cast<const uint8_t*>(blocks);
+  uint16_t* sp = static_cast<uint16_t*>(scales);
+  uint16_t* bp = static_cast<uint16_t*>(biases);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned int g = static_cast<unsigned int>(grid);
+  if (type == QMM_GGML_Q4_0) qmm::ggml_to_affine_kernel<0><<<g, qmm::kGgmlThreads, 0, st>>>(blk, nblk, Wq, sp, bp);
+  else if (type == QMM_GGML_Q4_1) qmm::ggml_to_affine_kernel<1><<<g, qmm::kGgmlThreads, 0, st>>>(blk, nblk, Wq, sp, bp);
+  else qmm::ggml_to_affine_kernel<2><<<g, qmm::kGgmlThreads, 0, st>>>(blk, nblk, Wq, sp, bp);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? QMM_OK : fail_cuda(e);
 }
