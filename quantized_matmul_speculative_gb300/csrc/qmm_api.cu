@@ -308,21 +308,24 @@ bool tma_supported(const CallArgs& a, int csize, const VariantDesc& d) {
   if (!tma_geometry(a.K, a.bits, a.gs, csize, &gp, &pw, &bw, &nb, &mbw)) return false;
   if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return false;
   // the CTA's stages, activations and at least one partial tile must fit
-  static int sm_bytes = 0, optin = 0;
-  if (sm_bytes == 0) {
+  struct SmemLimits {
+    int sm_bytes, optin;
+  };
+  static const SmemLimits lim = [] {  // one-time, thread-safe initialization
+    SmemLimits l{0, 0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&l.sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
       cudaGetLastError();
-      sm_bytes = 233472;  // sm_103a
-      optin = 232448;
+      l = {233472, 232448};  // sm_103a
     }
-  }
+    return l;
+  }();
   const int mp = a.M <= 8 ? 8 : 16;
   // two stages, one tile, every warp a slot; 8-bit codes stage 2g activations per group
   const TmaLayout L(pw, gp, a.bits == 8 ? 2 * a.gs : a.gs, mp, 2, 1, d.WN, mbw);
-  return L.total <= tma_smem_budget(sm_bytes, optin, d.WK);
+  return L.total <= tma_smem_budget(lim.sm_bytes, lim.optin, d.WK);
 }
 
 cudaError_t launch_own(const CallArgs& a, const VariantDesc& d, int splits, cudaStream_t stream, bool plan_only) {
