@@ -494,11 +494,109 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": w.name, "N": sh.N, "K": sh.K, "bits": w.bits,
                                         "group_size": w.group_size, "M": "1..16", "rows_sampled": rows},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+class StepGraphs:
+    """CUDA graphs of the bench step, so that exactly K steps can be replayed.
+
+    A graph of `reps` consecutive steps (the copy index advancing every call,
+    enough steps to touch every weight copy) is replayed K // reps times, then a
+    graph of K % reps steps once.  Graphs are captured on first use."""
+
+    def __init__(self, torch, stream, issue_step, reps):
+        self.torch, self.stream, self.issue_step, self.reps = torch, stream, issue_step, reps
+        self.graphs = {}
+
+    def _graph(self, n):
+        if n not in self.graphs:
+            g = self.torch.cuda.CUDAGraph()
+            with self.torch.cuda.graph(g, stream=self.stream):
+                for s in range(n):
+                    self.issue_step(s)
+            self.graphs[n] = g
+        return self.graphs[n]
+
+    def run(self, steps):
+        """Enqueue exactly `steps` steps on the stream (graphs captured beforehand by prepare())."""
+        full, rem = divmod(steps, self.reps)
+        with self.torch.cuda.stream(self.stream):
+            for _ in range(full):
+                self.graphs[self.reps].replay()
+            if rem:
+                self.graphs[rem].replay()
+
+    def prepare(self, *counts):
+        for steps in counts:
+            full, rem = divmod(steps, self.reps)
+            if full:
+                self._graph(self.reps)
+            if rem:
+                self._graph(rem)
+        self.stream.synchronize()
+
+    def release(self):
+        self.graphs.clear()
+
+
+def headline_line(*, value, world, steps, warmup, ms_per_step, workload, shape, ncopy, copy_mb, l2_mb, roofline,
+                  per_m, e2e, cpu, launches, clocks):
+    """The bench's last stdout line: compact (the driver keeps the tail of
+    stdout), every extra report goes out on earlier lines."""
+    N, K, bits, gs = shape
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "N": N, "K": K, "bits": bits, "group_size": gs, "M": "1..16",
+                   "chain": "dependent", "l2": f"{ncopy} weight copies, {copy_mb:.0f} MB > L2 {l2_mb:.0f} MB",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "per_m_us": [round(r["us_per_call"], 2) for r in per_m],
+        "per_m_frac": [round(r["frac_hbm"], 3) for r in per_m],
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks,
+    }
+
+
+def emit(report: str, body):
+    """One extra report as its own JSON line (before the headline)."""
+    print(json.dumps({"report": report, **body}), flush=True)
+
+
+def per_m_report(torch, stream, call, ms, call_b, peak, ncopy, names, select):
+    """us per call at each M: a graph of 64 chained calls at one M over `ncopy`
+    rotating weight copies (cold HBM when their total exceeds L2; one copy:
+    L2-warm), median of 5 replays."""
+    rows = []
+    for M in ms:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(64):
+                call(M, i % ncopy, i % 2)
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            for _ in range(5):
+                a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b2.record(stream)
+                b2.synchronize()
+                times.append(a.elapsed_time(b2) * 1e3 / 64)
+        del g
+        us = float(np.median(times))
+        gbs = call_b / (us * 1e-6) / 1e9
+        variant, splits = select(M)
+        rows.append({"M": M, "us_per_call": round(us, 3), "weight_gbs": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak, 4), "variant": names[variant], "splits": splits,
+                     "spread_us": round(max(times) - min(times), 3)})
+    return rows
 
 
 def run_ours(args, world, rank, local):
@@ -514,6 +612,7 @@ def run_ours(args, world, rank, local):
     N, K, bits, gs = sh.N, sh.K, w.bits, w.group_size
     ms = list(w.ms)
     call_b = workloads.call_bytes(N, K, bits, gs)
+    names = binding.variant_names()
 
     # weights: distinct copies whose total exceeds 4x L2, so each call reads cold HBM
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -527,85 +626,68 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(dev)
     handle = stream.cuda_stream
 
-    def call(M, ci, xb, yb):
+    def launch(M, ci, xb, yb):
         wq, s, b = copies[ci % ncopy]
         binding.small_m_ptr(xb.data_ptr(), wq.data_ptr(), s.data_ptr(), b.data_ptr(), M, N, K, bits, gs,
                             yb.data_ptr(), binding.OUT_BF16, -1, -1, handle)
 
-    calls_per_step = len(ms)
-    # Graph of `reps` steps: the copy index advances every call, the chain
-    # ping-pongs between two activation buffers.
-    reps = max(1, int(np.ceil(ncopy / calls_per_step)))
-    with torch.cuda.stream(stream):
-        for i, M in enumerate(ms * 2):  # eager warm-up (kernel attributes, module load)
-            call(M, i, bufs[i % 2], bufs[(i + 1) % 2])
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        ci = 0
-        for r in range(reps):
-            for M in ms:
-                call(M, ci, bufs[ci % 2], bufs[(ci + 1) % 2])
-                ci += 1
-    stream.synchronize()
+    def call(M, ci, parity):  # the chain ping-pongs between two activation buffers
+        launch(M, ci, bufs[parity], bufs[parity ^ 1])
 
-    # timed region: K steps = ceil(K/reps) replays of the `reps`-step graph
-    replays_w = max(1, int(np.ceil(args.warmup / reps)))
-    replays = max(1, int(np.ceil(args.steps / reps)))
-    steps_timed = replays * reps
+    calls_per_step = len(ms)
+    reps = max(1, int(np.ceil(ncopy / calls_per_step)))  # steps until every copy has been read
+
+    def issue_step(s):
+        for j, M in enumerate(ms):
+            ci = s * calls_per_step + j
+            call(M, ci, ci % 2)
+
     with torch.cuda.stream(stream):
-        for _ in range(replays_w):
-            graph.replay()
+        issue_step(0)  # eager warm-up: kernel attributes, module load, tensor maps
+        issue_step(1)
+    stream.synchronize()
+    graphs = StepGraphs(torch, stream, issue_step, reps)
+    graphs.prepare(args.warmup, args.steps)
+
+    # timed region: exactly --steps steps after exactly --warmup steps
+    graphs.run(args.warmup)
     stream.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(replays):
-                graph.replay()
-            end.record(stream)
+        start.record(stream)
+        graphs.run(args.steps)
+        end.record(stream)
         end.synchronize()
         torch.cuda.synchronize(dev)
         barrier(world)
-    ms_total = start.elapsed_time(end)
-    ms_total = max_over_ranks(ms_total, world, dev)
-    ms_per_step = ms_total / steps_timed
+    graphs.release()
+    ms_total = max_over_ranks(start.elapsed_time(end), world, dev)
+    ms_per_step = ms_total / args.steps
     step_bytes = calls_per_step * call_b
-    value = world * step_bytes * steps_timed / (ms_total * 1e-3) / 1e9
+    value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
+    clk = clocks.summary()
 
-    # per-M: graph of 64 calls at one M over rotating copies, median of 5 replays
-    per_m = []
-    for M in ms:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(64):
-                call(M, i, bufs[i % 2], bufs[(i + 1) % 2])
-        times = []
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g.replay()
-            for _ in range(5):
-                a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                g.replay()
-                b2.record(stream)
-                b2.synchronize()
-                times.append(a.elapsed_time(b2) * 1e3 / 64)
-        us = float(np.median(times))
-        gbs = call_b / (us * 1e-6) / 1e9
-        variant, splits = binding.select_variant(M, N, K, bits, gs)
-        per_m.append({"M": M, "us_per_call": round(us, 3), "weight_gbs": round(gbs, 1),
-                      "frac_hbm": round(gbs / peak, 4), "variant": binding.variant_names()[variant],
-                      "splits": splits, "spread_us": round(max(times) - min(times), 3)})
-        del g
+    def select(M):
+        return binding.select_variant(M, N, K, bits, gs)
+
+    per_m = per_m_report(torch, stream, call, ms, call_b, peak, ncopy, names, select)
+    per_m_warm = per_m_report(torch, stream, call, ms, call_b, peak, 1, names, select)
+    kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
+                      "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
+    if rank == 0:
+        emit("per_m_cold", {"workload": w.name, "per_m": per_m,
+                            "note": f"64 chained calls at one M over {ncopy} rotating weight copies, median of 5"})
+        emit("per_m_l2_warm", {"workload": w.name, "per_m": per_m_warm,
+                               "note": "L2-WARM: the same chain on one weight copy (14.7 MB stays in L2); "
+                                       "not the roofline figure"})
 
     # e2e: the public API with host buffers.  Every step copies the activations
     # of its 16 calls in from pinned host memory (one copy), runs the calls
     # (each on its own rows), and reads all their outputs back (one copy); the
-    # step is captured in a CUDA graph so that the timing is the device's.
+    # steps are graph-replayed so that the timing is the device's.
     rows = sum(ms)
     x_host = torch.empty((rows, K), dtype=torch.bfloat16).pin_memory()
     r0 = 0
@@ -615,88 +697,63 @@ def run_ours(args, world, rank, local):
     y_host = torch.empty((rows, N), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty((rows, K), dtype=torch.bfloat16, device=dev)
     yd = torch.empty((rows, N), dtype=torch.bfloat16, device=dev)
-    e2e_steps = max(3, min(args.steps, 200))
     h2d = 2 * rows * K
     d2h = 2 * rows * N
 
-    def e2e_step(ci0):
+    def e2e_step(s):
         xd.copy_(x_host, non_blocking=True)
         r = 0
-        for i, M in enumerate(ms):
-            call(M, ci0 + i, xd[r:r + M], yd[r:r + M])
+        for j, M in enumerate(ms):
+            launch(M, s * calls_per_step + j, xd[r:r + M], yd[r:r + M])
             r += M
         y_host.copy_(yd, non_blocking=True)
 
     with torch.cuda.stream(stream):
         e2e_step(0)
     stream.synchronize()
-    reps_e2e = max(1, int(np.ceil(ncopy / calls_per_step)))
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        for r in range(reps_e2e):
-            e2e_step(r * calls_per_step)
-    replays_e2e = max(1, int(np.ceil(e2e_steps / reps_e2e)))
-    e2e_steps = replays_e2e * reps_e2e
-    with torch.cuda.stream(stream):
-        g_e2e.replay()
-        stream.synchronize()
-        barrier(world)
-        a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(replays_e2e):
-            g_e2e.replay()
-        b2.record(stream)
-        b2.synchronize()
-    del g_e2e
+    e2e_graphs = StepGraphs(torch, stream, e2e_step, reps)
+    e2e_graphs.prepare(args.warmup, args.steps)
+    e2e_graphs.run(args.warmup)
+    stream.synchronize()
+    barrier(world)
+    a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    e2e_graphs.run(args.steps)
+    b2.record(stream)
+    b2.synchronize()
+    e2e_graphs.release()
     e2e_ms = max_over_ranks(a.elapsed_time(b2), world, dev)
-    e2e_value = world * step_bytes * e2e_steps / (e2e_ms * 1e-3) / 1e9
+    e2e_value = world * step_bytes * args.steps / (e2e_ms * 1e-3) / 1e9
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         nb, dt = cpu_oracle_sample(p, args.cpu_rows, ms)
-        cpu = {"value": nb / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"M=1..16 over the first {args.cpu_rows} of {N} rows, fp64 oracle, 1 thread, "
-                         f"{dt:.1f} s"}
+        cpu = {"value": round(nb / dt / 1e9, 5), "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(),
+               "kind": "oracle",
+               "sample": f"M=1..16, rows 0..{args.cpu_rows - 1} of {N}, 1 thread, {dt:.1f} s"}
 
-    extra = {}
-    if not args.no_extra:
-        extra["configs"] = configs_report(torch, dev, stream, peak)
-        extra["verify_step"] = verify_step_report(torch, dev, stream, peak)
-        extra["controls"] = dense_control(torch, dev, stream)
-        extra["residual"] = residual_report(torch, dev, stream)
-        extra["moe"] = moe_report(torch, dev, stream, peak)
-        extra["mx"] = mx_report(torch, dev, stream, peak)
-    kernels = sorted({"qmm_own_kernel" if "_own_" in r["variant"] else
-                      "qmm_tma_kernel" if r["variant"].startswith("tma") else "qmm_mma_kernel" for r in per_m})
+    if rank == 0 and not args.no_extra:
+        emit("configs", {"per_config": configs_report(torch, dev, stream, peak)})
+        emit("verify_step", verify_step_report(torch, dev, stream, peak))
+        emit("controls", dense_control(torch, dev, stream))
+        emit("residual", residual_report(torch, dev, stream))
+        emit("moe", moe_report(torch, dev, stream, peak))
+        emit("mx", mx_report(torch, dev, stream, peak))
 
-    clk = clocks.summary()
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps_timed,
-            "warmup": replays_w * reps, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "N": N, "K": K, "bits": bits, "group_size": gs, "M": "1..16",
-                       "calls_per_step": calls_per_step, "chain": "dependent (each call reads the previous output)",
-                       "l2": f"inputs larger than L2: {ncopy} rotating weight copies, "
-                             f"{ncopy * call_b / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB",
-                       "timing": "CUDA graph replays, CUDA events on the launching stream",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": round(value / world, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(value / world / peak, 4), "traffic": profiled_traffic(w.name),
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                         else "fallback 6.8 TB/s", "kernel": ", ".join(kernels),
-                         "achieved_def": "weight+metadata bytes per launch / mean launch time over the timed region"},
-            "per_m": per_m,
-            "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "note": "weights resident (model state); every step copies its calls' activations in from "
-                            "pinned host memory and their outputs back (one copy each way), graph-replayed"},
-            "gpu_launches": steps_timed * calls_per_step,
-            "clocks": clk,
-            **extra,
-        }
-        print(json.dumps(line), flush=True)
+        achieved = value / world
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name),
+                    "peak_source": "measured" if peak_kind == "measured" else "fallback",
+                    "kernel": ",".join(kernels)}
+        e2e = {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        clocks_short = None if clk is None else {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                                                  "reasons": clk["reasons"]}
+        line = headline_line(value=value, world=world, steps=args.steps, warmup=args.warmup,
+                             ms_per_step=ms_per_step, workload=w.name, shape=(N, K, bits, gs), ncopy=ncopy,
+                             copy_mb=ncopy * call_b / 1e6, l2_mb=l2 / 1e6, roofline=roofline, per_m=per_m,
+                             e2e=e2e, cpu=cpu, launches=args.steps * calls_per_step, clocks=clocks_short)
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     return 0
 
 

@@ -149,7 +149,11 @@ typedef enum { QMM_GGML_Q4_0 = 0, QMM_GGML_Q4_1 = 1, QMM_GGML_Q8_0 = 2 } qmm_ggm
  * [N, K*bits/32], scales and biases fp16 [N, K/32] (device, caller-owned) for
  * qmm_small_m* with group_size 32 and bits = 4 (Q4_0, Q4_1) or 8 (Q8_0):
  * codes unchanged (Q4) or q + 128 (Q8_0), scale d, bias -8 d (Q4_0), m (Q4_1)
- * or -128 d (Q8_0).  Asynchronous on `stream`.  QMM_ERR_UNSUPPORTED for an
+ * or -128 d (Q8_0).  Exact for every Q4_1 block, and for Q4_0 / Q8_0 blocks
+ * with |d| <= 8188 / 511.75: beyond that (or for a d that is inf or NaN) the
+ * bias has no finite fp16 value, the converted group is not the block, and
+ * bit 4 of qmm_device_status() is set.  Asynchronous on `stream`.
+ * QMM_ERR_UNSUPPORTED for an
  * unknown type, QMM_ERR_SHAPE for K not a multiple of 32, QMM_ERR_NULL /
  * QMM_ERR_ALIGN for the outputs (Wq 4-byte, scales/biases 2-byte aligned).   */
 qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uint32_t* Wq, void* scales,
@@ -171,8 +175,9 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
  * QMM_NVFP4: FP4 E2M1 codes with one FP8 E4M3 scale byte per group of 16,
  * scales uint8 [N, K/16] (a per-tensor scale, where a model has one, is left
  * to the caller).
- * K must be a multiple of 32.  An E4M3 NaN code (0x7F, 0xFF) reads as +-480,
- * an E8M0 255 as NaN.  Errors as qmm_small_m_ex.                               */
+ * K must be a multiple of 32.  NaN encodings are NaN, as the OCP format
+ * defines them: an E4M3 code or nvfp4 scale byte 0x7F / 0xFF, an E8M0 scale
+ * 255; every output whose sum meets one is NaN.  Errors as qmm_small_m_ex.    */
 typedef enum { QMM_MXFP4 = 0, QMM_MXFP8 = 1, QMM_NVFP4 = 2 } qmm_mx_format;
 qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scales, int M, int N, int K, int format,
                           void* Y, int out_dtype, int variant, int splits, void* stream);
@@ -219,7 +224,8 @@ int qmm_last_cuda_error(void);                 /* cudaError_t of the last failur
 /* Device status word of the kernels, OR-ed over all kernel units: bit 0 = a
  * consumer gave up waiting for a weight tile, bit 1 = the producer gave up
  * waiting for a free stage, bit 2 = copies still in flight at exit gave up,
- * bit 3 = a gathered call had an invalid index list (see qmm_gather_small_m).
+ * bit 3 = a gathered call had an invalid index list (see qmm_gather_small_m),
+ * bit 4 = qmm_from_ggml met a block outside its exact range.
  * Every wait is bounded (about 2 s), so a fault shows up here instead of as a
  * hang.  Synchronizes with the device; clears the word when `clear` != 0.
  * 0xFFFFFFFF if the word could not be read.                                    */

@@ -22,6 +22,13 @@
 #include "qmm_internal.h"
 
 namespace qmm {
+// Status word of the conversion kernel (this translation unit's; the host
+// reads it with the kernels' words in qmm_device_status()): bit 4, a Q4_0 /
+// Q8_0 block whose bias -8 d / -128 d is not a finite fp16 (|d| > 8188 /
+// 511.75, or d not finite), i.e. a block the affine layout cannot hold.
+constexpr unsigned int kStatusGgmlRange = 16u;
+static __device__ unsigned int g_qmm_ggml_status = 0;
+
 
 // Per-(bits, group) launchers, one translation unit each (qmm_mma_inst.cu).
 template <int BITS, int GS>
@@ -445,7 +452,13 @@ unsigned int qmm_device_status(int clear) {
   v |= read_device_status<8, 32>(clear);
   v |= read_device_status<8, 64>(clear);
   v |= read_device_status<8, 128>(clear);
-  return v;
+  unsigned int g = 0;
+  if (cudaMemcpyFromSymbol(&g, qmm::g_qmm_ggml_status, sizeof(g)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (clear && g) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(qmm::g_qmm_ggml_status, &zero, sizeof(zero));
+  }
+  return v | g;
 }
 
 }  // extern "C"
@@ -586,6 +599,14 @@ namespace qmm {
 constexpr int kGgmlThreads = 256;
 constexpr int kGgmlBlocks = 512;
 
+// fp16 bias of a Q4_0 (-8 d) or Q8_0 (-128 d) block: exact (a power-of-two
+// multiple) while finite; an infinite or NaN result flags the block.
+__device__ __forceinline__ uint16_t ggml_bias(float df, float mult) {
+  const uint16_t b = __half_as_ushort(__float2half_rn(mult * df));
+  if ((b & 0x7C00u) == 0x7C00u) atomicOr(&g_qmm_ggml_status, kStatusGgmlRange);
+  return b;
+}
+
 // Four bytes at a 2-byte aligned shared-memory address, as a little-endian word.
 __device__ __forceinline__ uint32_t ggml_word(const uint8_t* p) {
   const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
@@ -617,7 +638,7 @@ __device__ __forceinline__ void convert_ggml_block(const uint8_t* blk, int64_t i
   if constexpr (TYPE == 2) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) w[k] = ggml_word(blk + 2 + 4 * k) ^ 0x80808080u;
-    B[i] = __half_as_ushort(__float2half_rn(-128.f * df));
+    B[i] = ggml_bias(df, -128.f);
   } else {
     const uint8_t* qs = blk + (TYPE == 0 ? 2 : 4);
     const uint32_t b0 = ggml_word(qs), b1 = ggml_word(qs + 4), b2 = ggml_word(qs + 8), b3 = ggml_word(qs + 12);
@@ -625,7 +646,7 @@ __device__ __forceinline__ void convert_ggml_block(const uint8_t* blk, int64_t i
     w[1] = ggml_low_nibbles(b2, b3);
     w[2] = ggml_low_nibbles(b0 >> 4, b1 >> 4);
     w[3] = ggml_low_nibbles(b2 >> 4, b3 >> 4);
-    B[i] = (TYPE == 0) ? __half_as_ushort(__float2half_rn(-8.f * df)) : *reinterpret_cast<const uint16_t*>(blk + 2);
+    B[i] = (TYPE == 0) ? ggml_bias(df, -8.f) : *reinterpret_cast<const uint16_t*>(blk + 2);
   }
   uint32_t* dst = Wq + i * NW;
   if (vec) {

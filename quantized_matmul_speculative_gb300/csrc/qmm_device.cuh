@@ -74,8 +74,9 @@ __device__ __forceinline__ uint32_t bf16x2_times16(uint32_t v) {
 // value (exponent 0 lands on the bf16 subnormal m * 2^-127), and an FP8 E4M3
 // code s|eeee|mmm placed at bits 15 | 7-10 | 4-6 is exactly 2^-120 times its
 // value; one bf16x2 FMA by 2^126 or 2^120 then gives the value exactly.  A
-// word's pair i holds codes i and i + 16/b, as in unpack_pair.  (An E4M3 NaN
-// code is not propagated: it reads as 480.)
+// word's pair i holds codes i and i + 16/b, as in unpack_pair.  An E4M3 NaN
+// code (S.1111.111) becomes a bf16 NaN: the FMA's addend is -0 for every other
+// code and a NaN for those.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, uint32_t f2) {
   uint32_t r;
@@ -89,11 +90,19 @@ __device__ __forceinline__ uint32_t unpack_fp4_pair(uint32_t w, int i) {
 }
 __device__ __forceinline__ uint32_t unpack_fp8_pair(uint32_t w, int i) {
   const uint32_t u = w >> (8 * i);
-  const uint32_t v = ((u & 0x007F007Fu) << 4) | ((u & 0x00800080u) << 8);
-  return bf16x2_scale(v, 0x7B807B80u);  // 2^120
+  const uint32_t mag = u & 0x007F007Fu;
+  const uint32_t v = (mag << 4) | ((u & 0x00800080u) << 8);
+  // 1 in the low bit of a half whose magnitude bits are all ones (NaN): that
+  // half's +1 carries into bit 7 and no other half's does (magnitudes <= 0x7F).
+  const uint32_t nan1 = ((mag + 0x00010001u) >> 7) & 0x00010001u;
+  const uint32_t addend = nan1 * 0x7FC0u + 0x80008000u;  // per half: -0, or 0xFFC0 (a NaN)
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x7B807B80u), "r"(addend));  // 2^120
+  return r;
 }
-// E4M3 byte -> fp32, exactly (same placement as unpack_fp8_pair; NaN codes read as 480).
+// E4M3 byte -> fp32, exactly (same placement as unpack_fp8_pair); S.1111.111 is NaN.
 __device__ __forceinline__ float e4m3_to_float(uint32_t c) {
+  if ((c & 0x7Fu) == 0x7Fu) return __uint_as_float(0x7FC00000u);
   const uint32_t v = ((c & 0x7Fu) << 4) | ((c & 0x80u) << 8);
   return __uint_as_float(v << 16) * 1.329227995784915872903807060280344576e36f;  // 2^120
 }

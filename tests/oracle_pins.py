@@ -371,6 +371,34 @@ def pin_mx(lib):
             assert np.array_equal(yo[0], W[:, k0]), f"{fmt} one-hot {k0}"
 
 
+def pin_dequant(lib):
+    """oracle_dequant against the definition w[n, k] = s[n, k/g] * q[n, k] + b[n, k/g]
+    written out with exact rationals from the generator's codes (not the packed
+    words), on shapes with N != K so that a transposed or mis-strided write shows;
+    and each column of it against the one-hot product of oracle_qmm."""
+    for i, (bits, g, N, K) in enumerate(((4, 64, 3, 128), (4, 32, 5, 96), (2, 64, 4, 192), (8, 32, 2, 64),
+                                         (4, 128, 7, 256))):
+        p = synth.make_problem(1100 + i, N, K, bits, g, rows=1)
+        W = lib.dequant(lib.pack(p.q, bits), p.scales, p.biases, K, bits, g)
+        assert W.shape == (N, K), f"dequant shape {W.shape}"
+        for n in range(N):
+            for k in range(K):
+                exact = frac_half(int(p.scales[n, k // g])) * int(p.q[n, k]) + frac_half(int(p.biases[n, k // g]))
+                assert Fraction(float(W[n, k])) == exact, f"dequant ({bits}-bit g{g}) w[{n},{k}]"
+        wq = lib.pack(p.q, bits)
+        for k0 in (0, g - 1, g, K - 1):
+            xo = np.zeros((1, K), dtype=np.uint16)
+            xo[0, k0] = BF16_ONE
+            y, _ = lib.qmm(xo, wq, p.scales, p.biases, bits, g)
+            assert np.array_equal(y[0], W[:, k0]), f"dequant column {k0} vs one-hot product"
+    # hand-built: codes 0..7 along one 4-bit row, scale 2, bias -1 -> w = 2q - 1
+    q = np.arange(64, dtype=np.uint8).reshape(1, 64) % 16
+    s = np.full((1, 1), 0x4000, dtype=np.uint16)   # fp16 2.0
+    b = np.full((1, 1), 0xBC00, dtype=np.uint16)   # fp16 -1.0
+    W = lib.dequant(lib.pack(q, 4), s, b, 64, 4, 64)
+    assert np.array_equal(W[0], 2.0 * q[0].astype(np.float64) - 1.0), "hand-built dequant row"
+
+
 def pin_sampled(lib):
     M, N, K, bits, g = 4, 11, 192, 2, 64
     p = synth.make_problem(995, N, K, bits, g, rows=M)
@@ -385,5 +413,5 @@ def pin_sampled(lib):
 # Pins that run fast enough for the mutation test (the exhaustive decoder pin
 # is run once against the real oracle only).
 FAST_PINS = (pin_pack_words, pin_brute_force, pin_closed_forms, pin_integer_special_case,
-             pin_invariants, pin_residual, pin_gather, pin_ggml, pin_mx, pin_sampled)
+             pin_invariants, pin_dequant, pin_residual, pin_gather, pin_ggml, pin_mx, pin_sampled)
 ALL_PINS = (pin_decoders,) + FAST_PINS

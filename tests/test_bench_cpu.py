@@ -83,3 +83,31 @@ def test_reference_arm_under_torchrun_world2():
     line = json.loads(lines[0])
     _check_reference_line(line)
     assert line["n_gpus"] == 2
+
+
+def test_headline_fits_the_stdout_tail():
+    """The last stdout line carries every headline key and stays well under the
+    1500 characters of stdout that a caller keeping only the tail sees, with
+    realistic worst-case field widths."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    per_m = [{"M": m, "us_per_call": 12345.678, "frac_hbm": 0.123456} for m in range(1, 17)]
+    roof = {"bound": "hbm", "achieved": 99999.9, "peak": 6777.6, "unit": "GB/s", "frac": 0.1234,
+            "traffic": 14889984.0, "peak_source": "measured", "kernel": "qmm_mma_kernel,qmm_own_kernel,qmm_tma_kernel"}
+    cpu = {"value": 0.04062, "unit": "GB/s", "cores": 1, "host_cores": 144, "kind": "oracle",
+           "sample": "M=1..16, rows 0..5119 of 5120, 1 thread, 123.4 s"}
+    e2e = {"value": 12345.67, "unit": "GB/s", "h2d_bytes_per_step": 1392640, "d2h_bytes_per_step": 1392640}
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    line = bench.headline_line(value=123456.78, world=8, steps=20000, warmup=200, ms_per_step=0.123456,
+                               workload="m_sweep_5120x5120_4b_g64", shape=(5120, 5120, 4, 64), ncopy=38,
+                               copy_mb=560.3, l2_mb=132.1, roofline=roof, per_m=per_m, e2e=e2e, cpu=cpu,
+                               launches=320000, clocks=clocks)
+    text = json.dumps(line, separators=(",", ":"))
+    assert len(text) < 1300, len(text)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "cpu_baseline",
+                "gpu_launches", "clocks"):
+        assert key in line
+    assert line["config"]["workload"] == "m_sweep_5120x5120_4b_g64"
+    assert len(line["per_m_us"]) == 16 and len(line["per_m_frac"]) == 16

@@ -115,3 +115,37 @@ def test_conversion_unaligned_buffers(torch_cuda, kind):
                         b.cpu().numpy().view(np.uint16), K, bits, 32)
     assert np.array_equal(w_conv, ol.ggml_dequant(kind, blocks, N, K))
     assert int(wq_buf[0]) == 0, "a word before Wq was written"
+
+
+# |d| at and just past the largest value whose bias -8 d (Q4_0) / -128 d
+# (Q8_0) is a finite fp16, and the fp16 maximum: (kind, d, exact)
+RANGE_CASES = [("q8_0", 511.75, True), ("q8_0", -511.75, True), ("q8_0", 512.0, False), ("q8_0", -512.0, False),
+               ("q8_0", 65504.0, False), ("q4_0", 8188.0, True), ("q4_0", -8188.0, True), ("q4_0", 8192.0, False),
+               ("q4_0", 65504.0, False), ("q4_1", 65504.0, True), ("q4_1", -65504.0, True)]
+
+
+@pytest.mark.parametrize("kind,d,exact", RANGE_CASES, ids=[f"{k}_{d:g}" for k, d, _ in RANGE_CASES])
+def test_conversion_range(torch_cuda, kind, d, exact):
+    """Blocks with a large scale d: inside the stated range the conversion is
+    still exact (the converted matrix dequantizes to the oracle's decoding of
+    the blocks) and the status word stays clear; past it, bit 4 of the status
+    word is set (the affine layout cannot hold the block)."""
+    torch = torch_cuda
+    N, K = 5, 96
+    blocks = synth.make_ggml_blocks(8800, N, K, kind)
+    blocks[7, 0:2] = np.array([d], dtype=np.float16).view(np.uint8)  # row 2, block 1
+    if kind == "q4_1":  # m stays in range: fp16(-7.5 d) would overflow for |d| > 8733
+        blocks[7, 2:4] = np.array([-0.5 * d], dtype=np.float16).view(np.uint8)
+    binding.device_status(clear=True)
+    wq, s, b, bits = convert(torch, blocks, N, K, kind)
+    status = binding.device_status(clear=True)
+    if not exact:
+        assert status == 16, f"status {status:#x}"
+        return
+    assert status == 0, f"status {status:#x}"
+    ol = oracle.load()
+    w_conv = ol.dequant(wq.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint16),
+                        b.cpu().numpy().view(np.uint16), K, bits, 32)
+    w_ref = ol.ggml_dequant(kind, blocks, N, K)
+    assert np.array_equal(w_conv, w_ref)
+    assert np.abs(w_ref[2, 32:64]).max() > 100.0  # the large block is really there

@@ -47,10 +47,11 @@ def upload(torch, q, sc, bits):
 @pytest.mark.parametrize("fmt,bits", FORMATS)
 def test_every_code_value(torch_cuda, fmt, bits):
     """Each code of the format in turn (one-hot X picks it out): the GPU
-    reproduces the oracle's decoding of every E2M1 / non-NaN E4M3 code."""
+    reproduces the oracle's decoding of every E2M1 and every E4M3 code, the
+    two NaN codes (0x7F, 0xFF) included (NaN where the oracle has NaN)."""
     torch = torch_cuda
     ncode = 16 if bits == 4 else 256
-    codes = [c for c in range(ncode) if not (bits == 8 and (c & 0x7F) == 0x7F)]
+    codes = list(range(ncode))
     N, K = len(codes), 64
     q = np.zeros((N, K), dtype=np.uint8)
     q[:, 5] = codes
@@ -62,7 +63,48 @@ def test_every_code_value(torch_cuda, fmt, bits):
     x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
     y = to_f64(binding.small_m_mx(x, wq, s, fmt, out_dtype=torch.float32))
     ref, _ = oracle.load().mx_qmm(fmt, xb, binding.pack(q, bits), sc)
-    assert np.array_equal(y[0], ref[0])
+    assert np.array_equal(y[0], ref[0], equal_nan=True)
+    if bits == 8:
+        assert np.isnan(ref[0][[0x7F, 0xFF]]).all() and np.isfinite(np.delete(ref[0], [0x7F, 0xFF])).all()
+
+
+@pytest.mark.parametrize("fmt,bits", FORMATS)
+def test_nan_encodings(torch_cuda, fmt, bits):
+    """NaN encodings planted in the weights: E4M3 NaN codes (mxfp8), E4M3 NaN
+    scale bytes (nvfp4) and E8M0 255 scales (mxfp4, mxfp8).  On the default
+    and on every variant that takes the shape, bf16 and fp32, the outputs that
+    are NaN are exactly the oracle's NaN outputs, and every other output meets
+    the bound."""
+    torch = torch_cuda
+    ol = oracle.load()
+    N, K = 200, 512
+    q, sc = synth.make_mx(8700 + bits, N, K, fmt)
+    rng = np.random.default_rng(8700)
+    rows = rng.choice(N, size=12, replace=False)
+    for r in rows[:6]:  # NaN scale bytes
+        sc[r, rng.integers(sc.shape[1])] = (0x7F | (0x80 * int(rng.integers(2)))) if fmt == "nvfp4" else 255
+    if bits == 8:
+        for r in rows[6:]:  # NaN codes
+            q[r, rng.integers(K)] = 0x7F | (0x80 * int(rng.integers(2)))
+    wq, s = upload(torch, q, sc, bits)
+    xb = synth.make_x(8700, K)
+    x = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+    y_ref, a_ref = ol.mx_qmm(fmt, xb, binding.pack(q, bits), sc)
+    nan_ref = np.isnan(y_ref)
+    assert nan_ref[:, rows[:6]].all() and nan_ref.any(axis=0).sum() == (12 if bits == 8 else 6)
+    names = binding.variant_names()
+    for v in [-1] + list(range(len(names))):
+        for M in (1, 9, 16):
+            for dt in (torch.float32, torch.bfloat16):
+                try:
+                    y = to_f64(binding.small_m_mx(x[:M].contiguous(), wq, s, fmt, out_dtype=dt, variant=v))
+                except binding.QmmError as e:
+                    assert e.status == 3 and names[v].startswith("tma"), names[v]
+                    break
+                what = f"{fmt} {'default' if v < 0 else names[v]} M={M} {dt}"
+                assert np.array_equal(np.isnan(y), nan_ref[:M]), what + ": NaN positions"
+                fin = ~nan_ref[:M]
+                assert_within(y[fin], y_ref[:M][fin], a_ref[:M][fin], what, bf16=dt == torch.bfloat16)
 
 
 @pytest.mark.parametrize("fmt,bits", FORMATS)

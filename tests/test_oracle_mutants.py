@@ -29,6 +29,8 @@ MUTANTS = [
     ("e4m3_subnormal", "std::ldexp(m / 8.0, -6)", "std::ldexp(m / 8.0, -7)"),
     ("e8m0_bias", "static_cast<int>(e) - 127", "static_cast<int>(e) - 128"),
     ("nvfp4_group", "const int64_t g = format == 2 ? 16 : 32;", "const int64_t g = 32;"),
+    ("dequant_transposed", "W[n * K + k] = weight_at(Wq, S, B, K, bits, g, n, k);",
+     "W[k * N + n] = weight_at(Wq, S, B, K, bits, g, n, k);"),
     ("gather_expert_stride", "const int64_t words_per_matrix = N * (K * bits / 32);",
      "const int64_t words_per_matrix = K * bits / 32;"),
 ]
