@@ -118,12 +118,27 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
 // LOP3: bits [b*i, b*i+b) land in the low half and bits [16+b*i, 16+b*i+b) in
 // the high half, i.e. codes i and i + 16/b of the word.  The +128 offset is
 // removed later, once per group, through the group's activation sum.
+//
+// The mask-and-or has two 32-bit constants, and the hardware's three-input
+// logic instruction takes one immediate: with both as literals the compiler
+// spends two instructions per pair.  The OR constant therefore comes in a
+// register (`magic`, from unpack_magic(), made once per thread), which keeps
+// the pair at one logic instruction (plus the shift for i > 0).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t unpack_magic() {
+  // %laneid >> 5 is always 0; the compiler cannot know it, so the constant
+  // stays in a register instead of being folded back into an immediate.
+  uint32_t z;
+  asm volatile("mov.u32 %0, %%laneid;" : "=r"(z));
+  return 0x43004300u | (z >> 5);
+}
 template <int BITS>
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int i) {
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t w, int i, uint32_t magic) {
   constexpr uint32_t kMask = (1u << BITS) - 1u;
   constexpr uint32_t kMask2 = kMask | (kMask << 16);
-  return ((w >> (BITS * i)) & kMask2) | 0x43004300u;
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w >> (BITS * i)), "n"(kMask2), "r"(magic));  // (a & b) | c
+  return r;
 }
 
 // ---------------------------------------------------------------------------

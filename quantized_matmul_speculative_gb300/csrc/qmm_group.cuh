@@ -197,10 +197,10 @@ struct GroupMath {
   }
 
   // The A operand pair i of a packed word for this code format.
-  __device__ static uint32_t unpack(uint32_t w, int i) {
+  __device__ static uint32_t unpack(uint32_t w, int i, uint32_t magic) {
     if constexpr (CODES == kCodesMx4 || CODES == kCodesNv4) return unpack_fp4_pair(w, i);
     else if constexpr (CODES == kCodesMx8) return unpack_fp8_pair(w, i);
-    else return unpack_pair<BITS>(w, i);
+    else return unpack_pair<BITS>(w, i, magic);
   }
 
   // Fragment geometry of a lane: rows g and g + 8 of the 16-row block,
@@ -209,9 +209,11 @@ struct GroupMath {
   // threads) the first MMA step it feeds.
   struct Lane {
     int g, t, wofs, tsub;
+    uint32_t magic;  // unpack_magic(), the OR constant of the affine unpack
   };
   __device__ static Lane lane_geometry(int lane) {
     Lane l;
+    l.magic = unpack_magic();
     l.g = lane >> 2;
     l.t = lane & 3;
     l.wofs = (TPW == 1) ? l.t * LW : l.t / TPW;
@@ -234,7 +236,7 @@ struct GroupMath {
   // of rows g, g + 8 (from wl, wh), B = the activations at xg (the group's
   // start in this lane's row of Xs, rows 8 apart by 8 * rsx).
   __device__ static void mma(const uint32_t (&wl)[LW], const uint32_t (&wh)[LW], const uint16_t* xg, int rsx,
-                             int tsub, float (&tmp)[NB][4]) {
+                             int tsub, float (&tmp)[NB][4], uint32_t magic) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
@@ -244,10 +246,10 @@ struct GroupMath {
       const int lwi = (TPW == 1) ? st / SPW : 0;
       const int sub = (TPW == 1) ? st % SPW : tsub + st;
       uint32_t a[4];
-      a[0] = unpack(wl[lwi], 2 * sub);
-      a[1] = unpack(wh[lwi], 2 * sub);
-      a[2] = unpack(wl[lwi], 2 * sub + 1);
-      a[3] = unpack(wh[lwi], 2 * sub + 1);
+      a[0] = unpack(wl[lwi], 2 * sub, magic);
+      a[1] = unpack(wh[lwi], 2 * sub, magic);
+      a[2] = unpack(wl[lwi], 2 * sub + 1, magic);
+      a[3] = unpack(wh[lwi], 2 * sub + 1, magic);
       const int ko = (TPW == 1) ? (lwi * VPW + 4 * sub) : 4 * st;
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {

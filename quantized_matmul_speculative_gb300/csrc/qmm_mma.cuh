@@ -137,6 +137,7 @@ qmm_mma_kernel(const MmaParams p) {
   const int wn = warp % WN;
   const int wk = warp / WN;
   const int g = lane >> 2;
+  const uint32_t magic = unpack_magic();  // the affine unpack's OR constant, in a register
   const int t = lane & 3;
 
   // Gathered form: this CTA's expert, its entries' activation rows and output
@@ -352,7 +353,7 @@ qmm_mma_kernel(const MmaParams p) {
           auto unpack = [&](uint32_t w, int i) {
             if constexpr (CODES == kCodesMx4 || CODES == kCodesNv4) return unpack_fp4_pair(w, i);
             else if constexpr (CODES == kCodesMx8) return unpack_fp8_pair(w, i);
-            else return unpack_pair<BITS>(w, i);
+            else return unpack_pair<BITS>(w, i, magic);
           };
           a[0] = unpack(wcur[r][0][lwi], 2 * s);
           a[1] = unpack(wcur[r][1][lwi], 2 * s);

@@ -351,7 +351,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     auto group = [&](int j, float (&tmp)[NB][4]) {
       uint32_t wl[GM::LW], wh[GM::LW];
       GM::load_words(next_words(), p.bw, wl, wh);
-      GM::mma(wl, wh, xu + j * GS, L.rsx, ln.tsub, tmp);
+      GM::mma(wl, wh, xu + j * GS, L.rsx, ln.tsub, tmp, ln.magic);
     };
     auto fold = [&](int j, const float (&tmp)[NB][4]) {
       if constexpr (MX) GM::fold_mx(meta8 + j, p.mbw, tmp, acc);

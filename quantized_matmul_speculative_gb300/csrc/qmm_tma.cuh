@@ -258,7 +258,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   auto group_mma = [&](const uint32_t* wp, int j, float (&tmp)[NB][4]) {
     uint32_t wl[C::LW], wh[C::LW];
     GM::load_words(wp, p.box_words, wl, wh);
-    GM::mma(wl, wh, xrow + j * GS, L.rsx, ln.tsub, tmp);
+    GM::mma(wl, wh, xrow + j * GS, L.rsx, ln.tsub, tmp, ln.magic);
   };
   // Fold group j's scale and bias into acc.
   auto group_fold = [&](const uint16_t* meta, int j, const float (&tmp)[NB][4], float (&acc)[NB][4]) {
@@ -383,9 +383,11 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     // a time); with the push reduction, send the sum straight to the tile's
     // owner (CTA slot % C of the cluster), else park it in slot 0.
     asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");
+    QMM_TRACE_POINT(9);
     const int per_tile = p.M * 16;
     const int nslots = i_hi - i_lo;
     if (p.push) cluster_wait();  // every CTA of the cluster has initialized its barriers
+    QMM_TRACE_POINT(12);
     for (int e4 = tid; e4 < nslots * (per_tile / 4); e4 += cthreads) {
       const int slot = e4 / (per_tile / 4);
       const int r = (e4 - slot * (per_tile / 4)) * 4;  // m * 16 + row
@@ -410,11 +412,13 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
           v.w += x4.w;
         }
       }
+      QMM_TRACE_POINT(14);
       if (p.push) {
         const uint32_t q = static_cast<uint32_t>(slot % csize);
         const int o = slot / csize;
         const uint32_t dst = smem_addr(smem + L.recv_off) + 4u * static_cast<uint32_t>((o * csize + rank) * C::MP * 16 + r);
         st_async_v4(mapa_shared(dst, q), v, mapa_shared(recv_bar, q));
+        QMM_TRACE_POINT(15);
       } else {
         *reinterpret_cast<float4*>(base) = v;
       }
@@ -423,8 +427,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       // Owned tiles: slot % C == rank.  Wait for every peer's bytes, sum the
       // C partials in rank order, write Y.
       const int owned = (nslots > rank) ? (nslots - rank + csize - 1) / csize : 0;
+      QMM_TRACE_POINT(10);
       if (tid == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(owned * csize * per_tile * 4));
       if (owned > 0) mbar_wait(recv_bar, 0, kStatusTimeoutFull);
+      QMM_TRACE_POINT(11);
       const float* recv = reinterpret_cast<const float*>(smem + L.recv_off);
       for (int e = tid; e < owned * per_tile; e += cthreads) {
         const int o = e / per_tile;

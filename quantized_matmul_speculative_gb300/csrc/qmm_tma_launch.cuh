@@ -127,6 +127,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget_all, csize);
   if (ncl < 1) return cudaErrorInvalidConfiguration;
   if (ncl > p.tiles) ncl = p.tiles;
+  if (const char* cap = std::getenv("QMM_EXP_NCL_DIV")) { const int dv = std::atoi(cap); if (dv > 1) ncl = (ncl + dv - 1) / dv; }
   p.ncl = ncl;
   const int nt_max = (p.tiles + ncl - 1) / ncl;
   const int nt_min = p.tiles / ncl;
