@@ -152,6 +152,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator input: d = a * b (the first MMA of a group
+// needs no zeroed registers).
+__device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block clusters: barrier and distributed shared memory.
 // ---------------------------------------------------------------------------
@@ -246,14 +256,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
 }
 
 // Wait for the phase with the given parity to complete; gives up after
-// kWaitLimitNs, sets `flag` in the status word and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int flag) {
+// `limit_ns` (kWaitLimitNs unless a test asks for less), sets `flag` in the
+// status word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity, 20000u)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity, 20000u)) return true;
     __nanosleep(64);
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(&g_qmm_status, flag);
       return false;
     }

@@ -5,6 +5,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -76,6 +77,15 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.K = a.K;
   p.G = a.K / GS;
   p.out_f32 = a.out_f32;
+  // Test-only fault injection (host-triggered): a short wait limit and one
+  // tile whose declared bytes never all arrive; the waits on it give up and
+  // set bits of the device status word, the call still completes.
+  {
+    const char* inject = std::getenv("QMM_TEST_INJECT");
+    const bool short_wait = inject != nullptr && std::strcmp(inject, "short_wait") == 0 && a.rhs == nullptr;
+    p.wait_ns = short_wait ? 100000ull : kWaitLimitNs;
+    p.inject = short_wait ? 1 : 0;
+  }
   if (!tma_geometry(a.K, BITS, GS, csize, &p.gp, &p.pw, &p.box_words, &p.nbox, &p.mbw)) return cudaErrorInvalidValue;
   p.gp_magic = ((1ull << 32) + static_cast<unsigned long long>(p.gp) - 1) / static_cast<unsigned long long>(p.gp);
   if ((reinterpret_cast<uintptr_t>(a.S) | reinterpret_cast<uintptr_t>(a.B)) & 15) return cudaErrorInvalidValue;
@@ -127,7 +137,6 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   int ncl = max_active_clusters(reinterpret_cast<const void*>(kern), Cfg::THREADS, budget_all, csize);
   if (ncl < 1) return cudaErrorInvalidConfiguration;
   if (ncl > p.tiles) ncl = p.tiles;
-  if (const char* cap = std::getenv("QMM_EXP_NCL_DIV")) { const int dv = std::atoi(cap); if (dv > 1) ncl = (ncl + dv - 1) / dv; }
   p.ncl = ncl;
   const int nt_max = (p.tiles + ncl - 1) / ncl;
   const int nt_min = p.tiles / ncl;
@@ -149,9 +158,15 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   // Single shot: when every tile of a cluster fits, each gets a stage of its
   // own, all copies are issued at once and the warps split all the tiles'
   // groups evenly (one window, one round).
+  // Layout with every warp pushing its partials to the tiles' owners (no park area).
+  auto push_layout = [&](int stages_, int slots_) {
+    const int recv_tiles = (nt_max + csize - 1) / csize;
+    return TmaLayout(p.pw, p.gp, GS, Cfg::MP, stages_, 0, slots_, p.mbw, recv_tiles, csize, slots_);
+  };
   if (nt_max <= S) {
     const int sl = round_slots(nt_max, nt_max);
-    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget) {
+    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget ||
+        push_layout(nt_max, sl).total <= budget) {
       p.single = 1;
       stages = nt_max;
       ws = nt_max;
@@ -178,18 +193,16 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.rt = rt;
   p.slots = slots;
   p.ws = ws;
-  // One round for every cluster: reduce by pushing partials to their owners,
-  // if the receive buffer still fits.
+  // One round for every cluster: every warp pushes its partial of each tile it
+  // meets straight to the tile's owner, if the receive buffer fits.
   p.push = 0;
   p.recv_tiles = 0;
-  if (rt == nt_max) {
-    const int recv_tiles = (rt + csize - 1) / csize;
-    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, recv_tiles, csize).total <= budget) {
-      p.push = 1;
-      p.recv_tiles = recv_tiles;
-    }
+  if (rt == nt_max && push_layout(p.stages, p.slots).total <= budget) {
+    p.push = 1;
+    p.recv_tiles = (rt + csize - 1) / csize;
   }
-  int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
+  int smem = p.push ? push_layout(p.stages, p.slots).total
+                    : TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw).total;
   if (gathered) {
     p.gather_off = (smem + 15) & ~15;
     smem = p.gather_off + gather_bytes;
