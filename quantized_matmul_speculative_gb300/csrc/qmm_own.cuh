@@ -53,6 +53,8 @@ struct OwnParams {
                                 // ([16 rows][G] each), copied through a [rows*G/8, 8] view of the
                                 // [rows, G] arrays: their rows are not 16-byte strided (G % 8 != 0);
                                 // microscaling: the scale bytes, through a [rows*G/16, 16] view
+  int swz;                      // 1: weight boxes are 32-word (128-byte) rows copied with the 128-byte
+                                // swizzle (16-byte chunk c of box row r at c ^ (r & 7)), bw = 32
   int tiles;                    // 16-row tiles of W
   int ncl;                      // clusters in the grid
   int maxw;                     // receive slots per (tile, CTA): most warps that meet one tile
@@ -79,20 +81,25 @@ struct OwnLayout {
   // meta_row: shared-memory bytes of scale/bias data per weight row of a unit
   // (affine: fp16 scales and biases, (bofs + 16 mbw) / 8, i.e. 4 mbw unless the
   // biases are placed further; microscaling: mbw scale bytes).
+  // swz: swizzled weight boxes, whose destinations must be 1024-byte aligned:
+  // the ring starts and every stage spans a multiple of 1024 bytes from a base
+  // that the kernel aligns itself (`total` keeps 1024 bytes of slack for it).
   __host__ __device__ OwnLayout(int W, int D, int gp, int gs, int mp, int nb, int nbox, int bw, int meta_row,
-                                int owned_max, int csize, int maxw, int m) {
+                                int owned_max, int csize, int maxw, int m, int swz = 0) {
     const int nbar = W * D + owned_max;  // full barriers of the rings, then one per owned tile
+    const int al = swz ? 1023 : 127;
     rsx = gp * gs + 4;                   // X row stride (halves): 8 bytes past a 16-byte multiple
     x_off = (8 * nbar + 127) & ~127;
     xs_off = (x_off + m * rsx * 2 + 15) & ~15;
-    ring_off = (xs_off + gp * mp * 4 + 127) & ~127;
+    ring_off = (xs_off + gp * mp * 4 + al) & ~al;
     w_bytes = nbox * 16 * bw * 4;
-    stage_bytes = (w_bytes + 16 * meta_row + 127) & ~127;
+    stage_bytes = (w_bytes + 16 * meta_row + al) & ~al;
     recv_off = ring_off + W * D * stage_bytes;
     slot_bytes = 32 * 16 * nb;  // 32 lanes x 4 floats x activation tiles
     total = recv_off + owned_max * csize * maxw * slot_bytes;
     const int x_end = x_off + mp * rsx * 2;  // the reads of all mp rows stay inside
     if (total < x_end) total = x_end;
+    if (swz) total += 1024;
   }
 };
 
@@ -107,13 +114,14 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   constexpr int MP = GM::MP;
   constexpr int GW = GM::GW;
   extern __shared__ __align__(128) unsigned char own_smem[];
-  unsigned char* smem = own_smem;
+  // Swizzled weight boxes need 1024-byte aligned destinations: align the base.
+  unsigned char* smem = own_smem + (p.swz ? ((1024u - (smem_addr(own_smem) & 1023u)) & 1023u) : 0u);
   const int csize = static_cast<int>(gridDim.x);  // CTAs per cluster (cluster spans x)
   const int rank = static_cast<int>(blockIdx.x);
   const int q = static_cast<int>(blockIdx.y);
   // shared memory per weight row of a stage for its metadata (bytes), and the bytes the copies deliver
   const int meta_row = MX ? p.mbw : (p.bofs + 16 * p.mbw) / 8;
-  const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, meta_row, p.owned_max, csize, p.maxw, p.M);
+  const OwnLayout L(W, D, p.gp, GS, MP, NB, p.nbox, p.bw, meta_row, p.owned_max, csize, p.maxw, p.M, p.swz);
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -243,6 +251,19 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   QMM_TRACE_POINT(2);
 
   const typename GM::Lane ln = GM::lane_geometry(lane);
+  // Swizzled boxes (p.swz): GPB groups per 128-byte box row; this lane's words
+  // of group jj of a box start at word sw[jj] of its row (16-byte chunk index
+  // XOR the row's low three bits; rows g and g + 8 share them).  Only for
+  // groups of 4..16 words per row, where a lane's words of a group lie in one
+  // 16-byte chunk.
+  constexpr bool SWZ_OK = GW >= 4 && GW <= 16 && 32 % GW == 0;
+  constexpr int GPB = SWZ_OK ? 32 / GW : 1;
+  int sw[GPB];
+#pragma unroll
+  for (int jj = 0; jj < GPB; ++jj) {
+    const int wd = jj * GW + ln.wofs;
+    sw[jj] = (((wd >> 2) ^ (ln.g & 7)) << 2) | (wd & 3);
+  }
   const uint16_t* xrow = GM::x_row(Xs, L.rsx, ln);
   const int gpb = p.bw / GW;  // groups per weight box
 
@@ -358,6 +379,47 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       else GM::fold(meta + j, p.mbw, p.bofs, xsu + j * MP, ln.t, tmp, acc);
     };
     int j = 0;
+    if (SWZ_OK && p.swz) {
+      // whole boxes of GPB groups each, the groups' word offsets known at compile time
+      auto sgroup = [&](const uint32_t* bp, const int jj, int jg, float (&tmp)[NB][4]) {
+        uint32_t wl[GM::LW], wh[GM::LW];
+        GM::load_words(bp + sw[jj], 32, wl, wh);
+        GM::mma(wl, wh, xu + jg * GS, L.rsx, ln.tsub, tmp, ln.magic);
+      };
+      const uint32_t* wrow = reinterpret_cast<const uint32_t*>(stage) + ln.g * 32;
+      for (int b = 0; b < p.nbox; ++b) {
+        const uint32_t* bp = wrow + b * 512;
+        const int jb = b * GPB;
+        if constexpr (NB == 1 && GPB >= 4) {
+#pragma unroll
+          for (int c = 0; c < GPB; c += 4) {
+            float t0[NB][4], t1[NB][4], t2[NB][4], t3[NB][4];
+            sgroup(bp, c, jb + c, t0);
+            sgroup(bp, c + 1, jb + c + 1, t1);
+            sgroup(bp, c + 2, jb + c + 2, t2);
+            sgroup(bp, c + 3, jb + c + 3, t3);
+            fold(jb + c, t0);
+            fold(jb + c + 1, t1);
+            fold(jb + c + 2, t2);
+            fold(jb + c + 3, t3);
+          }
+        } else if constexpr (GPB >= 2) {
+#pragma unroll
+          for (int c = 0; c < GPB; c += 2) {
+            float t0[NB][4], t1[NB][4];
+            sgroup(bp, c, jb + c, t0);
+            sgroup(bp, c + 1, jb + c + 1, t1);
+            fold(jb + c, t0);
+            fold(jb + c + 1, t1);
+          }
+        } else {
+          float t0[NB][4];
+          sgroup(bp, 0, jb, t0);
+          fold(jb, t0);
+        }
+      }
+      j = p.gq;
+    }
     for (; NB == 1 && j + 3 < p.gq; j += 4) {  // four independent MMA chains
       float t0[NB][4], t1[NB][4], t2[NB][4], t3[NB][4];
       group(j, t0);

@@ -111,11 +111,15 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
   for (int kp = 1; kp <= p->gp; ++kp) {
     if (p->gp % kp != 0) continue;
     const int gq = p->gp / kp;
-    // weight boxes of whole groups, 16-byte multiples of <= 256 words: the
-    // widest (fewest copies per unit; measured to matter more than the
-    // shared-memory bank conflicts of the fragment loads)
-    int bw = 0;
-    for (int d = 1; d <= gq; ++d) {
+    // Weight boxes: 32-word (128-byte) rows copied with the 128-byte swizzle
+    // when a unit is whole such boxes and a lane's words of a group sit in one
+    // 16-byte chunk (4..16 words per group row; the fragment loads are then free of
+    // shared-memory bank conflicts); else boxes of whole groups, 16-byte
+    // multiples of <= 256 words, the widest (fewer copies per unit measured
+    // better than narrow unswizzled boxes without conflicts).
+    const bool swz = GW >= 4 && GW <= 16 && 32 % GW == 0 && (gq * GW) % 32 == 0;
+    int bw = swz ? 32 : 0;
+    for (int d = 1; !swz && d <= gq; ++d) {
       if (gq % d != 0) continue;
       const int w = d * GW;
       if (w <= 256 && w % 4 == 0) bw = w;
@@ -137,7 +141,7 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
       }
     }
     const int owned_max = (nt_max + csize - 1) / csize;
-    const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, meta_row, owned_max, csize, maxw, a.M);
+    const OwnLayout L(W, D, p->gp, GS, MP, NB, gq * GW / bw, bw, meta_row, owned_max, csize, maxw, a.M, swz ? 1 : 0);
     int total = L.total;
     if constexpr (GATHER) {
       // The union decides the tile count nt <= nt_max in the kernel, which
@@ -157,19 +161,20 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
       total = L.recv_off + static_cast<int>(slots) * csize * L.slot_bytes;
       const int x_end = L.x_off + MP * L.rsx * 2;
       if (total < x_end) total = x_end;
-      total = ((total + 15) & ~15) + gather_bytes;
+      total = ((total + 15) & ~15) + gather_bytes + (swz ? 1024 : 0);
       maxw = 0;  // the kernel finds its own
     }
     if (total > *budget) continue;
     p->kp = kp;
     p->gq = gq;
+    p->swz = swz ? 1 : 0;
     p->bw = bw;
     p->nbox = gq * GW / bw;
     p->mbw = mbw;
     p->bofs = bofs;
     p->maxw = maxw;
     p->owned_max = owned_max;
-    p->gather_off = GATHER ? total - gather_bytes : 0;
+    p->gather_off = GATHER ? total - gather_bytes - (swz ? 1024 : 0) : 0;
     *smem = total;
     found = true;
     if (nt_min * kp >= 2 * W) break;
@@ -196,7 +201,8 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(p.bw), 16u};
     const cuuint32_t estride[2] = {1u, 1u};
     if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(a.Wq), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, p.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -237,8 +243,9 @@ cudaError_t launch_own_impl(const CallArgs& a, int csize, int ctas_per_sm, int w
     if (lg != nullptr && lg[0] != '\0' && lg[0] != '0')
       std::fprintf(stderr,
                    "qmm own: grid %dx%d (clusters of %d) threads %d smem %d budget %d depth %d gp %d parts %d "
-                   "gq %d box %dx%d maxw %d owned %d\n",
-                   csize, p.ncl, csize, 32 * W, smem, budget, D, p.gp, p.kp, p.gq, p.nbox, p.bw, p.maxw, p.owned_max);
+                   "gq %d box %dx%d%s maxw %d owned %d\n",
+                   csize, p.ncl, csize, 32 * W, smem, budget, D, p.gp, p.kp, p.gq, p.nbox, p.bw, p.swz ? " swizzled" : "", p.maxw,
+                   p.owned_max);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, p.ncl, 1);
