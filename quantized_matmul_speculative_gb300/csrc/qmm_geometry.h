@@ -121,12 +121,9 @@ struct TmaLayout {
   int stage_bytes, w_bytes, meta_bytes, rsx;
   int stage_off, x_off, xs_off, part_off, recv_off, total;
   // `recv_tiles` = tiles one CTA owns in the push reduction (0 = not used),
-  // `csize` = CTAs per cluster, `recv_slots` = partials received per (owned
-  // tile, CTA): 1 when each CTA sums its warps' partials before pushing, the
-  // most warps that meet one tile when every warp pushes its own (the park
-  // area is then not used: rt = 0).
+  // `csize` = CTAs per cluster.
   __host__ __device__ TmaLayout(int pw, int gp, int gs, int mp, int stages, int rt, int slots, int mbw,
-                                int recv_tiles = 0, int csize = 1, int recv_slots = 1) {
+                                int recv_tiles = 0, int csize = 1) {
     w_bytes = 16 * pw * 4;
     meta_bytes = 2 * 16 * mbw * 2;  // scales then biases, 16 rows x mbw halves each
     stage_bytes = (w_bytes + meta_bytes + 127) & ~127;
@@ -136,7 +133,7 @@ struct TmaLayout {
     xs_off = (x_off + mp * rsx * 2 + 15) & ~15;
     part_off = (xs_off + gp * mp * 4 + 15) & ~15;
     recv_off = (part_off + rt * slots * mp * 16 * 4 + 15) & ~15;
-    total = recv_off + recv_tiles * csize * recv_slots * mp * 16 * 4;
+    total = recv_off + recv_tiles * csize * mp * 16 * 4;
   }
 };
 

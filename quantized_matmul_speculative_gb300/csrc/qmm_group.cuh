@@ -56,24 +56,19 @@ struct GroupMath {
   // by shuffles.  Loads are issued a batch at a time before any is used.  Rows
   // m >= M are not staged: an MMA output column depends only on its own
   // activation row, and the columns of rows >= M are never stored.  Every
-  // thread of [0, nthreads) must call this (warp shuffles).  `salt` (e.g. the
-  // cluster index) rotates the order of the (row, group) units, so that the
-  // many CTAs that stage the same activations at the same moment start on
-  // different lines of L2 instead of all queueing on the same ones.
+  // thread of [0, nthreads) must call this (warp shuffles).
   __device__ static void stage_x(const uint16_t* X, int K, int M, int g0, int gp, unsigned long long gp_magic,
-                                 uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads, int salt) {
-    const int nunits = M * gp;
-    const int rot = static_cast<int>((static_cast<unsigned>(salt) * 13u) % static_cast<unsigned>(nunits > 0 ? nunits : 1));
+                                 uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
     if constexpr (E8) {
-      stage_x_e8(X, K / 2, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads, rot);
+      stage_x_e8(X, K / 2, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads);
       return;
     } else if constexpr (BITS == 8) {
-      stage_x_8(X, K, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads, rot);
+      stage_x_8(X, K, M, g0, gp, gp_magic, Xs, rsx, xsum, tid, nthreads);
       return;
     }
     constexpr int CH = GS / VPW;  // tasks per unit (2..16, divides 32)
     constexpr int TQ = VPW >= 8 ? VPW / 8 : 1;  // 16-byte loads per task (8-bit codes returned above)
-    constexpr int BATCH = TQ == 1 ? 8 : 4;      // loads in flight per thread
+    constexpr int BATCH = 4;
     static_assert(32 % CH == 0, "a unit's tasks must share a warp");
     const int ntask = M * gp * CH;
     for (int base = 0; base < ntask; base += BATCH * nthreads) {
@@ -81,21 +76,19 @@ struct GroupMath {
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
         const uint16_t* src =
-            X + static_cast<int64_t>(m) * K + static_cast<int64_t>(g0 + j) * GS + (u - unit0 * CH) * VPW;
+            X + static_cast<int64_t>(m) * K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * VPW;
 #pragma unroll
         for (int q8 = 0; q8 < TQ; ++q8) v[b][q8] = (u < ntask) ? ld_nc_v4(src + 8 * q8) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int c = u - unit0 * CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
         const uint32_t* e = reinterpret_cast<const uint32_t*>(v[b]);
@@ -127,11 +120,10 @@ struct GroupMath {
   // (x0, x2), (16x0, 16x2), (x1, x3), (16x1, 16x3).  xsum holds sums of the
   // real activations.
   __device__ static void stage_x_e8(const uint16_t* X, int Kr, int M, int g0, int gp, unsigned long long gp_magic,
-                                    uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads, int rot) {
+                                    uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
     constexpr int CH = GS / VPW;  // words per row and group (8..32, divides 32)
     constexpr int GSR = GS / 2;   // real codes per group
-    constexpr int BATCH = 8;  // loads in flight per thread
-    const int nunits = M * gp;
+    constexpr int BATCH = 4;
     static_assert(32 % CH == 0, "a unit's tasks must share a warp");
     const int ntask = M * gp * CH;
     for (int base = 0; base < ntask; base += BATCH * nthreads) {
@@ -139,20 +131,18 @@ struct GroupMath {
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
         const uint16_t* src =
-            X + static_cast<int64_t>(m) * Kr + static_cast<int64_t>(g0 + j) * GSR + (u - unit0 * CH) * 4;
+            X + static_cast<int64_t>(m) * Kr + static_cast<int64_t>(g0 + j) * GSR + (u - unit * CH) * 4;
         v[b] = (u < ntask) ? ld_nc_v2(src) : make_uint2(0, 0);
       }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int c = u - unit0 * CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
         float sum = add_bf16x2_f32(v[b].y, add_bf16x2_f32(v[b].x, 0.f));
@@ -172,10 +162,9 @@ struct GroupMath {
   // stage_x for native 8-bit codes (FP8 E4M3): a task is one packed word of 4
   // codes, i.e. 4 activations of one row (8 bytes), staged as (x0, x2), (x1, x3).
   __device__ static void stage_x_8(const uint16_t* X, int K, int M, int g0, int gp, unsigned long long gp_magic,
-                                   uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads, int rot) {
+                                   uint16_t* Xs, int rsx, float* xsum, int tid, int nthreads) {
     constexpr int CH = GS / VPW;  // words per row and group
-    constexpr int BATCH = 8;  // loads in flight per thread
-    const int nunits = M * gp;
+    constexpr int BATCH = 4;
     static_assert(32 % CH == 0, "a unit's tasks must share a warp");
     const int ntask = M * gp * CH;
     for (int base = 0; base < ntask; base += BATCH * nthreads) {
@@ -183,19 +172,17 @@ struct GroupMath {
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
-        const uint16_t* src = X + static_cast<int64_t>(m) * K + static_cast<int64_t>(g0 + j) * GS + (u - unit0 * CH) * 4;
+        const uint16_t* src = X + static_cast<int64_t>(m) * K + static_cast<int64_t>(g0 + j) * GS + (u - unit * CH) * 4;
         v[b] = (u < ntask) ? ld_nc_v2(src) : make_uint2(0, 0);
       }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int u = base + b * nthreads + tid;
-        const int unit0 = u / CH;
-        const int c = u - unit0 * CH;
-        const int unit = (unit0 + rot < nunits) ? unit0 + rot : unit0 + rot - nunits;
+        const int unit = u / CH;
+        const int c = u - unit * CH;
         const int m = static_cast<int>((static_cast<unsigned long long>(unit) * gp_magic) >> 32);
         const int j = unit - m * gp;
         float sum = add_bf16x2_f32(v[b].y, add_bf16x2_f32(v[b].x, 0.f));

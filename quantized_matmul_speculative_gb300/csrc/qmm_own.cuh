@@ -245,7 +245,7 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
 
   griddep_wait();  // X may be the previous call's output; Y may still be read by it
   QMM_TRACE_POINT(1);
-  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, 32 * W, q);
+  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, 32 * W);
   __syncthreads();
   cluster_wait();  // every CTA of the cluster has initialized its barriers
   QMM_TRACE_POINT(2);

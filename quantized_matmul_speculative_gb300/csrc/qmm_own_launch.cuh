@@ -112,12 +112,13 @@ cudaError_t own_plan(const CallArgs& a, int csize, int ctas_per_sm, int wave, Ow
     if (p->gp % kp != 0) continue;
     const int gq = p->gp / kp;
     // Weight boxes: 32-word (128-byte) rows copied with the 128-byte swizzle
-    // when a unit is whole such boxes and a lane's words of a group sit in one
-    // 16-byte chunk (4..16 words per group row; the fragment loads are then free of
+    // when a unit is whole such boxes of 4 or 8 groups (4 or 8 words per group
+    // row: 4-bit g32 / g64, 2-bit g64 / g128; measured slower with 16-word
+    // groups, two per box); the fragment loads are then free of
     // shared-memory bank conflicts); else boxes of whole groups, 16-byte
     // multiples of <= 256 words, the widest (fewer copies per unit measured
     // better than narrow unswizzled boxes without conflicts).
-    const bool swz = GW >= 4 && GW <= 16 && 32 % GW == 0 && (gq * GW) % 32 == 0;
+    const bool swz = (GW == 4 || GW == 8) && (gq * GW) % 32 == 0;
     int bw = swz ? 32 : 0;
     for (int d = 1; !swz && d <= gq; ++d) {
       if (gq % d != 0) continue;

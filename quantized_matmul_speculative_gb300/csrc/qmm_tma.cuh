@@ -80,9 +80,9 @@ struct TmaParams {
   int recv_tiles; // tiles one CTA owns in the push reduction
   int mbw;        // scale/bias TMA box width in halves
   int out_f32;
-  unsigned long long wait_ns;  // limit of every bounded wait (kWaitLimitNs; shorter only under test)
+  unsigned long long wait_ns;  // limit of the waits on tile data (kWaitLimitNs; shorter only under test)
   int inject;     // test only: the first tile of cluster 0 declares 16 bytes more than its copies
-                  // deliver, so that its phase never completes and its waits give up
+                  // deliver, so that its phase never completes and the waits on it give up
   // Gathered form (rhs null: a plain call).  The tensor maps span the whole
   // stack (E*N rows); tile tau is row tile tau % tpe of the expert in union
   // slot tau / tpe; every token row (M = T) is computed against it and the
@@ -120,9 +120,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int S = p.stages;
   extern __shared__ __align__(128) unsigned char tma_smem[];
   unsigned char* smem = tma_smem;
-  // (push reduction: no park area; p.slots receive slots per owned tile and CTA)
-  const TmaLayout L(p.pw, p.gp, GS, C::MP, p.stages, p.push ? 0 : p.rt, p.slots, p.mbw, p.recv_tiles,
-                    static_cast<int>(gridDim.x), p.push ? p.slots : 1);
+  const TmaLayout L(p.pw, p.gp, GS, C::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, static_cast<int>(gridDim.x));
   const uint32_t sbase = smem_addr(smem);
   auto full_bar = [&](int s) { return sbase + 8u * s; };
   auto empty_bar = [&](int s) { return sbase + 8u * (SMAX + s); };
@@ -249,12 +247,9 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   QMM_TRACE_POINT(1);
   const int cthreads = C::CONSUMER_THREADS;
   // This CTA's K-piece of X in unpack order, with its per-group sums.
-  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, cthreads, q);
+  GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, cthreads);
   asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");  // consumers only
   QMM_TRACE_POINT(2);
-  // Push reduction: partials go to the tiles' owners as soon as a warp leaves
-  // a tile, so every CTA of the cluster must have initialized its barriers.
-  if (p.push) cluster_wait();
 
   const typename GM::Lane ln = GM::lane_geometry(lane);
   const int g = ln.g;
@@ -366,30 +361,14 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
           // slot of this warp in the tile: warps before it that meet the tile
           int first = warp;
           while (first > 0 && (first * U / W) > t0u) --first;
-          if (p.push) {
-            // Straight to the owner (CTA slot % C): this lane's fragment into
-            // receive slot (this CTA's rank, this warp's place in the tile).
-            const int slot = i - i_lo;
-            const uint32_t owner = static_cast<uint32_t>(slot % csize);
-            const int o = slot / csize;
-            const uint32_t dst =
-                sbase + static_cast<uint32_t>(L.recv_off) +
-                static_cast<uint32_t>((((o * csize + rank) * p.slots + (warp - first)) * 32 + lane) * 16 * NB);
-            const uint32_t rbar = mapa_shared(recv_bar, owner);
+          float* pt = part + ((i - i_lo) * p.slots + (warp - first)) * (C::MP * 16);
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-              st_async_v4(mapa_shared(dst + 16u * nb, owner), make_float4(acc[nb][0], acc[nb][1], acc[nb][2], acc[nb][3]),
-                          rbar);
-          } else {
-            float* pt = part + ((i - i_lo) * p.slots + (warp - first)) * (C::MP * 16);
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-              const int m = 8 * nb + 2 * t;
-              pt[m * 16 + g] = acc[nb][0];
-              pt[(m + 1) * 16 + g] = acc[nb][1];
-              pt[m * 16 + g + 8] = acc[nb][2];
-              pt[(m + 1) * 16 + g + 8] = acc[nb][3];
-            }
+          for (int nb = 0; nb < NB; ++nb) {
+            const int m = 8 * nb + 2 * t;
+            pt[m * 16 + g] = acc[nb][0];
+            pt[(m + 1) * 16 + g] = acc[nb][1];
+            pt[m * 16 + g + 8] = acc[nb][2];
+            pt[(m + 1) * 16 + g + 8] = acc[nb][3];
           }
         }
         if (!p.single) {
@@ -404,92 +383,13 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       }
     }
 
+    // Sum the partials of each tile of the round in slot order (4 elements at
+    // a time); with the push reduction, send the sum straight to the tile's
+    // owner (CTA slot % C of the cluster), else park it in slot 0.
+    asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");
     const int per_tile = p.M * 16;
     const int nslots = i_hi - i_lo;
-    if (p.push) {
-      // Owned tiles (slot % C == rank): wait for every contributor's bytes,
-      // then each lane sums its fragment over the ranks in order, each rank's
-      // contributors in warp order, and writes its part of Y.  The
-      // contributors of a tile are the warps whose unit ranges meet it; the
-      // window split is the same in every CTA of the cluster.
-      QMM_TRACE_POINT(9);
-      const int owned = (nslots > rank) ? (nslots - rank + csize - 1) / csize : 0;
-      // first contributing warp of tile `slot` and the bounds of the warps' unit ranges
-      auto tile_split = [&](int slot, int& first, int& U, int& t0u) {
-        const int w0 = (slot / p.ws) * p.ws;
-        const int w1 = (w0 + p.ws < nslots) ? w0 + p.ws : nslots;
-        U = (w1 - w0) * p.gp;
-        t0u = (slot - w0) * p.gp;
-        first = W - 1;
-        while (first > 0 && (first * U / W) > t0u) --first;
-      };
-      if (tid == 0) {
-        uint32_t bytes = 0;
-        for (int o = 0; o < owned; ++o) {
-          int first, U, t0u;
-          tile_split(o * csize + rank, first, U, t0u);
-          for (int w2 = first; w2 < W; ++w2) {
-            const int a2 = w2 * U / W, b2 = (w2 + 1) * U / W;
-            if (a2 >= t0u + p.gp) break;
-            if (a2 < b2) bytes += static_cast<uint32_t>(csize * 32 * 16 * NB);
-          }
-        }
-        mbar_arrive_expect_tx(recv_bar, bytes);
-      }
-      const float* recv = reinterpret_cast<const float*>(smem + L.recv_off);
-      for (int o = warp; o < owned; o += W) {
-        const int slot = o * csize + rank;
-        int first, U, t0u;
-        tile_split(slot, first, U, t0u);
-        mbar_wait(recv_bar, 0, kStatusTimeoutFull);  // never the test's short limit: peers still push into this CTA
-        QMM_TRACE_POINT(11);
-        float v[NB][4];
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[nb][e] = 0.f;
-        for (int r2 = 0; r2 < csize; ++r2) {
-          float sr[NB][4];
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sr[nb][e] = 0.f;
-          for (int w2 = first; w2 < W; ++w2) {
-            const int a2 = w2 * U / W, b2 = (w2 + 1) * U / W;
-            if (a2 >= t0u + p.gp) break;
-            if (a2 < b2) {
-              const float* src = recv + ((((o * csize + r2) * p.slots + (w2 - first)) * 32 + lane) * 4 * NB);
-#pragma unroll
-              for (int nb = 0; nb < NB; ++nb) {
-                const float4 x4 = *reinterpret_cast<const float4*>(src + 4 * nb);
-                sr[nb][0] += x4.x;
-                sr[nb][1] += x4.y;
-                sr[nb][2] += x4.z;
-                sr[nb][3] += x4.w;
-              }
-            }
-          }
-#pragma unroll
-          for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[nb][e] += sr[nb][e];
-        }
-        const int i = i_lo + slot;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int m = 8 * nb + 2 * t + (e & 1);
-            const int n = tile_n0(t_begin + i) + g + ((e < 2) ? 0 : 8);
-            if (m < p.M && n < p.N) store_tile(t_begin + i, m, n, v[nb][e]);
-          }
-      }
-      QMM_TRACE_POINT(6);
-      return;  // one round only
-    }
-    // Park reduction: sum the partials of each tile of the round in slot
-    // order (4 elements at a time) into its slot 0.
-    asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");
+    if (p.push) cluster_wait();  // every CTA of the cluster has initialized its barriers
     for (int e4 = tid; e4 < nslots * (per_tile / 4); e4 += cthreads) {
       const int slot = e4 / (per_tile / 4);
       const int r = (e4 - slot * (per_tile / 4)) * 4;  // m * 16 + row
@@ -514,7 +414,35 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
           v.w += x4.w;
         }
       }
-      *reinterpret_cast<float4*>(base) = v;
+      if (p.push) {
+        const uint32_t q = static_cast<uint32_t>(slot % csize);
+        const int o = slot / csize;
+        const uint32_t dst = smem_addr(smem + L.recv_off) + 4u * static_cast<uint32_t>((o * csize + rank) * C::MP * 16 + r);
+        st_async_v4(mapa_shared(dst, q), v, mapa_shared(recv_bar, q));
+      } else {
+        *reinterpret_cast<float4*>(base) = v;
+      }
+    }
+    if (p.push) {
+      // Owned tiles: slot % C == rank.  Wait for every peer's bytes, sum the
+      // C partials in rank order, write Y.
+      const int owned = (nslots > rank) ? (nslots - rank + csize - 1) / csize : 0;
+      if (tid == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(owned * csize * per_tile * 4));
+      // (never the test's short limit: peers still push into this CTA)
+      if (owned > 0) mbar_wait(recv_bar, 0, kStatusTimeoutFull);
+      const float* recv = reinterpret_cast<const float*>(smem + L.recv_off);
+      for (int e = tid; e < owned * per_tile; e += cthreads) {
+        const int o = e / per_tile;
+        const int r = e - o * per_tile;
+        float v = 0.f;
+        for (int r2 = 0; r2 < csize; ++r2) v += recv[(o * csize + r2) * C::MP * 16 + r];
+        const int i = i_lo + o * csize + rank;
+        const int m = r >> 4;
+        const int n = tile_n0(t_begin + i) + (r & 15);
+        if (n < p.N) store_tile(t_begin + i, m, n, v);
+      }
+      QMM_TRACE_POINT(6);
+      return;  // one round only
     }
     QMM_TRACE_POINT(3);
     cluster_sync_all();  // every CTA's partials of this round are complete

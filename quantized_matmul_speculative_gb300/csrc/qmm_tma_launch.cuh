@@ -77,9 +77,9 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.K = a.K;
   p.G = a.K / GS;
   p.out_f32 = a.out_f32;
-  // Test-only fault injection (host-triggered): a short wait limit and one
-  // tile whose declared bytes never all arrive; the waits on it give up and
-  // set bits of the device status word, the call still completes.
+  // Test-only fault injection (host-triggered): a short limit for the waits on
+  // tile data and one tile whose declared bytes never all arrive; those waits
+  // give up and set bits of the device status word, the call still completes.
   {
     const char* inject = std::getenv("QMM_TEST_INJECT");
     const bool short_wait = inject != nullptr && std::strcmp(inject, "short_wait") == 0 && a.rhs == nullptr;
@@ -158,15 +158,9 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   // Single shot: when every tile of a cluster fits, each gets a stage of its
   // own, all copies are issued at once and the warps split all the tiles'
   // groups evenly (one window, one round).
-  // Layout with every warp pushing its partials to the tiles' owners (no park area).
-  auto push_layout = [&](int stages_, int slots_) {
-    const int recv_tiles = (nt_max + csize - 1) / csize;
-    return TmaLayout(p.pw, p.gp, GS, Cfg::MP, stages_, 0, slots_, p.mbw, recv_tiles, csize, slots_);
-  };
   if (nt_max <= S) {
     const int sl = round_slots(nt_max, nt_max);
-    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget ||
-        push_layout(nt_max, sl).total <= budget) {
+    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget) {
       p.single = 1;
       stages = nt_max;
       ws = nt_max;
@@ -193,16 +187,18 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   p.rt = rt;
   p.slots = slots;
   p.ws = ws;
-  // One round for every cluster: every warp pushes its partial of each tile it
-  // meets straight to the tile's owner, if the receive buffer fits.
+  // One round for every cluster: reduce by pushing partials to their owners,
+  // if the receive buffer still fits.
   p.push = 0;
   p.recv_tiles = 0;
-  if (rt == nt_max && push_layout(p.stages, p.slots).total <= budget) {
-    p.push = 1;
-    p.recv_tiles = (rt + csize - 1) / csize;
+  if (rt == nt_max) {
+    const int recv_tiles = (rt + csize - 1) / csize;
+    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, recv_tiles, csize).total <= budget) {
+      p.push = 1;
+      p.recv_tiles = recv_tiles;
+    }
   }
-  int smem = p.push ? push_layout(p.stages, p.slots).total
-                    : TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw).total;
+  int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
   if (gathered) {
     p.gather_off = (smem + 15) & ~15;
     smem = p.gather_off + gather_bytes;

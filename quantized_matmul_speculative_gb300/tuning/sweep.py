@@ -25,14 +25,17 @@ sys.path.insert(0, str(ROOT))
 from quantized_matmul_speculative_gb300 import binding, build, synth, workloads  # noqa: E402
 
 
-def shapes(quick: bool):
-    """(N, K, bits, group_size, Ms) of every workload shape."""
+def shapes(quick: bool, extra_m=()):
+    """(N, K, bits, group_size, Ms) of every workload shape; `extra_m` adds M
+    values to every shape (e.g. rows above 8 on shapes whose workload stops at
+    8, so that the dispatcher has measured entries for them too)."""
     out = []
     for w in workloads.ALL:
         pairs = w.variants or ((w.bits, w.group_size),)
         for sh in w.shapes:
             for bits, gs in pairs:
                 ms = tuple(w.ms) if not quick else tuple(m for m in w.ms if m in (1, 4, 8, 16))
+                ms = tuple(sorted(set(ms) | set(extra_m)))
                 out.append((sh.N, sh.K, bits, gs, ms or (w.ms[0],)))
     # merge duplicates (same N, K, bits, gs): union of Ms
     merged = {}
@@ -92,6 +95,7 @@ def main():
     ap.add_argument("--only-n", type=int, default=None, help="sweep only shapes with this N (repeatable)",
                     action="append")
     ap.add_argument("--only-bits", type=int, default=None, help="sweep only shapes of this code width")
+    ap.add_argument("--extra-m", type=int, action="append", default=[], help="also sweep this M on every shape")
     args = ap.parse_args()
     import torch
 
@@ -102,7 +106,7 @@ def main():
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     names = binding.variant_names()
     out = open(args.out, "w")
-    for N, K, bits, gs, ms in shapes(args.quick):
+    for N, K, bits, gs, ms in shapes(args.quick, args.extra_m):
         if args.only_n and N not in args.only_n:
             continue
         if args.only_bits and bits != args.only_bits:
