@@ -354,9 +354,11 @@ __device__ __forceinline__ void store_y(void* Y, const void* R, int64_t off, flo
   }
 }
 
-// Split cluster barrier: arrive (release) now, wait (acquire) later.
+// Split cluster barrier: arrive now, wait (acquire) later.  The arrive is
+// relaxed: it only publishes mbarrier initializations, which
+// fence.mbarrier_init.release.cluster has already ordered before it.
 __device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");

@@ -185,7 +185,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int nt = t_end - t_begin;
   const int nrounds = (nt + p.rt - 1) / p.rt;
   // Push reduction: tell the cluster this CTA's barriers exist (the matching
-  // wait comes right before the first remote store).
+  // wait comes after the activations are staged).
   if (p.push) cluster_arrive();
   griddep_launch_dependents();
 
@@ -228,6 +228,7 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     if (lane == 0) {
       const int first = nt > S ? nt - S : 0;
       for (int i = first; i < nt; ++i) mbar_wait(full_bar(i % S), (i / S) & 1, kStatusTimeoutDrain, p.wait_ns);
+      QMM_TRACE_POINT(33);
     }
     __syncwarp();
     if (p.push) {
@@ -249,6 +250,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   // This CTA's K-piece of X in unpack order, with its per-group sums.
   GM::stage_x(p.X, p.K, p.M, g0, p.gp, p.gp_magic, Xs, L.rsx, xsum, tid, cthreads);
   asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");  // consumers only
+  // Push reduction: every CTA of the cluster has initialized its barriers
+  // (waited for here, long before the first remote store, while the tiles
+  // are still landing).
+  if (p.push) cluster_wait();
   QMM_TRACE_POINT(2);
 
   const typename GM::Lane ln = GM::lane_geometry(lane);
@@ -387,9 +392,10 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     // a time); with the push reduction, send the sum straight to the tile's
     // owner (CTA slot % C of the cluster), else park it in slot 0.
     asm volatile("bar.sync 1, %0;" :: "r"(cthreads) : "memory");
+    QMM_TRACE_POINT(9);
     const int per_tile = p.M * 16;
     const int nslots = i_hi - i_lo;
-    if (p.push) cluster_wait();  // every CTA of the cluster has initialized its barriers
+    QMM_TRACE_POINT(10);
     for (int e4 = tid; e4 < nslots * (per_tile / 4); e4 += cthreads) {
       const int slot = e4 / (per_tile / 4);
       const int r = (e4 - slot * (per_tile / 4)) * 4;  // m * 16 + row
@@ -429,7 +435,9 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
       const int owned = (nslots > rank) ? (nslots - rank + csize - 1) / csize : 0;
       if (tid == 0) mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(owned * csize * per_tile * 4));
       // (never the test's short limit: peers still push into this CTA)
+      QMM_TRACE_POINT(11);
       if (owned > 0) mbar_wait(recv_bar, 0, kStatusTimeoutFull);
+      QMM_TRACE_POINT(12);
       const float* recv = reinterpret_cast<const float*>(smem + L.recv_off);
       for (int e = tid; e < owned * per_tile; e += cthreads) {
         const int o = e / per_tile;
