@@ -84,6 +84,18 @@ inline bool tma_geometry(int K, int bits, int gs, int csize, int* gp, int* pw, i
   return true;
 }
 
+// First 16-row tile of cluster q when `tiles` tiles are split over ncl
+// clusters: every cluster gets floor(tiles / ncl) or one more, and the ones
+// with one more come first.  In a chain of dependent calls the clusters are
+// launched in index order as the previous call's CTAs leave, so the last
+// ones start last, with the least time before the dependency wait to stream
+// their weights: they get the lighter share.
+QMM_HD inline int cluster_tile_begin(int tiles, int ncl, int q) {
+  const int base = tiles / ncl;
+  const int rem = tiles - base * ncl;
+  return q * base + (q < rem ? q : rem);
+}
+
 // First unit of warp w when U units are split into W contiguous ranges.
 QMM_HD inline int own_unit_begin(int w, int U, int W) {
   return static_cast<int>((static_cast<long long>(w) * U) / W);

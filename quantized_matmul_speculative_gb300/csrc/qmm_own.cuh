@@ -148,8 +148,8 @@ qmm_own_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     if constexpr (GATHER) return (tau % p.tpe) * 16;
     else return tau * 16;
   };
-  const int t_begin = static_cast<int>((static_cast<int64_t>(tiles) * q) / p.ncl);
-  const int t_end = static_cast<int>((static_cast<int64_t>(tiles) * (q + 1)) / p.ncl);
+  const int t_begin = cluster_tile_begin(tiles, p.ncl, q);
+  const int t_end = cluster_tile_begin(tiles, p.ncl, q + 1);
   const int nt = t_end - t_begin;
   const int g0 = rank * p.gp;
   const int U = nt * p.kp;

@@ -137,8 +137,8 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
   const int q = static_cast<int>(blockIdx.y);
   // this cluster's tiles (computed before the barrier below, which hides the
   // 64-bit divisions; a gathered call recomputes them for its actual union)
-  int t_begin = static_cast<int>((static_cast<int64_t>(p.tiles) * q) / p.ncl);
-  int t_end = static_cast<int>((static_cast<int64_t>(p.tiles) * (q + 1)) / p.ncl);
+  int t_begin = cluster_tile_begin(p.tiles, p.ncl, q);
+  int t_end = cluster_tile_begin(p.tiles, p.ncl, q + 1);
   const int g0 = rank * p.gp;  // first group of this CTA's K-piece
 
   QMM_TRACE_POINT(0);
@@ -160,8 +160,8 @@ qmm_tma_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__
     griddep_wait();
     gl = gather_lists<C::THREADS>(p.lhs, p.rhs, p.P, p.M, p.E, reinterpret_cast<int*>(smem + p.gather_off));
     const int tiles = gl.u * p.tpe;
-    t_begin = static_cast<int>((static_cast<int64_t>(tiles) * q) / p.ncl);
-    t_end = static_cast<int>((static_cast<int64_t>(tiles) * (q + 1)) / p.ncl);
+    t_begin = cluster_tile_begin(tiles, p.ncl, q);
+    t_end = cluster_tile_begin(tiles, p.ncl, q + 1);
   }
   // first weight row (of the tensor maps) of tile tau, and its first output row within its matrix
   auto tile_row = [&](int tau) {

@@ -138,7 +138,7 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   if (ncl < 1) return cudaErrorInvalidConfiguration;
   if (ncl > p.tiles) ncl = p.tiles;
   p.ncl = ncl;
-  const int nt_max = (p.tiles + ncl - 1) / ncl;
+  const int nt_max = (p.tiles + ncl - 1) / ncl;  // tiles per cluster (cluster_tile_begin)
   const int nt_min = p.tiles / ncl;
 
   const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
