@@ -162,11 +162,11 @@ inline int tma_slots(int tiles, int gp, int w) {
 // Shared memory one CTA may use when `ctas_per_sm` share an SM of
 // `smem_per_sm` bytes: the hardware reserves 1 KB per CTA, and the rest is
 // rounded down to 8 KB so that the co-residency the occupancy calculator
-// reports is the one intended (at the exact half, two CTAs do not fit).
-// Capped at the per-block opt-in limit.
+// reports is the one intended (at the exact half, two CTAs do not fit).  A
+// CTA alone on its SM takes everything up to the per-block opt-in limit.
 inline int tma_smem_budget(int smem_per_sm, int optin, int ctas_per_sm) {
   int b = smem_per_sm / ctas_per_sm - 1024;
-  b = (b / 8192) * 8192;
+  if (ctas_per_sm > 1) b = (b / 8192) * 8192;
   return b < optin ? b : optin;
 }
 
