@@ -70,6 +70,21 @@ int main() {
            L.recv_off, L.total, L.rsx);
   }
   printf("{\"kind\":\"budget\",\"one\":%d,\"two\":%d}\n", tma_smem_budget(233472, 232448, 1), tma_smem_budget(233472, 232448, 2));
+  // cluster split: begins from 0 to tiles, non-decreasing, every cluster within one tile of
+  // the even share, the larger shares first
+  int bad_split = 0, splits = 0;
+  for (int tiles = 1; tiles <= 2400; tiles += 7) for (int ncl = 1; ncl <= 160; ++ncl) {
+    ++splits;
+    bool ok = cluster_tile_begin(tiles, ncl, 0) == 0 && cluster_tile_begin(tiles, ncl, ncl) == tiles;
+    int prev = tiles;
+    for (int q = 0; q < ncl; ++q) {
+      const int n = cluster_tile_begin(tiles, ncl, q + 1) - cluster_tile_begin(tiles, ncl, q);
+      ok = ok && n >= tiles / ncl && n <= (tiles + ncl - 1) / ncl && n <= prev;
+      prev = n;
+    }
+    bad_split += ok ? 0 : 1;
+  }
+  printf("{\"kind\":\"split\",\"checked\":%d,\"bad\":%d}\n", splits, bad_split);
   // warp-owned split: contributors of every tile against the definition
   // (warps with a non-empty range [begin(w), begin(w+1)) meeting the tile's units)
   int bad_contrib = 0, checked = 0;
@@ -170,6 +185,16 @@ def test_warp_owned_contributors(records):
 
 
 def test_budget(records):
+    """Two CTAs per SM: each gets half the SM less the 1 KB the hardware
+    reserves, rounded down to 8 KB, and two such fit; a CTA alone gets the
+    whole per-block opt-in limit."""
     b = [r for r in records if r["kind"] == "budget"][0]
-    assert b["one"] == 229376 and b["two"] == 114688
+    assert b["one"] == 232448 and b["two"] == 114688
     assert 2 * (b["two"] + 1024) <= 233472
+
+
+def test_cluster_split(records):
+    """The tiles of a call split over its clusters cover every tile once,
+    give each cluster floor or ceil of the even share, larger shares first."""
+    r = [r for r in records if r["kind"] == "split"][0]
+    assert r["checked"] > 10000 and r["bad"] == 0, r
