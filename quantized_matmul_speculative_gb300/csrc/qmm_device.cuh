@@ -74,9 +74,10 @@ __device__ __forceinline__ uint32_t bf16x2_times16(uint32_t v) {
 // value (exponent 0 lands on the bf16 subnormal m * 2^-127), and an FP8 E4M3
 // code s|eeee|mmm placed at bits 15 | 7-10 | 4-6 is exactly 2^-120 times its
 // value; one bf16x2 FMA by 2^126 or 2^120 then gives the value exactly.  A
-// word's pair i holds codes i and i + 16/b, as in unpack_pair.  An E4M3 NaN
-// code (S.1111.111) becomes a bf16 NaN: the FMA's addend is -0 for every other
-// code and a NaN for those.
+// word's pair i holds codes i and i + 16/b, as in unpack_pair (for FP8 the
+// fields move straight from their place in the word: one shift for the sign,
+// one for the rest).  An E4M3 NaN code (S.1111.111) becomes a bf16 NaN: its
+// exponent bits are completed to all ones before the FMA.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t bf16x2_scale(uint32_t v, uint32_t f2) {
   uint32_t r;
@@ -89,16 +90,15 @@ __device__ __forceinline__ uint32_t unpack_fp4_pair(uint32_t w, int i) {
   return bf16x2_scale(v, 0x7E807E80u);  // 2^126
 }
 __device__ __forceinline__ uint32_t unpack_fp8_pair(uint32_t w, int i) {
-  const uint32_t u = w >> (8 * i);
-  const uint32_t mag = u & 0x007F007Fu;
-  const uint32_t v = (mag << 4) | ((u & 0x00800080u) << 8);
-  // 1 in the low bit of a half whose magnitude bits are all ones (NaN): that
-  // half's +1 carries into bit 7 and no other half's does (magnitudes <= 0x7F).
-  const uint32_t nan1 = ((mag + 0x00010001u) >> 7) & 0x00010001u;
-  const uint32_t addend = nan1 * 0x7FC0u + 0x80008000u;  // per half: -0, or 0xFFC0 (a NaN)
-  uint32_t r;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x7B807B80u), "r"(addend));  // 2^120
-  return r;
+  // codes i and i + 2: sign bits 8i + 7 and 8i + 23 to bits 15 and 31,
+  // exponent and mantissa bits 8i .. 8i + 6 (and + 16) to bits 4..10 (20..26)
+  const uint32_t sgn = i ? w : (w << 8);
+  const uint32_t mag = (i ? (w >> 4) : (w << 4)) & 0x07F007F0u;
+  // A NaN code has all seven of them set: adding 1 at bit 4 carries into bit
+  // 11 of that half only (no other magnitude reaches it), and bits 11..14
+  // set then make the half a bf16 NaN.
+  const uint32_t nanb = (mag + 0x00100010u) & 0x08000800u;
+  return bf16x2_scale((sgn & 0x80008000u) | mag | (nanb * 15u), 0x7B807B80u);  // 2^120
 }
 // E4M3 byte -> fp32, exactly (same placement as unpack_fp8_pair); S.1111.111 is NaN.
 __device__ __forceinline__ float e4m3_to_float(uint32_t c) {
