@@ -129,6 +129,39 @@ const TableEntry kTable[] = {
 };
 constexpr int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
 
+// One measured microscaling choice: the warp-owned variant and split count
+// for an exact (format, N, K) at one M (a table of its own: an mxfp4 call and
+// an affine 4-bit g32 call of one shape have the same (bits, group)).
+struct MxEntry {
+  int format, M, N, K;
+  int variant, splits;
+};
+
+const MxEntry kMxTable[] = {
+#include "qmm_mx_table.inc"
+};
+constexpr int kMxTableSize = static_cast<int>(sizeof(kMxTable) / sizeof(kMxTable[0]));
+
+// The microscaling table's entry: exact M if measured, else the nearest
+// measured M of the same (format, N, K) that uses the same number of 8-row
+// activation tiles; -1 if the shape was not swept.
+int mx_table_lookup(int format, int M, int N, int K, int* splits) {
+  int best = -1, best_d = 1 << 30;
+  for (int i = 0; i < kMxTableSize; ++i) {
+    const MxEntry& e = kMxTable[i];
+    if (e.variant < 0 || e.format != format || e.N != N || e.K != K) continue;
+    if ((e.M <= 8) != (M <= 8)) continue;
+    const int d = e.M > M ? e.M - M : M - e.M;
+    if (d < best_d) {
+      best_d = d;
+      best = i;
+    }
+  }
+  if (best < 0) return -1;
+  *splits = kMxTable[best].splits;
+  return kMxTable[best].variant;
+}
+
 // The dispatch table in use: the compiled-in one, or the file QMM_TABLE names
 // (read once per process, in the format of qmm_dispatch_table.inc: one
 // "{M, N, K, bits, group, variant, splits}," entry per line, anything after
@@ -903,14 +936,27 @@ qmm_status qmm_small_m_mx(const void* X, const uint32_t* Wq, const uint8_t* scal
   a.gs = format == QMM_NVFP4 ? 16 : 32;
   a.out_f32 = out_dtype == QMM_OUT_F32;
   // The warp-owned family when it can plan the shape, else mma.  Variant -1:
-  // tma_own_w8_d2_2cta, or tma_own_w16_d2_1cta above 12 rows (a sweep over the
-  // warp-owned variants on 5120^2 and 8192^2 for all three formats), the first
-  // cluster size of (4, 2, 1, 8) that plans; or a forced warp-owned variant.
+  // the microscaling table's choice for a swept (format, N, K) (nearest M of
+  // the same activation-tile class), else tma_own_w8_d2_2cta, or
+  // tma_own_w16_d2_1cta above 12 rows, with the first cluster size of
+  // (4, 2, 1, 8) that plans; or a forced warp-owned variant.
   auto own_mx = [&](const VariantDesc& dd, int cc, bool plan_only) {
     return (format == QMM_MXFP4)   ? launch_own_mx<0>(a, dd, cc, st, plan_only)
            : (format == QMM_MXFP8) ? launch_own_mx<1>(a, dd, cc, st, plan_only)
                                    : launch_own_mx<2>(a, dd, cc, st, plan_only);
   };
+  if (variant < 0 && splits <= 0) {
+    int ts = 0;
+    const int tv = mx_table_lookup(format, M, N, K, &ts);
+    if (tv >= 0 && tv < kNumVariants && kVariants[tv].family == kFamilyOwn &&
+        own_mx(kVariants[tv], ts, true) == cudaSuccess) {
+      if (env_flag("QMM_LOG"))
+        std::fprintf(stderr, "qmm mx: M=%d N=%d K=%d format=%d -> %s splits=%d (table)\n", M, N, K, format,
+                     kVariants[tv].name, ts);
+      const cudaError_t e = own_mx(kVariants[tv], ts, false);
+      return e == cudaSuccess ? QMM_OK : fail_cuda(e);
+    }
+  }
   const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
   if (variant < 0 || own_forced) {
     const VariantDesc& dd = kVariants[own_forced ? variant : (M > 12 ? kDefaultOwnWide : kDefaultOwn)];

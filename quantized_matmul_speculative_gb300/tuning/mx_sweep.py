@@ -1,11 +1,12 @@
 """Time the microscaling modes (mxfp4, mxfp8, nvfp4) on the warp-owned
-variants and cluster sizes, 5120x5120 and 8192x8192, M in {1, 4, 8, 9, 12, 16}:
-the evidence for qmm_small_m_mx's default choice.  Each measurement is a CUDA
+variants and cluster sizes, 5120x5120 and 8192x8192, M in {1, 4, 8, 9, 12, 16}
+(or --ms): the evidence for qmm_small_m_mx's choices (make_table.py turns it
+into the microscaling dispatch table).  Each measurement is a CUDA
 graph of 48 calls over rotating weight copies (> 4x L2), median of 5 replays.
 One JSON object per (shape, format, M) with the four fastest choices.
 
     python -m quantized_matmul_speculative_gb300.tuning.mx_sweep --out mx_sweep.jsonl
-        [--shapes 2880x2880,5120x5120] [--with-mma]
+        [--shapes 2880x2880,5120x5120] [--with-mma] [--ms 1,2,4,8,16]
 
 --shapes replaces the two square shapes (N x K); --with-mma times the mma
 variants too.
@@ -30,6 +31,7 @@ def main():
     ap.add_argument("--out", required=True)
     ap.add_argument("--shapes", default="5120x5120,8192x8192")
     ap.add_argument("--with-mma", action="store_true")
+    ap.add_argument("--ms", default="1,4,8,9,12,16")
     args = ap.parse_args()
     shapes = [tuple(int(v) for v in sh.split("x")) for sh in args.shapes.split(",")]
     import torch
@@ -53,7 +55,7 @@ def main():
             copies = [(wq, s8)] + [(wq.clone(), s8.clone()) for _ in range(nc - 1)]
             x = torch.from_numpy(synth.make_x(1, K).view(np.int16)).cuda().view(torch.bfloat16)
             y = torch.empty((16, N), dtype=torch.bfloat16, device="cuda")
-            for M in (1, 4, 8, 9, 12, 16):
+            for M in (int(m) for m in args.ms.split(",")):
                 res = []
                 for v in own:
                     for s in (1, 2, 4, 8):

@@ -219,6 +219,28 @@ def test_repack_validates_on_the_host(lib):
         assert fn(fake, 4, 64, 4, fake, None) == 0            # in place: the layouts coincide
 
 
+def test_mx_table_names_warp_owned_choices():
+    """The compiled-in microscaling table (generated from the committed
+    mx_sweep) names warp-owned variants with valid split counts, its comments
+    agree with the variant ids, and the 5120x5120 layer the bench times has an
+    entry for every format in both activation-tile classes."""
+    inc = Path(__file__).resolve().parents[1] / "quantized_matmul_speculative_gb300" / "csrc" / "qmm_mx_table.inc"
+    names = binding.variant_names()
+    have = set()
+    for line in inc.read_text().splitlines():
+        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (-?\d+), (-?\d+)\},\s*//\s*(\S+)", line)
+        if not m:
+            continue
+        f, M, N, K, v, s = (int(m.group(i)) for i in range(1, 7))
+        assert f in (0, 1, 2) and M >= 1, line
+        assert 0 <= v < len(names) and names[v].startswith("tma_own") and 1 <= s <= 16, line
+        assert names[v] == m.group(7), f"table comment {m.group(7)} != variant {v} ({names[v]})"
+        have.add((f, N, K, M <= 8))
+    for f in (0, 1, 2):
+        for small in (True, False):
+            assert (f, 5120, 5120, small) in have, f"no entry for format {f}, 5120x5120, M<=8={small}"
+
+
 def test_dispatch_table_covers_every_workload():
     """The compiled-in table (generated from the committed sweep) names real
     variants with valid split counts, its comments agree with the variant ids,
