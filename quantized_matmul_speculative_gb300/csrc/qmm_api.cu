@@ -813,13 +813,17 @@ qmm_status qmm_gather_small_m(const void* X, const uint32_t* Wq, const void* sca
   // The warp-owned family (the default when it can plan the shape, measured
   // about twice as fast as the mma family on the 128-expert top-8 stack):
   // every token row against each expert of the union, like the tma variants,
-  // with per-warp copy rings and no reduction rounds.
+  // with per-warp copy rings and no reduction rounds.  Cluster sizes from 1
+  // up: a union of a few experts has few tiles, and splitting K over a
+  // cluster then only adds reduction (on the 128-expert top-8 gate+up stack,
+  // T = 1, 2, 4, 8: 11.7 / 14.8 / 18.5 / 31.1 us unsplit against 12.1 / 15.4 /
+  // 20.6 / 34.1 with clusters of 4).
   const bool own_forced = variant >= 0 && kVariants[variant].family == kFamilyOwn;
   if (variant < 0 && T <= 16) {
     CallArgs ao = a;
     ao.M = T;
     const VariantDesc& dd = kVariants[kDefaultOwn];
-    for (int cc : {4, 2, 1, 8}) {
+    for (int cc : {1, 2, 4, 8}) {
       if (splits > 0 && cc != splits) continue;
       const cudaError_t pe = launch_own(ao, dd, cc, st, true);
       if (pe == cudaErrorNotSupported) continue;
