@@ -118,9 +118,10 @@ qmm_status qmm_small_m_residual(const void* X, const uint32_t* Wq, const void* s
  * "dense and MoE (gather_qmm) verify" and the "expert-union cost per verify
  * row".
  * variant = -1: with T <= 16 and a shape the "tma_own" variants take (see
- * qmm_small_m_ex), the warp-owned kernel computes all T rows against each
- * expert of the union and writes the rows the entries name (then any number
- * of entries per expert is fine); otherwise the "mma" variants take each
+ * qmm_small_m_ex), the warp-owned kernel (the first cluster size of 1, 2, 4, 8
+ * that plans) computes all T rows against each expert of the union and writes
+ * the rows the entries name (then any number of entries per expert is fine);
+ * otherwise the "mma" variants take each
  * expert's own entries.  A forced "tma" or "tma_own" variant takes the first
  * way (QMM_ERR_UNSUPPORTED if it cannot), a forced "mma" variant the second.
  * splits as in qmm_small_m_ex.  The index
@@ -167,11 +168,14 @@ qmm_status qmm_from_ggml(int type, const void* blocks, int64_t N, int64_t K, uin
  * bias 7, 3 mantissa bits, exponent 0 subnormal).  Encodings: the OCP
  * microscaling format; source of the modes: "MLX quantized_matmul small-M
  * verify kernels", facts "Fix family 1" / "qmv_wide covers affine, nvfp4,
- * mxfp4, mxfp8".  variant -1: the warp-owned family when it can plan the
- * shape (K/g a multiple of the cluster size, scales 16-byte aligned, and K/g
- * a multiple of 16 or else N*K/g a multiple of 16 with K/g <= 256), else the
- * first "mma" variant; a forced "mma" or "tma_own"
- * variant is used as given, a "tma" variant returns QMM_ERR_UNSUPPORTED.
+ * mxfp4, mxfp8".  variant -1 (with splits -1): the compiled-in
+ * microscaling table's choice for a swept (format, N, K), at the nearest
+ * measured M with as many 8-row activation tiles; else the warp-owned family
+ * when it can plan the shape (K/g a multiple of the cluster size, scales
+ * 16-byte aligned, and K/g a multiple of 16 or else N*K/g a multiple of 16
+ * with K/g <= 256), else the first "mma" variant; a forced "mma" or
+ * "tma_own" variant is used as given, a "tma" variant returns
+ * QMM_ERR_UNSUPPORTED.
  * QMM_NVFP4: FP4 E2M1 codes with one FP8 E4M3 scale byte per group of 16,
  * scales uint8 [N, K/16] (a per-tensor scale, where a model has one, is left
  * to the caller).
