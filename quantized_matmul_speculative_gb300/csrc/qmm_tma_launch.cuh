@@ -139,7 +139,11 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   if (ncl > p.tiles) ncl = p.tiles;
   p.ncl = ncl;
   const int nt_max = (p.tiles + ncl - 1) / ncl;  // tiles per cluster (cluster_tile_begin)
-  const int nt_min = p.tiles / ncl;
+  // The fewest tiles a cluster can get.  A gathered call's union, known only on
+  // the device, can be anything from one expert to the largest: its clusters
+  // can get as little as one tile, and a window of fewer tiles is met by more
+  // warps (tma_slots is largest at one tile).
+  const int nt_min = gathered ? 1 : p.tiles / ncl;
 
   const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
   // Partial slots per tile for rounds of rt tiles cut into windows of ws
