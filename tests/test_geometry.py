@@ -85,6 +85,14 @@ int main() {
     bad_split += ok ? 0 : 1;
   }
   printf("{\"kind\":\"split\",\"checked\":%d,\"bad\":%d}\n", splits, bad_split);
+  // tma_slots never grows with the window's tile count (the gathered planner
+  // sizes for one-tile windows as the worst case)
+  int bad_mono = 0, mono = 0;
+  for (int w : {4, 8, 12, 16}) for (int gp = 1; gp <= 128; ++gp) for (int n = 1; n < 64; ++n) {
+    ++mono;
+    bad_mono += tma_slots(n + 1, gp, w) > tma_slots(n, gp, w) ? 1 : 0;
+  }
+  printf("{\"kind\":\"slots_mono\",\"checked\":%d,\"bad\":%d}\n", mono, bad_mono);
   // warp-owned split: contributors of every tile against the definition
   // (warps with a non-empty range [begin(w), begin(w+1)) meeting the tile's units)
   int bad_contrib = 0, checked = 0;
@@ -197,4 +205,11 @@ def test_cluster_split(records):
     """The tiles of a call split over its clusters cover every tile once,
     give each cluster floor or ceil of the even share, larger shares first."""
     r = [r for r in records if r["kind"] == "split"][0]
+    assert r["checked"] > 10000 and r["bad"] == 0, r
+
+
+def test_slots_never_grow_with_tiles(records):
+    """A window of more tiles never needs more partial-tile slots: the one-tile
+    window is the worst case the gathered planner sizes for."""
+    r = [r for r in records if r["kind"] == "slots_mono"][0]
     assert r["checked"] > 10000 and r["bad"] == 0, r
