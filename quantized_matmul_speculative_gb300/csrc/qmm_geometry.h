@@ -149,6 +149,75 @@ struct TmaLayout {
   }
 };
 
+// Launch plan of the row-stacking TMA family for clusters of csize CTAs that
+// get nt_min..nt_max tiles each: a stage per tile (single shot) when every
+// tile of a cluster fits, else a ring of up to 8 stages worked in windows of
+// half the ring, reduction rounds of rt tiles (one round preferred, stages
+// given up down to 4 for it), partial-tile slots for every window the kernel
+// forms of the smallest cluster, and the push reduction when one round covers
+// every cluster and its receive buffer still fits.  smax is the kernel's
+// most stages, w its consumer warps, budget the shared memory the layout may
+// take.  Returns false if no ring fits.
+struct TmaPlan {
+  int single, stages, ws, rt, slots, push, recv_tiles;
+};
+
+inline int tma_slots(int tiles, int gp, int w);
+
+inline bool tma_plan(int pw, int gp, int gs, int mp, int mbw, int w, int smax, int csize, int nt_max, int nt_min,
+                     int budget, TmaPlan* pl) {
+  const TmaLayout base(pw, gp, gs, mp, 0, 0, 0, mbw);
+  // partial slots per tile for rounds of rt tiles cut into windows of ws
+  // tiles: full windows and the remainders of the smallest cluster
+  auto round_slots = [&](int ws, int rt) {
+    int sl = 0;
+    for (int n : {ws < rt ? ws : rt, rt % ws, nt_min % rt % ws, (nt_min % rt ? nt_min % rt : rt) % ws}) {
+      if (n <= 0) continue;
+      const int x = tma_slots(n, gp, w);
+      sl = x > sl ? x : sl;
+    }
+    return sl;
+  };
+  int stages = 0, rt = 0, slots = 0, ws = 1, single = 0;
+  if (nt_max <= smax) {
+    const int sl = round_slots(nt_max, nt_max);
+    if (TmaLayout(pw, gp, gs, mp, nt_max, nt_max, sl, mbw).total <= budget) {
+      single = 1;
+      stages = nt_max;
+      ws = nt_max;
+      rt = nt_max;
+      slots = sl;
+    }
+  }
+  if (!single) {
+    for (stages = smax < 8 ? smax : 8; stages >= 2; --stages) {
+      ws = stages / 2 > 0 ? stages / 2 : 1;
+      const int room = budget - base.total - stages * base.stage_bytes;
+      for (rt = nt_max; rt >= 1; --rt) {
+        slots = round_slots(ws, rt);
+        if (rt * slots * mp * 16 * 4 <= room) break;
+      }
+      if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
+    }
+    if (stages < 2 || rt < 1) return false;
+  }
+  pl->single = single;
+  pl->stages = stages;
+  pl->ws = ws;
+  pl->rt = rt;
+  pl->slots = slots;
+  pl->push = 0;
+  pl->recv_tiles = 0;
+  if (rt == nt_max) {
+    const int recv_tiles = (rt + csize - 1) / csize;
+    if (TmaLayout(pw, gp, gs, mp, stages, rt, slots, mbw, recv_tiles, csize).total <= budget) {
+      pl->push = 1;
+      pl->recv_tiles = recv_tiles;
+    }
+  }
+  return true;
+}
+
 // Partial-tile slots per tile: with units = tiles * gp groups cut into w equal
 // ranges, a tile (gp units) meets at most ceil(gp / floor(units / w)) + 1
 // ranges, and never more than w.

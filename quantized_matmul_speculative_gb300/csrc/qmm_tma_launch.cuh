@@ -145,63 +145,15 @@ cudaError_t launch_tma_impl(const CallArgs& a, int csize, int ctas_per_sm, cudaS
   // warps (tma_slots is largest at one tile).
   const int nt_min = gathered ? 1 : p.tiles / ncl;
 
-  const TmaLayout base(p.pw, p.gp, GS, Cfg::MP, 0, 0, 0, p.mbw);
-  // Partial slots per tile for rounds of rt tiles cut into windows of ws
-  // tiles: full windows and the remainders of either cluster size.
-  auto round_slots = [&](int ws, int rt) {
-    int sl = 0;
-    for (int n : {ws < rt ? ws : rt, rt % ws, nt_min % rt % ws, (nt_min % rt ? nt_min % rt : rt) % ws}) {
-      if (n <= 0) continue;
-      const int x = tma_slots(n, p.gp, W);
-      sl = x > sl ? x : sl;
-    }
-    return sl;
-  };
-  int stages = 0, rt = 0, slots = 0, ws = 1;
-  p.single = 0;
-  // Single shot: when every tile of a cluster fits, each gets a stage of its
-  // own, all copies are issued at once and the warps split all the tiles'
-  // groups evenly (one window, one round).
-  if (nt_max <= S) {
-    const int sl = round_slots(nt_max, nt_max);
-    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, nt_max, nt_max, sl, p.mbw).total <= budget) {
-      p.single = 1;
-      stages = nt_max;
-      ws = nt_max;
-      rt = nt_max;
-      slots = sl;
-    }
-  }
-  if (!p.single) {
-    // Ring of up to 8 stages, work window half the ring, reduction round up
-    // to all of a cluster's tiles: prefer one round; give up stages down to 4
-    // for it.
-    for (stages = S < 8 ? S : 8; stages >= 2; --stages) {
-      ws = stages / 2 > 0 ? stages / 2 : 1;
-      const int room = budget - base.total - stages * base.stage_bytes;
-      for (rt = nt_max; rt >= 1; --rt) {
-        slots = round_slots(ws, rt);
-        if (rt * slots * Cfg::MP * 16 * 4 <= room) break;
-      }
-      if (rt >= 1 && (rt == nt_max || stages <= 4)) break;
-    }
-    if (stages < 2 || rt < 1) return cudaErrorInvalidValue;
-  }
-  p.stages = stages;
-  p.rt = rt;
-  p.slots = slots;
-  p.ws = ws;
-  // One round for every cluster: reduce by pushing partials to their owners,
-  // if the receive buffer still fits.
-  p.push = 0;
-  p.recv_tiles = 0;
-  if (rt == nt_max) {
-    const int recv_tiles = (rt + csize - 1) / csize;
-    if (TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, recv_tiles, csize).total <= budget) {
-      p.push = 1;
-      p.recv_tiles = recv_tiles;
-    }
-  }
+  TmaPlan plan;
+  if (!tma_plan(p.pw, p.gp, GS, Cfg::MP, p.mbw, W, S, csize, nt_max, nt_min, budget, &plan)) return cudaErrorInvalidValue;
+  p.single = plan.single;
+  p.stages = plan.stages;
+  p.rt = plan.rt;
+  p.slots = plan.slots;
+  p.ws = plan.ws;
+  p.push = plan.push;
+  p.recv_tiles = plan.recv_tiles;
   int smem = TmaLayout(p.pw, p.gp, GS, Cfg::MP, p.stages, p.rt, p.slots, p.mbw, p.recv_tiles, csize).total;
   if (gathered) {
     p.gather_off = (smem + 15) & ~15;

@@ -93,6 +93,47 @@ int main() {
     bad_mono += tma_slots(n + 1, gp, w) > tma_slots(n, gp, w) ? 1 : 0;
   }
   printf("{\"kind\":\"slots_mono\",\"checked\":%d,\"bad\":%d}\n", mono, bad_mono);
+  // tma_plan: every window the kernel forms gets enough partial-tile slots.  A
+  // cluster of nc tiles runs rounds of rt tiles, each cut into windows of ws;
+  // the warps meeting a tile of a window of n tiles are at most
+  // tma_slots(n, gp, w).  Plain calls: clusters of nt_min or nt_max tiles (the
+  // split gives floor or ceil); gathered calls: any count up to nt_max.  A
+  // one-tile window may be met by more warps than planned only where its
+  // extra partials stay in the round's own slot region past its last tile.
+  long plans = 0, windows_checked = 0, bad_plan = 0, spills = 0;
+  for (int gathered = 0; gathered < 2; ++gathered)
+  for (int bits : {2, 4}) for (int gs : {32, 64, 128}) for (int K : {1024, 2048, 4096, 5120, 8192, 17408})
+  for (int N : {64, 136, 1024, 1536, 4096, 5120, 7168, 8192, 24576, 34816})
+  for (int c : {1, 2, 4, 8, 16}) for (int wcfg = 0; wcfg < 4; ++wcfg) for (int mp : {8, 16}) {
+    const int w = wcfg == 0 ? 4 : (wcfg == 3 ? 16 : 8), cps = wcfg < 2 ? 2 : 1;
+    int gp = 0, pw = 0, bw = 0, nb = 0, mbw = 0;
+    if (!tma_geometry(K, bits, gs, c, &gp, &pw, &bw, &nb, &mbw)) continue;
+    const int tiles = (N + 15) / 16 * (gathered ? 8 : 1);
+    int ncl = (148 * cps) / c;
+    if (ncl > tiles) ncl = tiles;
+    const int nt_max = (tiles + ncl - 1) / ncl;
+    const int nt_min = gathered ? 1 : tiles / ncl;
+    const int budget = tma_smem_budget(233472, 232448, cps) - (gathered ? (6 * 256 + 34) * 4 : 0);
+    TmaPlan pl;
+    if (!tma_plan(pw, gp, gs, mp, mbw, w, 16, c, nt_max, nt_min, budget, &pl)) continue;
+    ++plans;
+    for (int nc = gathered ? 1 : nt_min; nc <= nt_max; ++nc) {
+      if (!gathered && nc != nt_min && nc != nt_max) continue;
+      for (int r0 = 0; r0 < nc; r0 += pl.rt) {
+        const int r1 = r0 + pl.rt < nc ? r0 + pl.rt : nc;
+        for (int w0 = r0; w0 < r1; w0 += pl.ws) {
+          const int w1 = w0 + pl.ws < r1 ? w0 + pl.ws : r1;
+          const int n = w1 - w0, need = tma_slots(n, gp, w);
+          ++windows_checked;
+          if (need <= pl.slots) continue;
+          const bool contained = n == 1 && w1 == r1 && (w1 - 1 - r0) * pl.slots + need <= pl.rt * pl.slots;
+          if (contained && !gathered) ++spills; else ++bad_plan;
+        }
+      }
+    }
+  }
+  printf("{\"kind\":\"plan\",\"plans\":%ld,\"windows\":%ld,\"bad\":%ld,\"spills\":%ld}\n", plans, windows_checked,
+         bad_plan, spills);
   // warp-owned split: contributors of every tile against the definition
   // (warps with a non-empty range [begin(w), begin(w+1)) meeting the tile's units)
   int bad_contrib = 0, checked = 0;
@@ -213,3 +254,12 @@ def test_slots_never_grow_with_tiles(records):
     window is the worst case the gathered planner sizes for."""
     r = [r for r in records if r["kind"] == "slots_mono"][0]
     assert r["checked"] > 10000 and r["bad"] == 0, r
+
+
+def test_plan_gives_every_window_its_slots(records):
+    """The row-stacking family's planner (tma_plan) gives every window the
+    kernel can form enough partial-tile slots: all windows of gathered calls
+    (any union), and all windows of plain calls except one-tile remainder
+    windows whose extra partials stay inside their round's slot region."""
+    r = [r for r in records if r["kind"] == "plan"][0]
+    assert r["plans"] > 1000 and r["windows"] > 10000 and r["bad"] == 0, r
